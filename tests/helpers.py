@@ -1,0 +1,82 @@
+"""Shared helpers for the tests: run the oracle on a seeded case, compare results."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+from paged_kv_attention_out_gb300 import workloads as W
+
+# Attention tolerance on bf16 outputs against the fp64 oracle (both must hold).
+MAX_ABS_TOL = 2e-2
+MEAN_ABS_TOL = 2e-3
+# lse is an fp32 output: its error is dominated by fp32 score accumulation.
+LSE_ABS_TOL = 2e-3
+
+
+def oracle_inputs(case: W.Case):
+    """Host inputs of a case as the oracle takes them (uint16 bf16 bits)."""
+    pool = W.bf16_bits(case.make_pool("cpu", poison=True)).reshape(case.pool_shape).copy()
+    k, v = case.new_kv("cpu")
+    q = case.q("cpu")
+    return pool, W.bf16_bits(k), W.bf16_bits(v), W.bf16_bits(q)
+
+
+def oracle_run(case: W.Case):
+    """store_kv of the case's new tokens, then its attention, all on the oracle.
+
+    Returns (o fp64, lse fp64, pool after store as uint16 bits).
+    """
+    pool, k, v, q = oracle_inputs(case)
+    oracle.kv_store(pool, case.layer, k, v, case.out_loc)
+    if case.kind == "decode":
+        o, lse = oracle.decode_attn(pool, case.layer, q, case.page_table, case.seq_lens,
+                                    case.scale, case.table_idx)
+    else:
+        o, lse = oracle.extend_attn(pool, case.layer, q, case.qo_indptr, case.page_table,
+                                    case.seq_lens, case.scale, case.table_idx)
+    return o, lse, pool
+
+
+def compare(got: np.ndarray, want: np.ndarray, max_tol=MAX_ABS_TOL, mean_tol=MEAN_ABS_TOL,
+            what="o"):
+    got = np.asarray(got, np.float64)
+    want = np.asarray(want, np.float64)
+    assert got.shape == want.shape, (got.shape, want.shape)
+    assert np.all(np.isfinite(got)), f"{what}: non-finite values in the result"
+    err = np.abs(got - want)
+    max_err = float(err.max()) if err.size else 0.0
+    mean_err = float(err.mean()) if err.size else 0.0
+    rms = float(np.sqrt((want ** 2).mean())) if want.size else 0.0
+    rel_rms = float(np.sqrt((err ** 2).mean()) / rms) if rms > 0 else 0.0
+    msg = (f"{what}: max|err| {max_err:.3e} (tol {max_tol}), mean|err| {mean_err:.3e} "
+           f"(tol {mean_tol}), rel-rms {rel_rms:.3e}")
+    assert max_err <= max_tol and mean_err <= mean_tol, msg
+    return max_err, mean_err
+
+
+def lse_compare(got, want, tol=LSE_ABS_TOL):
+    got = np.asarray(got, np.float64)
+    want = np.asarray(want, np.float64)
+    inf = np.isneginf(want)
+    assert np.array_equal(np.isneginf(got), inf), "lse: -inf positions differ"
+    if (~inf).any():
+        err = np.abs(got[~inf] - want[~inf])
+        assert err.max() <= tol, f"lse: max|err| {err.max():.3e} (tol {tol})"
+
+
+def to_bits(t: torch.Tensor) -> np.ndarray:
+    return W.bf16_bits(t)
+
+
+def bits_to_f64(bits: np.ndarray) -> np.ndarray:
+    u = bits.astype(np.uint32) << 16
+    return u.view(np.float32).astype(np.float64)
+
+
+def f64_to_bits_exact(x) -> np.ndarray:
+    """Values that are exact in bf16 -> bits (asserts exactness)."""
+    f = np.asarray(x, np.float32)
+    u = f.view(np.uint32)
+    assert np.all((u & 0xFFFF) == 0), "value is not exact in bf16"
+    return (u >> 16).astype(np.uint16)
