@@ -1,0 +1,205 @@
+/*
+ * pkv.h - C ABI of a GB300 (sm_103a) library for the paged KV-cache attention
+ * step of an LLM serving engine: store new tokens' K/V into a paged pool,
+ * then run decode or extend (chunked-prefill) attention through page tables.
+ *
+ * The operations follow the Mini-SGLang pages:
+ *  - "Code Notes: mini-sglang", Engine Layer table, BaseKVCachePool row:
+ *    the pool is ONE tensor (2, num_layers, num_pages, page_size, heads,
+ *    head_dim) (index 0 = K, 1 = V), and store_kv() writes it at out_loc
+ *    indices.
+ *  - same page, Scheduler Layer table, TableManager row: one page_table row
+ *    per request; CacheManager row: free_slots are token positions (slots).
+ *  - same page, Engine Layer table, BaseAttnBackend row: prefill and decode
+ *    are separate attention calls; Scheduler Layer table, PrefillManager row
+ *    and "Introduction", Key Features (Chunked Prefill, Radix Cache): a prompt
+ *    chunk attends over its cached, possibly shared, prefix plus itself.
+ *  - same page, Engine Layer table, GraphRunner row: decode is replayed from
+ *    CUDA graphs, so every call here is asynchronous on the given stream,
+ *    never synchronises, never allocates and never changes the current
+ *    device.
+ *
+ * Conventions for every call:
+ *  - Pointers marked "device" are device memory owned by the caller. The
+ *    library keeps no pointer after a call returns.
+ *  - bf16 tensors are row-major and contiguous unless a stride is given.
+ *    All integer tables (page_table, out_loc, seq_lens, qo_indptr,
+ *    table_idx) are int32; address arithmetic is int64 throughout.
+ *  - Layout of the pool (element offset, all int64):
+ *      ((((c * L + layer) * num_pages + page) * page_size + off) * Hkv + h) * D + d
+ *    with c = 0 for K and 1 for V. A slot is page * page_size + off.
+ *  - A page_table entry is a physical page id: key i of a row lives at page
+ *    row[i / page_size], offset i % page_size. For page_size 1 an entry is
+ *    the slot itself. Entries past a row's seq_len are never read.
+ *  - GQA: q head h reads kv head h / (Hq / Hkv).
+ *  - lse outputs are natural-log log-sum-exp of the scaled scores, fp32.
+ *  - Host-visible arguments are validated: a bad one returns
+ *    PKV_ERR_INVALID_ARG (or PKV_ERR_UNSUPPORTED for a valid but unsupported
+ *    shape) and launches nothing. A failed launch returns PKV_ERR_CUDA.
+ *    pkv_last_error() gives a one-line reason for the last failure on the
+ *    calling thread.
+ *  - Device-resident values (page_table entries, out_loc, seq_lens,
+ *    qo_indptr) are bounds-checked on the device: an out-of-range value is
+ *    skipped (its key is treated as absent, its store is dropped), never
+ *    dereferenced, and a bit is set in the device error word that
+ *    pkv_read_device_errors() returns.
+ *  - Supported: head_dim 64 or 128; Hq / Hkv = 1..8 (decode) or 1..16
+ *    (extend); any page_size >= 1; the current device must be compute
+ *    capability 10.3 (pkv_init checks it).
+ */
+#ifndef PKV_H
+#define PKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  PKV_OK = 0,
+  PKV_ERR_INVALID_ARG = 1,
+  PKV_ERR_UNSUPPORTED = 2,
+  PKV_ERR_WORKSPACE_TOO_SMALL = 3,
+  PKV_ERR_CUDA = 4
+} pkv_status;
+
+/* Bits of the device error word (pkv_read_device_errors). */
+#define PKV_DEVERR_OUT_LOC_RANGE 0x1    /* kv_store: out_loc outside the pool  */
+#define PKV_DEVERR_PAGE_RANGE 0x2       /* a page_table entry outside the pool */
+#define PKV_DEVERR_SEQ_LEN_RANGE 0x4    /* seq_len < 0 or past the row's stride */
+#define PKV_DEVERR_INDPTR 0x8           /* qo_indptr not monotone / prefix < 0 */
+#define PKV_DEVERR_TABLE_IDX_RANGE 0x10 /* table_idx negative                  */
+
+/* The KV pool (one tensor, see the layout above). base: device, bf16,
+ * 16-byte aligned. Passed by pointer; the library does not keep it. */
+typedef struct {
+  void *base;
+  int32_t num_layers;
+  int64_t num_pages;
+  int32_t page_size;
+  int32_t num_kv_heads;
+  int32_t head_dim;
+} pkv_pool;
+
+/* Checks that the current device is compute capability 10.3 and caches its
+ * SM count. PKV_ERR_UNSUPPORTED otherwise. Every other call performs the
+ * same check lazily; calling this first only moves it out of the hot path. */
+pkv_status pkv_init(void);
+
+/* Human-readable name of a status code (static string). */
+const char *pkv_status_string(pkv_status s);
+
+/* One-line reason for the last non-OK status returned on this thread
+ * (thread-local static buffer, valid until the next failing call). */
+const char *pkv_last_error(void);
+
+/*
+ * store_kv ("Code Notes: mini-sglang", Engine Layer table, BaseKVCachePool
+ * row): for i < num_tokens,
+ *   pool[0, layer, out_loc[i]] = k[i]   and   pool[1, layer, out_loc[i]] = v[i]
+ * k, v: device bf16 [num_tokens, Hkv, D], token rows kv_row_stride elements
+ * apart (>= Hkv * D, a multiple of 8), heads and dims contiguous, 16-byte
+ * aligned (so k and v may be column slices of a fused QKV output).
+ * out_loc: device int32 [num_tokens], flat slots. Two tokens with the same
+ * slot give an unspecified one of the two rows. Bits are copied unchanged.
+ */
+pkv_status pkv_kv_store(const pkv_pool *pool, int32_t layer, const void *k, const void *v,
+                        int64_t kv_row_stride, const int32_t *out_loc, int64_t num_tokens,
+                        cudaStream_t stream);
+
+/*
+ * Bytes of device workspace pkv_paged_decode_attn needs for these host-side
+ * sizes on the current device (0 when no request is split). The split plan
+ * depends only on these arguments and the device's SM count, never on
+ * device data, so the call stays graph-capturable.
+ * max_seq_len_hint: an upper bound on every seq_len of the call; it sets how
+ * finely long rows are split. A value < 1 means "no bound known" and
+ * disables splitting (correct, but one CTA per request and head group).
+ */
+size_t pkv_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                                 int32_t head_dim, int32_t max_seq_len_hint);
+
+/*
+ * Decode attention ("Code Notes: mini-sglang", Engine Layer table,
+ * BaseAttnBackend and BaseKVCachePool rows; Scheduler Layer table,
+ * TableManager row). For request b < batch and q head h < num_q_heads, with
+ * row = page_table + (table_idx ? table_idx[b] : b) * table_stride and
+ * n = seq_lens[b]:
+ *   s_i = scale * <q[b,h,:], K[key i of row, h / g, :]>    for i < n
+ *   o[b,h,:] = sum_i softmax(s)_i V[key i of row, h / g, :]
+ *   lse[b,h] = log sum_i exp(s_i)
+ * n = 0 gives o = 0 and lse = -inf. The newest token must already be in
+ * the pool (call pkv_kv_store first, on the same stream).
+ * q, o: device bf16 [batch, Hq, D], 16-byte aligned. lse: device fp32
+ * [batch, Hq] or NULL. page_table: device int32 [rows, table_stride].
+ * table_idx: device int32 [batch] or NULL (row b). seq_lens: device int32
+ * [batch]. Long rows are split across CTAs (split-KV) and merged by
+ * log-sum-exp; the partial states live in the caller's workspace (device,
+ * 256-byte aligned, >= pkv_decode_workspace_size(...) bytes, contents
+ * irrelevant on entry). A seq_len above max_seq_len_hint is still computed
+ * correctly, only with less parallelism.
+ */
+pkv_status pkv_paged_decode_attn(const pkv_pool *pool, int32_t layer, const void *q, void *o,
+                                 float *lse, const int32_t *page_table, int64_t table_stride,
+                                 const int32_t *table_idx, const int32_t *seq_lens,
+                                 int32_t batch, int32_t num_q_heads, float scale,
+                                 int32_t max_seq_len_hint, void *workspace,
+                                 size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * Extend (chunked-prefill) attention ("Code Notes: mini-sglang", Scheduler
+ * Layer table, PrefillManager row; "Introduction", Key Features, Chunked
+ * Prefill and Radix Cache). Request r < batch owns queries qo_indptr[r] ..
+ * qo_indptr[r+1]-1 of q (chunk length c_r); seq_lens[r] counts its cached
+ * prefix plus the chunk, so the prefix is p_r = seq_lens[r] - c_r and the
+ * chunk's keys are already stored (pkv_kv_store) at positions p_r .. p_r +
+ * c_r - 1 of its row. Chunk query j attends to keys 0 .. p_r + j (full
+ * prefix, causal within the chunk):
+ *   o[t,h,:], lse[t,h] = attention of q[t,h,:] over those keys (as decode).
+ * q, o: device bf16 [total_q, Hq, D], 16-byte aligned; lse: device fp32
+ * [total_q, Hq] or NULL; qo_indptr: device int32 [batch + 1], qo_indptr[0]
+ * = 0, non-decreasing, qo_indptr[batch] = total_q. Other tables as for
+ * decode. max_chunk_hint: an upper bound on every c_r, or 0 if unknown.
+ */
+pkv_status pkv_paged_extend_attn(const pkv_pool *pool, int32_t layer, const void *q,
+                                 const int32_t *qo_indptr, void *o, float *lse,
+                                 const int32_t *page_table, int64_t table_stride,
+                                 const int32_t *table_idx, const int32_t *seq_lens,
+                                 int32_t batch, int32_t total_q, int32_t num_q_heads,
+                                 float scale, int32_t max_chunk_hint, cudaStream_t stream);
+
+/*
+ * Merge of two attention states over disjoint key sets (the log-sum-exp
+ * combination split-KV decode uses internally, exported so callers can
+ * compose attention over a shared prefix with attention over a private
+ * suffix). For each row and head:
+ *   lse = log(exp(lse_a) + exp(lse_b))
+ *   o   = exp(lse_a - lse) * o_a + exp(lse_b - lse) * o_b
+ * A state with lse = -inf contributes nothing; two such states give o = 0,
+ * lse = -inf. o_a, o_b: device fp32 [rows, heads, head_dim]; lse_a, lse_b:
+ * device fp32 [rows, heads]. o_out: device [rows, heads, head_dim], bf16 if
+ * o_out_is_bf16 else fp32 (may alias o_a or o_b when fp32). lse_out: device
+ * fp32 [rows, heads] or NULL (may alias lse_a or lse_b). head_dim must be a
+ * multiple of 4 and every pointer 16-byte aligned (lse pointers 4-byte).
+ */
+pkv_status pkv_merge_lse(const float *o_a, const float *lse_a, const float *o_b,
+                         const float *lse_b, void *o_out, int32_t o_out_is_bf16,
+                         float *lse_out, int64_t rows, int32_t heads, int32_t head_dim,
+                         cudaStream_t stream);
+
+/*
+ * Reads and clears the device error word of the current device (see the
+ * PKV_DEVERR_* bits) into *flags. This call SYNCHRONISES the device: it is
+ * a debugging aid, not part of the hot path.
+ */
+pkv_status pkv_read_device_errors(uint32_t *flags);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H */

@@ -1,0 +1,482 @@
+// decode.cu - paged GQA decode attention with split-KV and a log-sum-exp merge.
+//
+// What it computes ("Code Notes: mini-sglang", Engine Layer table,
+// BaseAttnBackend / BaseKVCachePool rows; Scheduler Layer table, TableManager
+// row): for every request b and q head h, softmax attention of q[b,h] over
+// the first seq_len[b] keys of its page_table row, on kv head h / g.
+//
+// Design (HBM-bound: every K/V byte is read once, 4 flops per byte at g=4):
+//  * Grid (kv-head group, split, request). A CTA of 4 warps covers up to 4
+//    kv heads of one request over one split (a contiguous key range), so the
+//    CTA's loads of one token are one contiguous 1 KB (4 heads x 256 B) run.
+//  * Each warp streams 16-key tiles of its kv head through its own 3-stage
+//    cp.async pipeline (16-byte chunks, zero-filled past the end, slots
+//    resolved from the page table one key per lane) into XOR-swizzled shared
+//    memory. No CTA-wide barrier inside the loop.
+//  * Scores are S^T = K q^T on the m16n8k16 tensor-core MMA with keys as the
+//    M dimension and the g <= 8 q heads of the group as N: the MMA work is
+//    exact at g = 8 and the FMA pipe is left free. The bf16 probabilities go
+//    through movmatrix to become the B operand of O^T += V^T P^T (V^T from
+//    ldmatrix.trans). Online softmax runs in the log2 domain; per-thread sums
+//    are reduced across lanes only once, at the end.
+//  * Warps sharing a head, then splits, are merged by log-sum-exp: in shared
+//    memory inside the CTA, and by a small second kernel across splits (the
+//    partial states sit in the caller's workspace and are mostly L2 hits).
+//  * The split size comes from host scalars only (batch, heads, a bound on
+//    seq_len, SM count), so the call never syncs and is graph-capturable.
+#include <math.h>
+
+#include "pkv_common.cuh"
+#include "pkv_internal.h"
+
+namespace pkv {
+namespace {
+
+constexpr int kWarps = 4;
+constexpr int kThreads = kWarps * 32;
+constexpr int kTileKeys = 16;
+constexpr int kStages = 3;
+
+template <int D>
+struct DecodeSmem {
+  static constexpr int kTileBytes = kTileKeys * D * 2;  // one K (or V) tile
+  static constexpr int kStageBytes = 2 * kTileBytes;    // K + V
+  static constexpr int kWarpBytes = kStages * kStageBytes;
+  static constexpr int kTotal = kWarps * kWarpBytes;
+  // epilogue reuse of a warp's region: O^T [8][D] fp32 + m[8] + l[8]
+  static_assert(8 * D * 4 + 64 <= kWarpBytes, "epilogue does not fit");
+};
+
+struct DecodeArgs {
+  const __nv_bfloat16 *pool;
+  int64_t plane;
+  int64_t slots;
+  int32_t num_layers;
+  int32_t layer;
+  int32_t page_size;
+  int32_t hkv;
+  const __nv_bfloat16 *q;
+  __nv_bfloat16 *o;
+  float *lse;
+  const int32_t *page_table;
+  int64_t table_stride;
+  const int32_t *table_idx;
+  const int32_t *seq_lens;
+  int32_t hq;
+  int32_t group;
+  float scale_log2;
+  int32_t heads_per_cta;
+  int32_t warps_per_head;
+  int32_t chunk;
+  int32_t splits;
+  float *part_o;    // [B, Hq, splits, D]
+  float *part_lse;  // [B, Hq, splits] (natural log)
+  unsigned *err;
+};
+
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ uint32_t ld_b32(const __nv_bfloat16 *p) {
+  return *reinterpret_cast<const uint32_t *>(p);
+}
+
+// Request-level facts every CTA (and the merge kernel) derives the same way.
+struct RowInfo {
+  const int32_t *row;
+  int seq;
+  int nsplit;
+};
+
+__device__ __forceinline__ RowInfo row_info(const DecodeArgs &a, int b, bool report) {
+  RowInfo r;
+  int row_id = a.table_idx ? a.table_idx[b] : b;
+  int seq = a.seq_lens[b];
+  const int64_t max_keys = a.table_stride * a.page_size;
+  if (row_id < 0) {
+    if (report) flag_error(a.err, kErrTableIdx);
+    row_id = 0;
+    seq = 0;
+  }
+  if (seq < 0 || seq > max_keys) {
+    if (report) flag_error(a.err, kErrSeqLen);
+    seq = seq < 0 ? 0 : static_cast<int>(max_keys);
+  }
+  r.row = a.page_table + static_cast<int64_t>(row_id) * a.table_stride;
+  r.seq = seq;
+  int n = (seq + a.chunk - 1) / a.chunk;
+  r.nsplit = n < 1 ? 1 : (n > a.splits ? a.splits : n);
+  return r;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeArgs a) {
+  using S = DecodeSmem<D>;
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int split = blockIdx.y;
+  const int b = blockIdx.z;
+
+  const RowInfo ri = row_info(a, b, split == 0 && blockIdx.x == 0 && threadIdx.x == 0);
+  if (split >= ri.nsplit) return;
+  const int key_begin = split * a.chunk;
+  const int key_end = (split == ri.nsplit - 1) ? ri.seq : key_begin + a.chunk;
+
+  const int head_slot = warp % a.heads_per_cta;
+  const int sub = warp / a.heads_per_cta;
+  const int kvh = blockIdx.x * a.heads_per_cta + head_slot;
+  const int ntiles = (key_end - key_begin + kTileKeys - 1) / kTileKeys;
+  const int my_tiles = ntiles > sub ? (ntiles - sub + a.warps_per_head - 1) / a.warps_per_head : 0;
+
+  // q of the group as the MMA B operand: k = head dim, n = q head in group.
+  uint32_t bq[D / 16][2];
+  {
+    const int n = lane >> 2;
+    const int kk = (lane & 3) * 2;
+    const bool valid = n < a.group;
+    const __nv_bfloat16 *qp =
+        a.q + (static_cast<int64_t>(b) * a.hq + kvh * a.group + (valid ? n : 0)) * D;
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+      bq[ks][0] = valid ? ld_b32(qp + ks * 16 + kk) : 0u;
+      bq[ks][1] = valid ? ld_b32(qp + ks * 16 + kk + 8) : 0u;
+    }
+  }
+
+  float acc[D / 16][4];
+#pragma unroll
+  for (int mt = 0; mt < D / 16; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+
+  uint8_t *wsm = smem + warp * S::kWarpBytes;
+  const uint32_t wbase = smem_addr(wsm);
+  const int64_t slot_stride = static_cast<int64_t>(a.hkv) * D;
+  const __nv_bfloat16 *kbase =
+      a.pool + static_cast<int64_t>(a.layer) * a.plane + static_cast<int64_t>(kvh) * D;
+  const __nv_bfloat16 *vbase =
+      a.pool + (static_cast<int64_t>(a.num_layers) + a.layer) * a.plane +
+      static_cast<int64_t>(kvh) * D;
+  const int P = a.page_size;
+
+  auto issue = [&](int j, int stage) {
+    const int k0 = key_begin + (sub + j * a.warps_per_head) * kTileKeys;
+    long long slot = -1;
+    if (lane < kTileKeys) {
+      const int key = k0 + lane;
+      if (key < key_end) {
+        const int pi = (P == 1) ? key : key / P;
+        const int off = (P == 1) ? 0 : key - pi * P;
+        const long long pg = ri.row[pi];
+        const long long s = pg * P + off;
+        if (pg < 0 || s >= a.slots) {
+          flag_error(a.err, kErrPage);
+        } else {
+          slot = s;
+        }
+      }
+    }
+    constexpr int CPK = D / 8;      // 16-byte chunks per key row
+    constexpr int KPI = 32 / CPK;   // keys per warp instruction
+    const int chunk = lane % CPK;
+    const uint32_t st = wbase + stage * S::kStageBytes;
+#pragma unroll
+    for (int it = 0; it < kTileKeys / KPI; ++it) {
+      const int r = it * KPI + lane / CPK;
+      const long long s = __shfl_sync(0xffffffffu, slot, r);
+      const bool ok = s >= 0;
+      const int64_t off = ok ? s * slot_stride + chunk * 8 : 0;
+      const uint32_t dk = st + swz<D>(r, chunk);
+      cp_async_16(dk, ok ? kbase + off : a.pool, ok ? 16 : 0);
+      cp_async_16(dk + S::kTileBytes, ok ? vbase + off : a.pool, ok ? 16 : 0);
+    }
+  };
+
+#pragma unroll
+  for (int j = 0; j < kStages - 1; ++j) {
+    if (j < my_tiles) issue(j, j);
+    cp_async_commit();
+  }
+
+  const int r0 = lane >> 2;
+  for (int j = 0; j < my_tiles; ++j) {
+    const int jn = j + kStages - 1;
+    if (jn < my_tiles) issue(jn, jn % kStages);
+    cp_async_commit();
+    cp_async_wait<kStages - 1>();
+    __syncwarp();
+
+    const uint32_t kst = wbase + (j % kStages) * S::kStageBytes;
+    const uint32_t vst = kst + S::kTileBytes;
+    const int k0 = key_begin + (sub + j * a.warps_per_head) * kTileKeys;
+
+    // S^T[16 keys][8 heads] = K_tile . q^T
+    float s[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+      uint32_t a0, a1, a2, a3;
+      ldmatrix_x4(kst + swz<D>((lane & 7) + ((lane >> 3) & 1) * 8, ks * 2 + (lane >> 4)), a0,
+                  a1, a2, a3);
+      mma_bf16_16816(s, a0, a1, a2, a3, bq[ks][0], bq[ks][1]);
+    }
+    // s[0]: key r0, head n0; s[1]: key r0, head n0+1; s[2], s[3]: key r0 + 8.
+    const bool ok0 = k0 + r0 < key_end;
+    const bool ok1 = k0 + r0 + 8 < key_end;
+    s[0] = ok0 ? s[0] * a.scale_log2 : -INFINITY;
+    s[1] = ok0 ? s[1] * a.scale_log2 : -INFINITY;
+    s[2] = ok1 ? s[2] * a.scale_log2 : -INFINITY;
+    s[3] = ok1 ? s[3] * a.scale_log2 : -INFINITY;
+    float mx0 = fmaxf(s[0], s[2]);
+    float mx1 = fmaxf(s[1], s[3]);
+#pragma unroll
+    for (int x = 4; x < 32; x <<= 1) {
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, x));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, x));
+    }
+    const float mn0 = fmaxf(m0, mx0);
+    const float mn1 = fmaxf(m1, mx1);
+    const float ref0 = mn0 == -INFINITY ? 0.f : mn0;
+    const float ref1 = mn1 == -INFINITY ? 0.f : mn1;
+    const float al0 = fast_exp2(m0 - ref0);
+    const float al1 = fast_exp2(m1 - ref1);
+    const float p0 = fast_exp2(s[0] - ref0);
+    const float p1 = fast_exp2(s[1] - ref1);
+    const float p2 = fast_exp2(s[2] - ref0);
+    const float p3 = fast_exp2(s[3] - ref1);
+    l0 = l0 * al0 + (p0 + p2);
+    l1 = l1 * al1 + (p1 + p3);
+    m0 = mn0;
+    m1 = mn1;
+#pragma unroll
+    for (int mt = 0; mt < D / 16; ++mt) {
+      acc[mt][0] *= al0;
+      acc[mt][1] *= al1;
+      acc[mt][2] *= al0;
+      acc[mt][3] *= al1;
+    }
+    // P^T as the B operand (k = key, n = head): transpose the two 8x8 halves.
+    const uint32_t bp0 = movmatrix_trans(pack_bf16(p0, p1));
+    const uint32_t bp1 = movmatrix_trans(pack_bf16(p2, p3));
+#pragma unroll
+    for (int mt = 0; mt < D / 16; ++mt) {
+      uint32_t a0, a1, a2, a3;
+      ldmatrix_x4_trans(vst + swz<D>((lane & 7) + (lane >> 4) * 8, mt * 2 + ((lane >> 3) & 1)),
+                        a0, a1, a2, a3);
+      mma_bf16_16816(acc[mt], a0, a1, a2, a3, bp0, bp1);
+    }
+    __syncwarp();
+  }
+  cp_async_wait<0>();
+  __syncwarp();
+
+#pragma unroll
+  for (int x = 4; x < 32; x <<= 1) {
+    l0 += __shfl_xor_sync(0xffffffffu, l0, x);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, x);
+  }
+
+  // Per-warp state to shared memory: O^T [8 heads][D], m[8], l[8] (log2 domain).
+  float *so = reinterpret_cast<float *>(wsm);
+  float *sm_m = so + 8 * D;
+  float *sm_l = sm_m + 8;
+  const int n0 = (lane & 3) * 2;
+#pragma unroll
+  for (int mt = 0; mt < D / 16; ++mt) {
+    so[n0 * D + mt * 16 + r0] = acc[mt][0];
+    so[(n0 + 1) * D + mt * 16 + r0] = acc[mt][1];
+    so[n0 * D + mt * 16 + r0 + 8] = acc[mt][2];
+    so[(n0 + 1) * D + mt * 16 + r0 + 8] = acc[mt][3];
+  }
+  if (lane < 4) {
+    sm_m[n0] = m0;
+    sm_m[n0 + 1] = m1;
+    sm_l[n0] = l0;
+    sm_l[n0 + 1] = l1;
+  }
+  __syncthreads();
+
+  // Merge the warps that share a kv head; write the final or the partial state.
+  const bool final_out = ri.nsplit == 1;
+  const int items = a.heads_per_cta * a.group * (D / 4);
+  for (int it = threadIdx.x; it < items; it += kThreads) {
+    const int d4 = it % (D / 4);
+    const int n = (it / (D / 4)) % a.group;
+    const int hs = it / (D / 4) / a.group;
+    float M = -INFINITY;
+    for (int w = 0; w < a.warps_per_head; ++w) {
+      const float *base = reinterpret_cast<const float *>(smem + (hs + w * a.heads_per_cta) * S::kWarpBytes);
+      M = fmaxf(M, base[8 * D + n]);
+    }
+    const float ref = M == -INFINITY ? 0.f : M;
+    float L = 0.f;
+    float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int w = 0; w < a.warps_per_head; ++w) {
+      const float *base = reinterpret_cast<const float *>(smem + (hs + w * a.heads_per_cta) * S::kWarpBytes);
+      const float sc = fast_exp2(base[8 * D + n] - ref);
+      L += base[8 * D + 8 + n] * sc;
+      const float4 v = *reinterpret_cast<const float4 *>(base + n * D + d4 * 4);
+      O.x += v.x * sc;
+      O.y += v.y * sc;
+      O.z += v.z * sc;
+      O.w += v.w * sc;
+    }
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    O.x *= inv;
+    O.y *= inv;
+    O.z *= inv;
+    O.w *= inv;
+    const float lse_nat = L > 0.f ? (M + __log2f(L)) * kLn2 : -INFINITY;
+    const int h = (blockIdx.x * a.heads_per_cta + hs) * a.group + n;
+    const int64_t bh = static_cast<int64_t>(b) * a.hq + h;
+    if (final_out) {
+      uint2 packed;
+      packed.x = pack_bf16(O.x, O.y);
+      packed.y = pack_bf16(O.z, O.w);
+      *reinterpret_cast<uint2 *>(a.o + bh * D + d4 * 4) = packed;
+      if (d4 == 0 && a.lse) a.lse[bh] = lse_nat;
+    } else {
+      *reinterpret_cast<float4 *>(a.part_o + (bh * a.splits + split) * D + d4 * 4) = O;
+      if (d4 == 0) a.part_lse[bh * a.splits + split] = lse_nat;
+    }
+  }
+}
+
+// Cross-split merge: one warp per (request, q head) with more than one split.
+template <int D>
+__global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs a, int32_t batch) {
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int64_t bh = static_cast<int64_t>(blockIdx.x) * 4 + warp;
+  if (bh >= static_cast<int64_t>(batch) * a.hq) return;
+  const int b = static_cast<int>(bh / a.hq);
+  const RowInfo ri = row_info(a, b, false);
+  const int n = ri.nsplit;
+  if (n <= 1) return;
+  const float *pl = a.part_lse + bh * a.splits;
+  float M = -INFINITY;
+  for (int s = lane; s < n; s += 32) M = fmaxf(M, pl[s]);
+#pragma unroll
+  for (int x = 16; x > 0; x >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, x));
+  const float ref = M == -INFINITY ? 0.f : M;
+  float L = 0.f;
+  for (int s = lane; s < n; s += 32) L += expf(pl[s] - ref);
+#pragma unroll
+  for (int x = 16; x > 0; x >>= 1) L += __shfl_xor_sync(0xffffffffu, L, x);
+  const float inv = L > 0.f ? 1.f / L : 0.f;
+  if (lane < D / 4) {
+    float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+    const float *po = a.part_o + bh * a.splits * D + lane * 4;
+    for (int s = 0; s < n; ++s) {
+      const float w = expf(pl[s] - ref) * inv;
+      const float4 v = *reinterpret_cast<const float4 *>(po + static_cast<int64_t>(s) * D);
+      O.x += w * v.x;
+      O.y += w * v.y;
+      O.z += w * v.z;
+      O.w += w * v.w;
+    }
+    uint2 packed;
+    packed.x = pack_bf16(O.x, O.y);
+    packed.y = pack_bf16(O.z, O.w);
+    *reinterpret_cast<uint2 *>(a.o + bh * D + lane * 4) = packed;
+  }
+  if (lane == 0 && a.lse) a.lse[bh] = L > 0.f ? ref + logf(L) : -INFINITY;
+}
+
+}  // namespace
+
+DecodePlan plan_decode(int32_t batch, int32_t hq, int32_t hkv, int32_t d, int32_t max_seq_len,
+                       int32_t sm_count) {
+  (void)hq;
+  DecodePlan p{};
+  p.heads_per_cta = hkv >= kWarps ? kWarps : hkv;
+  p.warps_per_head = kWarps / p.heads_per_cta;
+  p.head_groups = hkv / p.heads_per_cta;
+  const int64_t max_seq = max_seq_len < 1 ? 1 : max_seq_len;
+  const int64_t tiles = (max_seq + kTileKeys - 1) / kTileKeys;
+  // Aim for about 16 CTAs of work per SM if every request were max_seq long,
+  // with at least 8 tiles (128 keys) per split so partial states stay a few
+  // percent of the KV bytes.
+  const int64_t units = static_cast<int64_t>(batch) * p.head_groups * tiles;
+  const int64_t target = static_cast<int64_t>(sm_count > 0 ? sm_count : 1) * 16;
+  int64_t chunk_tiles = (units + target - 1) / target;
+  if (chunk_tiles < 8) chunk_tiles = 8;
+  int64_t splits = (tiles + chunk_tiles - 1) / chunk_tiles;
+  while (splits > 65535) {
+    chunk_tiles *= 2;
+    splits = (tiles + chunk_tiles - 1) / chunk_tiles;
+  }
+  p.chunk = static_cast<int32_t>(chunk_tiles * kTileKeys);
+  p.splits = static_cast<int32_t>(splits);
+  if (p.splits > 1) {
+    const size_t rows = static_cast<size_t>(batch) * hq * p.splits;
+    const size_t o_bytes = (rows * d * sizeof(float) + 255) & ~size_t(255);
+    const size_t l_bytes = (rows * sizeof(float) + 255) & ~size_t(255);
+    p.workspace_bytes = o_bytes + l_bytes;
+  } else {
+    p.workspace_bytes = 0;
+  }
+  return p;
+}
+
+cudaError_t launch_decode(const PoolGeom &g, int32_t layer, const void *q, void *o, float *lse,
+                          const int32_t *page_table, int64_t table_stride,
+                          const int32_t *table_idx, const int32_t *seq_lens, int32_t batch,
+                          int32_t hq, float scale, const DecodePlan &plan, void *workspace,
+                          unsigned *err, cudaStream_t stream) {
+  DecodeArgs a{};
+  a.pool = static_cast<const __nv_bfloat16 *>(g.base);
+  a.plane = g.plane;
+  a.slots = g.slots;
+  a.num_layers = g.num_layers;
+  a.layer = layer;
+  a.page_size = g.page_size;
+  a.hkv = g.hkv;
+  a.q = static_cast<const __nv_bfloat16 *>(q);
+  a.o = static_cast<__nv_bfloat16 *>(o);
+  a.lse = lse;
+  a.page_table = page_table;
+  a.table_stride = table_stride;
+  a.table_idx = table_idx;
+  a.seq_lens = seq_lens;
+  a.hq = hq;
+  a.group = hq / g.hkv;
+  a.scale_log2 = scale * kLog2e;
+  a.heads_per_cta = plan.heads_per_cta;
+  a.warps_per_head = plan.warps_per_head;
+  a.chunk = plan.chunk;
+  a.splits = plan.splits;
+  a.err = err;
+  if (plan.splits > 1) {
+    const size_t rows = static_cast<size_t>(batch) * hq * plan.splits;
+    const size_t o_bytes = (rows * g.d * sizeof(float) + 255) & ~size_t(255);
+    a.part_o = static_cast<float *>(workspace);
+    a.part_lse = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + o_bytes);
+  }
+  cudaError_t e;
+  const dim3 grid(plan.head_groups, plan.splits, batch);
+  if (g.d == 128) {
+    e = cudaFuncSetAttribute(decode_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             DecodeSmem<128>::kTotal);
+    if (e != cudaSuccess) return e;
+    decode_kernel<128><<<grid, kThreads, DecodeSmem<128>::kTotal, stream>>>(a);
+  } else {
+    e = cudaFuncSetAttribute(decode_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             DecodeSmem<64>::kTotal);
+    if (e != cudaSuccess) return e;
+    decode_kernel<64><<<grid, kThreads, DecodeSmem<64>::kTotal, stream>>>(a);
+  }
+  e = cudaGetLastError();
+  if (e != cudaSuccess || plan.splits <= 1) return e;
+  const int64_t pairs = static_cast<int64_t>(batch) * hq;
+  const unsigned mblocks = static_cast<unsigned>((pairs + 3) / 4);
+  if (g.d == 128)
+    decode_merge_kernel<128><<<mblocks, 128, 0, stream>>>(a, batch);
+  else
+    decode_merge_kernel<64><<<mblocks, 128, 0, stream>>>(a, batch);
+  return cudaGetLastError();
+}
+
+}  // namespace pkv

@@ -1,0 +1,55 @@
+// pkv_internal.h - launchers shared between the C ABI (pkv_api.cu) and the
+// kernel translation units. Arguments arrive here already validated.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace pkv {
+
+// Pool geometry as the kernels use it.
+struct PoolGeom {
+  const void *base;   // bf16 pool
+  int64_t plane;      // elements of one (c, layer) plane: num_pages * page_size * Hkv * D
+  int64_t slots;      // num_pages * page_size
+  int32_t num_layers;
+  int32_t page_size;
+  int32_t hkv;
+  int32_t d;
+};
+
+struct DecodePlan {
+  int32_t heads_per_cta;   // kv heads one CTA covers
+  int32_t warps_per_head;  // warps that share one kv head's keys
+  int32_t head_groups;     // Hkv / heads_per_cta
+  int32_t chunk;           // keys per split (multiple of 16)
+  int32_t splits;          // splits per request (grid.y)
+  size_t workspace_bytes;  // 0 when splits == 1
+};
+
+DecodePlan plan_decode(int32_t batch, int32_t hq, int32_t hkv, int32_t d, int32_t max_seq_len,
+                       int32_t sm_count);
+
+cudaError_t launch_kv_store(const PoolGeom &g, int32_t layer, const void *k, const void *v,
+                            int64_t row_stride, const int32_t *out_loc, int64_t n,
+                            int32_t sm_count, unsigned *err, cudaStream_t stream);
+
+cudaError_t launch_decode(const PoolGeom &g, int32_t layer, const void *q, void *o, float *lse,
+                          const int32_t *page_table, int64_t table_stride,
+                          const int32_t *table_idx, const int32_t *seq_lens, int32_t batch,
+                          int32_t hq, float scale, const DecodePlan &plan, void *workspace,
+                          unsigned *err, cudaStream_t stream);
+
+cudaError_t launch_extend(const PoolGeom &g, int32_t layer, const void *q,
+                          const int32_t *qo_indptr, void *o, float *lse,
+                          const int32_t *page_table, int64_t table_stride,
+                          const int32_t *table_idx, const int32_t *seq_lens, int32_t batch,
+                          int32_t total_q, int32_t hq, float scale, int32_t sm_count,
+                          unsigned *err, cudaStream_t stream);
+
+cudaError_t launch_merge(const float *o_a, const float *lse_a, const float *o_b,
+                         const float *lse_b, void *o_out, bool out_bf16, float *lse_out,
+                         int64_t rows, int32_t heads, int32_t head_dim, int32_t sm_count,
+                         cudaStream_t stream);
+
+}  // namespace pkv

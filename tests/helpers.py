@@ -80,3 +80,62 @@ def f64_to_bits_exact(x) -> np.ndarray:
     u = f.view(np.uint32)
     assert np.all((u & 0xFFFF) == 0), "value is not exact in bf16"
     return (u >> 16).astype(np.uint16)
+
+
+# ---------------------------------------------------------------------------
+# GPU side: the same case through the C ABI (pkv_* bindings)
+# ---------------------------------------------------------------------------
+_BUILT = False
+
+
+def ensure_built():
+    global _BUILT
+    if not _BUILT:
+        import __graft_entry__
+        __graft_entry__.build()
+        _BUILT = True
+
+
+def gpu_inputs(case: W.Case, poison: bool = True, device="cuda"):
+    ensure_built()
+    pool = case.make_pool(device, poison=poison)
+    k, v = case.new_kv(device)
+    q = case.q(device)
+    return pool, k, v, q, case.device_tables(device)
+
+
+def gpu_attention(case: W.Case, pool, q, t, hint=None, with_lse=True, table_idx=True):
+    """Runs the case's attention call on the GPU; returns (o, lse) tensors."""
+    import paged_kv_attention_out_gb300 as pkv
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:2], dtype=torch.float32, device=q.device) if with_lse else None
+    ti = t.get("table_idx") if table_idx else None
+    if case.kind == "decode":
+        h = case.max_seq_len if hint is None else hint
+        n = pkv.pkv_decode_workspace_size(case.B, case.Hq, case.Hkv, case.D, h)
+        ws = torch.empty(max(n, 1), dtype=torch.uint8, device=q.device)
+        pkv.pkv_paged_decode_attn(pool, case.layer, q, o, lse, t["page_table"], t["seq_lens"],
+                                  case.scale, h, ws, table_idx=ti)
+    else:
+        pkv.pkv_paged_extend_attn(pool, case.layer, q, t["qo_indptr"], o, lse, t["page_table"],
+                                  t["seq_lens"], case.scale, table_idx=ti,
+                                  max_chunk_hint=case.max_chunk)
+    return o, lse
+
+
+def gpu_run(case: W.Case, poison: bool = True, hint=None):
+    """store_kv then attention on the GPU. Returns host fp64 (o, lse) and the pool."""
+    import paged_kv_attention_out_gb300 as pkv
+    pool, k, v, q, t = gpu_inputs(case, poison)
+    pkv.pkv_kv_store(pool, case.layer, k, v, t["out_loc"])
+    o, lse = gpu_attention(case, pool, q, t, hint=hint)
+    torch.cuda.synchronize()
+    return (o.float().cpu().double().numpy(), lse.cpu().double().numpy(), pool)
+
+
+def check_against_oracle(case: W.Case, hint=None):
+    o, lse, _ = gpu_run(case, hint=hint)
+    want_o, want_lse, _ = oracle_run(case)
+    compare(o, want_o)
+    lse_compare(lse, want_lse)
+    return o, lse

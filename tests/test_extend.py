@@ -1,0 +1,69 @@
+"""Paged extend (chunked-prefill) attention on the GPU against the oracle.
+
+Small cases run the whole oracle. The full-size chunked-prefill workload is
+checked on sampled chunk queries: query j of request r equals a decode over
+the first p_r + j + 1 keys of its row (a pin of the oracle), computed on a
+compact cut of that request.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from helpers import (check_against_oracle, compare, gpu_run, lse_compare, oracle_inputs)
+from paged_kv_attention_out_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("P", [1, 16])
+@pytest.mark.parametrize("Hq,Hkv", [(4, 4), (8, 2), (32, 8), (16, 2), (32, 2)])
+def test_extend_sweep(D, P, Hq, Hkv):
+    seq = [1, 17, 80, 300, 129, 64]
+    chunks = [1, 17, 65, 100, 1, 64]  # prefix 0, 0, 15, 200, 128, 0
+    case = W.random_case(51 + Hq + D + P, kind="extend", seq_lens=seq, chunk_lens=chunks,
+                         Hq=Hq, Hkv=Hkv, D=D, P=P)
+    check_against_oracle(case)
+
+
+def test_extend_with_empty_chunk_and_table_idx():
+    case = W.random_case(52, kind="extend", seq_lens=[40, 9, 260, 33],
+                         chunk_lens=[12, 0, 190, 33], Hq=8, Hkv=2, D=128, P=16,
+                         use_table_idx=True)
+    check_against_oracle(case)
+
+
+def test_extend_group_that_does_not_divide_the_tile():
+    case = W.random_case(53, kind="extend", seq_lens=[90, 200], chunk_lens=[70, 31],
+                         Hq=12, Hkv=2, D=128, P=1)
+    check_against_oracle(case)
+
+
+def test_extend_shared_prefix():
+    case = W.random_case(54, kind="extend", seq_lens=[700, 650, 600], chunk_lens=[100, 90, 80],
+                         Hq=32, Hkv=8, D=128, P=16, shared_prefix=480, group_size=3)
+    check_against_oracle(case)
+
+
+def test_chunked_prefill_full_size_sampled():
+    case = W.chunked_prefill_extend(0)
+    o, lse, _ = gpu_run(case)
+    assert np.isfinite(o).all()
+    rng = np.random.default_rng(0)
+    q_all = W.bf16_bits(case.q())
+    for r in range(case.B):
+        sub = case.compact([r])
+        pool, k, v, _ = oracle_inputs(sub)
+        oracle.kv_store(pool, 0, k, v, sub.out_loc)
+        c = int(case.qo_indptr[r + 1] - case.qo_indptr[r])
+        p = int(case.seq_lens[r]) - c
+        js = sorted({0, c - 1, *rng.integers(0, c, 3).tolist()})
+        for j in js:
+            t = int(case.qo_indptr[r]) + j
+            want_o, want_l = oracle.decode_attn(pool, 0, q_all[t:t + 1], sub.page_table,
+                                                np.array([p + j + 1], np.int32), case.scale)
+            compare(o[t:t + 1], want_o)
+            lse_compare(lse[t:t + 1], want_l)
