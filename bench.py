@@ -1,0 +1,594 @@
+#!/usr/bin/env python
+"""Benchmark of the paged KV-cache attention step on GB300 (sm_103a).
+
+One step = one pass of the decode hot path over one batch of the
+Llama-3-8B-shaped workload (64 requests, 32 q / 8 kv heads, head_dim 128,
+page_size 1, seq_len uniform in [512, 4096], a 400k-slot pool of 32
+layers): store_kv of the 64 new tokens, split-KV decode attention through
+the page table, and the cross-split log-sum-exp merge. `value` is decode
+attention KV throughput in GB/s (algorithmic bytes: every K/V byte of every
+key, the page-table entries, q and o) over whole-step device time, inputs
+resident in HBM, L2 flushed between steps. The other named workloads
+(chunked-prefill extend in TFLOP/s, long-context and radix-shared decode in
+GB/s, the tiny decode in microseconds) are measured in the same run and
+reported under "workloads".
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl pkv|reference]
+
+--impl reference times the fp64 CPU oracle (the correctness reference) on a
+bounded sample of the same workload on this machine's host cores. With
+torchrun (N > 1) every rank runs an independent replica on its own GPU
+(weak scaling); rank 0 prints the one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from paged_kv_attention_out_gb300 import workloads as W  # noqa: E402
+
+L2_FLUSH_BYTES = 320 << 20  # > 2x the 129 MB L2
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+METRIC = "paged decode attn KV GB/s"
+
+
+# ---------------------------------------------------------------------------
+# ranks (replicas only: the path has no exchange step)
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return rank, world, local
+
+
+def aggregate_ranks(elapsed_ms: float, units: float, world: int):
+    """Max step time and total units over ranks (control-plane collectives only)."""
+    if world <= 1:
+        return elapsed_ms, units
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([elapsed_ms], dtype=torch.float64, device=dev)
+    u = torch.tensor([units], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ---------------------------------------------------------------------------
+# algorithmic work
+# ---------------------------------------------------------------------------
+
+def decode_bytes(case: W.Case, unique: bool = False) -> int:
+    """Bytes decode attention must move: K and V of every key (all kv heads),
+    the page-table entries and seq_lens it reads, q in and o + lse out."""
+    kv_row = 2 * case.Hkv * case.D * 2  # K + V of one token, bytes
+    keys = len(case.referenced_slots()) if unique else int(case.seq_lens.sum())
+    table = int(((case.seq_lens + case.P - 1) // case.P).sum()) * 4 + case.B * 4
+    qo = 2 * case.B * case.Hq * case.D * 2 + case.B * case.Hq * 4
+    return keys * kv_row + table + qo
+
+
+def store_bytes(case: W.Case) -> int:
+    return case.n_new * (2 * case.Hkv * case.D * 2 * 2 + 4)
+
+
+def extend_flops(case: W.Case) -> float:
+    """4 D Hq sum_r [c_r p_r + c_r (c_r + 1) / 2]: QK^T and PV over exactly the
+    (query, key) pairs the causal rule allows."""
+    c = np.diff(case.qo_indptr).astype(np.float64)
+    p = case.seq_lens.astype(np.float64) - c
+    return 4.0 * case.D * case.Hq * float((c * p + c * (c + 1) / 2).sum())
+
+
+def extend_bytes(case: W.Case) -> int:
+    kv = int(case.seq_lens.sum()) * 2 * case.Hkv * case.D * 2
+    qo = 2 * case.total_q * case.Hq * case.D * 2 + case.total_q * case.Hq * 4
+    return kv + qo
+
+
+# ---------------------------------------------------------------------------
+# peaks and clocks
+# ---------------------------------------------------------------------------
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples, each stamped on arrival."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int | None, interval_ms: int = 50):
+        self.samples = []
+        self.proc = None
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               f"--loop-ms={interval_ms}"]
+        if gpu_index is not None:
+            cmd.insert(1, f"--id={gpu_index}")
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.monotonic(), [x.strip() for x in line.split(",")]))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float):
+        rows = [s for (t, s) in self.samples if t0 <= t <= t1 and len(s) >= 8]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        sm = [float(r[0]) for r in rows if r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[4 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+def gpu_index_for(dev: int):
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+        out = subprocess.run(["nvidia-smi", "--query-gpu=index,uuid", "--format=csv,noheader"],
+                             capture_output=True, text=True, timeout=20).stdout
+        for line in out.strip().splitlines():
+            idx, u = [x.strip() for x in line.split(",")]
+            if uuid.replace("GPU-", "") in u:
+                return int(idx)
+    except Exception:
+        pass
+    return None
+
+
+# ---------------------------------------------------------------------------
+# the pkv arm
+# ---------------------------------------------------------------------------
+
+class Workload:
+    """Device-resident inputs of one case plus the calls of one step."""
+
+    def __init__(self, case: W.Case, dev, pool_layers: int | None = None):
+        import paged_kv_attention_out_gb300 as pkv
+        self.pkv = pkv
+        self.case = case
+        if pool_layers is not None and pool_layers != case.L:
+            case.L = pool_layers
+            case.layer = min(case.layer, pool_layers - 1)
+        self.pool = case.make_pool(dev, poison=False)
+        self.k, self.v = case.new_kv(dev)
+        self.q = case.q(dev)
+        self.t = case.device_tables(dev)
+        self.o = torch.empty_like(self.q)
+        self.lse = torch.empty(self.q.shape[:2], dtype=torch.float32, device=dev)
+        self.hint = case.max_seq_len
+        self.ws = None
+        if case.kind == "decode":
+            n = pkv.pkv_decode_workspace_size(case.B, case.Hq, case.Hkv, case.D, self.hint)
+            self.ws = torch.empty(max(n, 256), dtype=torch.uint8, device=dev)
+        self.launches_per_step = None
+
+    def store(self):
+        c = self.case
+        self.pkv.pkv_kv_store(self.pool, c.layer, self.k, self.v, self.t["out_loc"])
+
+    def attention(self):
+        c, t = self.case, self.t
+        if c.kind == "decode":
+            self.pkv.pkv_paged_decode_attn(self.pool, c.layer, self.q, self.o, self.lse,
+                                           t["page_table"], t["seq_lens"], c.scale, self.hint,
+                                           self.ws, table_idx=t.get("table_idx"))
+        else:
+            self.pkv.pkv_paged_extend_attn(self.pool, c.layer, self.q, t["qo_indptr"], self.o,
+                                           self.lse, t["page_table"], t["seq_lens"], c.scale,
+                                           table_idx=t.get("table_idx"),
+                                           max_chunk_hint=c.max_chunk)
+
+    def kernels_per_step(self) -> int:
+        c = self.case
+        if c.kind == "extend":
+            return 2
+        from paged_kv_attention_out_gb300.binding import load
+        split = self.ws is not None and load().pkv_decode_workspace_size(
+            c.B, c.Hq, c.Hkv, c.D, self.hint) > 0
+        return 3 if split else 2
+
+
+def time_steps(wl: Workload, steps: int, warmup: int, flush: torch.Tensor):
+    """Per-step CUDA-event times (ms) of store + attention, and of attention alone."""
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        flush.zero_()
+        wl.store()
+        wl.attention()
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    for i in range(steps):
+        flush.zero_()
+        ev[i][0].record(stream)
+        wl.store()
+        ev[i][1].record(stream)
+        wl.attention()
+        ev[i][2].record(stream)
+    torch.cuda.synchronize()
+    step = [e[0].elapsed_time(e[2]) for e in ev]
+    attn = [e[1].elapsed_time(e[2]) for e in ev]
+    return step, attn
+
+
+def time_e2e(wl: Workload, steps: int, warmup: int, flush: torch.Tensor):
+    """Same step through the public API from pinned host buffers: H2D of the
+    step's inputs (q, new k/v, out_loc, page_table, seq_lens), the calls, and
+    D2H of the result (o, lse), all inside the timed region."""
+    c = wl.case
+    host = {
+        "q": wl.q.cpu().pin_memory(), "k": wl.k.cpu().pin_memory(),
+        "v": wl.v.cpu().pin_memory(),
+        **{n: x.cpu().pin_memory() for n, x in wl.t.items()},
+    }
+    dev = {"q": wl.q, "k": wl.k, "v": wl.v, **wl.t}
+    o_h = torch.empty(wl.o.shape, dtype=wl.o.dtype).pin_memory()
+    l_h = torch.empty(wl.lse.shape, dtype=wl.lse.dtype).pin_memory()
+    h2d = sum(x.numel() * x.element_size() for x in host.values())
+    d2h = o_h.numel() * o_h.element_size() + l_h.numel() * l_h.element_size()
+    stream = torch.cuda.current_stream()
+
+    def one():
+        for n, x in host.items():
+            dev[n].copy_(x, non_blocking=True)
+        wl.store()
+        wl.attention()
+        o_h.copy_(wl.o, non_blocking=True)
+        l_h.copy_(wl.lse, non_blocking=True)
+
+    for _ in range(warmup):
+        flush.zero_()
+        one()
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+    for i in range(steps):
+        flush.zero_()
+        ev[i][0].record(stream)
+        one()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    ms = [e[0].elapsed_time(e[1]) for e in ev]
+    del c
+    return ms, h2d, d2h
+
+
+def roofline(kind: str, work: float, ms: float, peaks, peak_src: str, traffic=None,
+             sustained: bool = False):
+    if kind == "hbm":
+        achieved = work / (ms * 1e-3) / 1e9
+        peak = peaks["hbm_gbs"]
+        unit = "GB/s"
+    else:
+        achieved = work / (ms * 1e-3) / 1e12
+        peak = peaks["bf16_tflops_sustained" if sustained else "bf16_tflops"]
+        unit = "TFLOP/s"
+    return {"bound": kind, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
+            "frac": round(achieved / peak, 4), "traffic": traffic,
+            "peak_source": f"{peak_src} ({'sustained' if sustained else 'burst'})"
+            if kind == "tensor" else peak_src}
+
+
+def cpu_baseline(case: W.Case, budget_s: float, every: int = 4):
+    """The oracle (as it stands) on a sample of the workload: every `every`-th
+    request, store_kv + decode, repeated until `budget_s` of CPU time."""
+    import oracle
+    req = list(range(0, case.B, every))
+    sub = case.compact(req)
+    pool = W.bf16_bits(sub.make_pool("cpu", poison=True)).reshape(sub.pool_shape).copy()
+    k, v = sub.new_kv("cpu")
+    kb, vb, qb = W.bf16_bits(k), W.bf16_bits(v), W.bf16_bits(sub.q("cpu"))
+    threads = oracle.max_threads()
+    reps = 0
+    t0 = time.perf_counter()
+    while True:
+        oracle.kv_store(pool, 0, kb, vb, sub.out_loc)
+        oracle.decode_attn(pool, 0, qb, sub.page_table, sub.seq_lens, sub.scale)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    gbs = decode_bytes(sub) * reps / el / 1e9
+    return {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": f"{len(req)} of {case.B} requests (every {every}th), store_kv + decode, "
+                      f"{reps} repetitions in {el:.1f} s, fp64"}, el / reps, decode_bytes(sub)
+
+
+def run_pkv(args):
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    import __graft_entry__
+    __graft_entry__.build()
+    import paged_kv_attention_out_gb300 as pkv
+    pkv.pkv_init()
+    peaks, peak_src = load_peaks()
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    # ---- main workload: Llama-3-8B-shaped decode -----------------------------
+    case = W.llama8b_decode(args.seed + rank)
+    wl = Workload(case, dev, pool_layers=args.pool_layers)
+    sampler = ClockSampler(gpu_index_for(dev.index)) if rank == 0 else None
+    barrier(world)
+    torch.cuda.synchronize()
+    t_start = time.monotonic()
+    step_ms, attn_ms = time_steps(wl, args.steps, args.warmup, flush)
+    torch.cuda.synchronize()
+    barrier(world)
+    t_end = time.monotonic()
+    # keep the GPU under the same load until clocks have been sampled for ~1.5 s
+    while time.monotonic() - t_start < 1.5 and sampler is not None:
+        time_steps(wl, 50, 0, flush)
+    t_load_end = time.monotonic()
+    if sampler:
+        sampler.stop()
+    units = decode_bytes(case)
+    total_ms = float(sum(step_ms))
+    max_ms, all_units = aggregate_ranks(total_ms, units * args.steps, world)
+    value = all_units / (max_ms * 1e-3) / 1e9
+    e2e_ms, h2d, d2h = time_e2e(wl, max(3, min(args.steps, 200)), args.warmup, flush)
+    e2e_value = units / (statistics.mean(e2e_ms) * 1e-3) / 1e9
+    kernels = wl.kernels_per_step()
+    attn_mean = statistics.mean(attn_ms)
+    main = {
+        "roofline": roofline("hbm", units, attn_mean, peaks, peak_src),
+        "attn_ms": round(attn_mean, 5),
+        "store_ms": round(statistics.mean(s - a for s, a in zip(step_ms, attn_ms)), 5),
+    }
+    main["roofline"]["kernel"] = ("pkv_paged_decode_attn: decode_kernel + decode_merge_kernel "
+                                  "(both launches inside the timed duration)")
+    main["roofline"]["traffic"] = args.decode_traffic
+    del wl
+    torch.cuda.empty_cache()
+
+    clocks = sampler.summary(t_start, t_load_end) if sampler else None
+    if clocks is not None:
+        clocks["window"] = ("timed region" if t_end - t_start >= 1.0 else
+                            "timed region + identical untimed steps to 1.5 s")
+
+    # ---- the other named workloads -----------------------------------------
+    workloads = {}
+    if rank == 0 and not args.main_only:
+        workloads = other_workloads(args, dev, peaks, peak_src, flush)
+
+    if rank != 0:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
+    cpu = None
+    if not args.no_cpu_baseline:
+        cpu, _, _ = cpu_baseline(case, args.cpu_budget)
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(max_ms / args.steps, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded counter-based N(0,1) bf16 values and seeded page tables)",
+        "config": {"workload": "llama3-8b-decode", "batch": case.B, "q_heads": case.Hq,
+                   "kv_heads": case.Hkv, "head_dim": case.D, "page_size": case.P,
+                   "seq_len": "uniform [512, 4096]", "sum_seq_len": int(case.seq_lens.sum()),
+                   "pool": f"{case.NP} slots x {case.L} layers", "seed": args.seed,
+                   "step": "kv_store + split-KV decode + split merge",
+                   "algorithmic_bytes_per_step": units, "l2": "flushed between steps",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": main["roofline"],
+        "cpu_baseline": cpu,
+        "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h,
+                "ms_per_step": round(statistics.mean(e2e_ms), 5)},
+        "gpu_launches": kernels * args.steps,
+        "clocks": clocks,
+        "detail": {"decode_call_ms": main["attn_ms"], "kv_store_ms": main["store_ms"],
+                   "kernels_per_step": kernels},
+        "workloads": workloads,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def _measure(wl: Workload, steps: int, warmup: int, flush):
+    step_ms, attn_ms = time_steps(wl, steps, warmup, flush)
+    return statistics.mean(step_ms), statistics.mean(attn_ms)
+
+
+def other_workloads(args, dev, peaks, peak_src, flush):
+    out = {}
+    steps = max(5, min(args.steps, 100))
+    warm = max(3, args.warmup)
+    # chunked-prefill extend
+    case = W.chunked_prefill_extend(args.seed)
+    wl = Workload(case, dev)
+    st, at = _measure(wl, steps, warm, flush)
+    fl = extend_flops(case)
+    out["chunked-prefill-extend"] = {
+        "metric": "extend attn TFLOP/s", "value": round(fl / (at * 1e-3) / 1e12, 2),
+        "unit": "TFLOP/s", "ms_attention": round(at, 4), "ms_step_with_store": round(st, 4),
+        "flops": fl, "tokens_per_s": round(case.total_q / (st * 1e-3), 1),
+        "roofline": {**roofline("tensor", fl, at, peaks, peak_src),
+                     "kernel": "extend_kernel", "traffic": args.extend_traffic}}
+    del wl
+    torch.cuda.empty_cache()
+    # long-context decode (page_size 16, split-KV)
+    case = W.long_context_decode(args.seed)
+    wl = Workload(case, dev)
+    st, at = _measure(wl, steps, warm, flush)
+    by = decode_bytes(case)
+    out["long-context-decode"] = {
+        "metric": METRIC, "value": round(by / (at * 1e-3) / 1e9, 2), "unit": "GB/s",
+        "ms_attention": round(at, 4), "ms_step_with_store": round(st, 4),
+        "algorithmic_bytes": by, "tokens_per_s": round(case.B / (st * 1e-3), 1),
+        "roofline": {**roofline("hbm", by, at, peaks, peak_src),
+                     "kernel": "decode_kernel + decode_merge_kernel"}}
+    del wl
+    torch.cuda.empty_cache()
+    # radix-shared-prefix decode: unique bytes (roofline) and logical bytes
+    case = W.radix_shared_decode(args.seed)
+    wl = Workload(case, dev)
+    st, at = _measure(wl, steps, warm, flush)
+    uniq, logical = decode_bytes(case, unique=True), decode_bytes(case)
+    out["radix-shared-decode"] = {
+        "metric": METRIC + " (unique bytes)", "value": round(uniq / (at * 1e-3) / 1e9, 2),
+        "unit": "GB/s", "logical_gbs": round(logical / (at * 1e-3) / 1e9, 2),
+        "ms_attention": round(at, 4), "ms_step_with_store": round(st, 4),
+        "unique_bytes": uniq, "logical_bytes": logical,
+        "roofline": {**roofline("hbm", uniq, at, peaks, peak_src),
+                     "kernel": "decode_kernel + decode_merge_kernel"}}
+    del wl
+    torch.cuda.empty_cache()
+    # tiny decode: latency
+    case = W.tiny_decode(args.seed)
+    wl = Workload(case, dev)
+    st, at = _measure(wl, steps, warm, flush)
+    out["tiny-decode"] = {"metric": "step latency", "value": round(st * 1e3, 2), "unit": "us",
+                          "attention_us": round(at * 1e3, 2)}
+    del wl
+    torch.cuda.empty_cache()
+    return out
+
+
+# ---------------------------------------------------------------------------
+# the reference arm: the fp64 CPU oracle on a bounded sample
+# ---------------------------------------------------------------------------
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    case = W.llama8b_decode(args.seed)
+    every = 8
+    req = list(range(0, case.B, every))
+    sub = case.compact(req)
+    pool = W.bf16_bits(sub.make_pool("cpu", poison=True)).reshape(sub.pool_shape).copy()
+    k, v = sub.new_kv("cpu")
+    kb, vb, qb = W.bf16_bits(k), W.bf16_bits(v), W.bf16_bits(sub.q("cpu"))
+
+    def step():
+        oracle.kv_store(pool, 0, kb, vb, sub.out_loc)
+        oracle.decode_attn(pool, 0, qb, sub.page_table, sub.seq_lens, sub.scale)
+
+    for _ in range(args.warmup):
+        step()
+    ts = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        step()
+        ts.append(time.perf_counter() - t0)
+    units = decode_bytes(sub)
+    value = units / statistics.mean(ts) / 1e9
+    sample = (f"{len(req)} of {case.B} requests (every {every}th) per step, "
+              f"store_kv + decode in fp64")
+    line = {
+        "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(statistics.mean(ts) * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (same seeded generator as the pkv arm)",
+        "config": {"workload": "llama3-8b-decode", "batch": case.B, "q_heads": case.Hq,
+                   "kv_heads": case.Hkv, "head_dim": case.D, "page_size": case.P,
+                   "seed": args.seed, "sample": sample, "algorithmic_bytes_per_step": units},
+        "impl": "reference",
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s",
+                         "cores": oracle.max_threads(), "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["pkv", "reference"], default="pkv")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--main-only", action="store_true",
+                    help="skip the other named workloads")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=12.0,
+                    help="seconds of oracle time for cpu_baseline")
+    ap.add_argument("--pool-layers", type=int, default=None,
+                    help="allocate the pool with this many layers (same attended data)")
+    ap.add_argument("--decode-traffic", type=float, default=None,
+                    help="ncu dram bytes per decode call, from a capture of this kernel")
+    ap.add_argument("--extend-traffic", type=float, default=None,
+                    help="ncu dram bytes per extend call, from a capture of this kernel")
+    a = ap.parse_args(argv)
+    if a.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if a.steps < 1:
+        ap.error("--steps must be >= 1")
+    return a
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_pkv(args)
+
+
+if __name__ == "__main__":
+    main()
