@@ -150,6 +150,41 @@ pkv_status pkv_paged_decode_attn(const pkv_pool *pool, int32_t layer, const void
                                  int32_t max_seq_len_hint, void *workspace,
                                  size_t workspace_bytes, cudaStream_t stream);
 
+/* Size of the library-owned scratch used by pkv_paged_decode_attn_noalloc. */
+#define PKV_NOALLOC_SCRATCH_BYTES (64u << 20)
+
+/*
+ * Decode attention that allocates nothing and takes no workspace. The pages
+ * have no counterpart to this call: it exists for callers that cannot
+ * allocate device memory or hand the library a workspace, such as a plugin
+ * running inside a host framework that owns all device memory and gives the
+ * plugin no allocation hook, or a serving loop that must never call
+ * cudaMalloc because it can synchronise the device and can fail with
+ * out-of-memory in the middle of a step.
+ *
+ * Same arguments and results as pkv_paged_decode_attn, minus the workspace:
+ * the split-KV partial states go to a fixed scratch array in device memory
+ * that the library owns (PKV_NOALLOC_SCRATCH_BYTES = 64 MiB, held by every
+ * GPU that loads the library until the process exits).
+ *  - If the split plan for these sizes needs more than that
+ *    (pkv_decode_workspace_size(...) > PKV_NOALLOC_SCRATCH_BYTES), the call
+ *    returns PKV_ERR_WORKSPACE_TOO_SMALL and launches nothing; lower batch
+ *    or max_seq_len_hint, or use pkv_paged_decode_attn.
+ *  - The first call on a device looks up the scratch array's device address
+ *    (cudaGetSymbolAddress, with that device current). Make that first call
+ *    before any stream capture begins.
+ *  - Every call on a device shares the one array and it keeps whatever the
+ *    last call left; nothing in it needs to start at zero. Calls whose
+ *    kernels can overlap on the GPU (different streams without ordering
+ *    between them) race on the array: order them on one stream.
+ */
+pkv_status pkv_paged_decode_attn_noalloc(const pkv_pool *pool, int32_t layer, const void *q,
+                                         void *o, float *lse, const int32_t *page_table,
+                                         int64_t table_stride, const int32_t *table_idx,
+                                         const int32_t *seq_lens, int32_t batch,
+                                         int32_t num_q_heads, float scale,
+                                         int32_t max_seq_len_hint, cudaStream_t stream);
+
 /*
  * Extend (chunked-prefill) attention ("Code Notes: mini-sglang", Scheduler
  * Layer table, PrefillManager row; "Introduction", Key Features, Chunked

@@ -5,5 +5,6 @@ behind the C ABI of include/pkv.h. This package holds the ctypes binding
 synthetic-input generator used by the tests and the benchmark.
 """
 from .binding import (PkvError, pkv_decode_workspace_size, pkv_init, pkv_kv_store,  # noqa: F401
-                      pkv_merge_lse, pkv_paged_decode_attn, pkv_paged_extend_attn,
+                      pkv_merge_lse, pkv_paged_decode_attn, pkv_paged_decode_attn_noalloc,
+                      pkv_paged_extend_attn,
                       pkv_read_device_errors)

@@ -66,6 +66,10 @@ def load() -> ctypes.CDLL:
     L.pkv_paged_decode_attn.argtypes = [pool_p, _c_int32, _p, _p, _p, _p, _c_int64, _p, _p,
                                         _c_int32, _c_int32, ctypes.c_float, _c_int32, _p,
                                         ctypes.c_size_t, _p]
+    L.pkv_paged_decode_attn_noalloc.restype = ctypes.c_int
+    L.pkv_paged_decode_attn_noalloc.argtypes = [pool_p, _c_int32, _p, _p, _p, _p, _c_int64, _p,
+                                                _p, _c_int32, _c_int32, ctypes.c_float,
+                                                _c_int32, _p]
     L.pkv_paged_extend_attn.restype = ctypes.c_int
     L.pkv_paged_extend_attn.argtypes = [pool_p, _c_int32, _p, _p, _p, _p, _p, _c_int64, _p, _p,
                                         _c_int32, _c_int32, _c_int32, ctypes.c_float,
@@ -171,6 +175,36 @@ def pkv_paged_decode_attn(pool, layer: int, q, o, lse, page_table, seq_lens, sca
         ctypes.byref(ps), int(layer), _ptr(q), _ptr(o), _ptr(lse), _ptr(page_table),
         page_table.shape[1], _ptr(table_idx), _ptr(seq_lens), B, Hq, float(scale),
         int(max_seq_len_hint), _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def pkv_paged_decode_attn_noalloc(pool, layer: int, q, o, lse, page_table, seq_lens,
+                                  scale: float, max_seq_len_hint: int, table_idx=None,
+                                  stream=None) -> None:
+    """Decode attention with no workspace, for callers that cannot allocate.
+
+    The split-KV scratch is a fixed library-owned device array (64 MiB), so
+    nothing is allocated; calls whose kernels overlap on the GPU race on it.
+    """
+    ps = pool_struct(pool)
+    _want(q, torch.bfloat16, "q", 3)
+    _want(o, torch.bfloat16, "o", 3)
+    _contig(q, "q")
+    _contig(o, "o")
+    _want(page_table, torch.int32, "page_table", 2)
+    _contig(page_table, "page_table")
+    _want(seq_lens, torch.int32, "seq_lens", 1)
+    B, Hq, D = q.shape
+    if o.shape != q.shape or seq_lens.shape[0] != B:
+        raise ValueError("o must match q and seq_lens must have batch entries")
+    if lse is not None:
+        _want(lse, torch.float32, "lse", 2)
+        _contig(lse, "lse")
+    if table_idx is not None:
+        _want(table_idx, torch.int32, "table_idx", 1)
+    _check(load().pkv_paged_decode_attn_noalloc(
+        ctypes.byref(ps), int(layer), _ptr(q), _ptr(o), _ptr(lse), _ptr(page_table),
+        page_table.shape[1], _ptr(table_idx), _ptr(seq_lens), B, Hq, float(scale),
+        int(max_seq_len_hint), _stream(stream)))
 
 
 def pkv_paged_extend_attn(pool, layer: int, q, qo_indptr, o, lse, page_table, seq_lens,

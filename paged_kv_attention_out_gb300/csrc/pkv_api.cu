@@ -104,6 +104,16 @@ int32_t effective_hint(int32_t hint) { return hint < 1 ? 1 : hint; }
 
 }  // namespace
 
+namespace pkv {
+pkv_status fail_status(pkv_status s, const char *fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof g_last_error, fmt, ap);
+  va_end(ap);
+  return s;
+}
+}  // namespace pkv
+
 extern "C" {
 
 pkv_status pkv_init(void) {

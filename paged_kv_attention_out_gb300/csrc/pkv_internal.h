@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "pkv.h"
+
 namespace pkv {
 
 // Pool geometry as the kernels use it.
@@ -51,5 +53,8 @@ cudaError_t launch_merge(const float *o_a, const float *lse_a, const float *o_b,
                          const float *lse_b, void *o_out, bool out_bf16, float *lse_out,
                          int64_t rows, int32_t heads, int32_t head_dim, int32_t sm_count,
                          cudaStream_t stream);
+
+// Records a one-line reason for pkv_last_error() and returns s.
+pkv_status fail_status(pkv_status s, const char *fmt, ...);
 
 }  // namespace pkv

@@ -1,0 +1,73 @@
+"""pkv_paged_decode_attn_noalloc: decode attention that allocates nothing.
+
+Some callers cannot allocate device memory or hand the library a
+workspace: a plugin inside a host framework that owns all device memory and
+offers no allocation hook, or a serving loop that must never call cudaMalloc
+because it can synchronise the device and fail with out-of-memory mid-step.
+For them the library keeps the split-KV scratch in a fixed device array of
+its own. These tests call that entry point through the C ABI and check it
+against pkv_paged_decode_attn with a caller workspace, on two calls in a row
+(the second call finds the first call's leftovers in the shared scratch),
+and check that a plan larger than the array is refused.
+"""
+from __future__ import annotations
+
+import pytest
+import torch
+
+from helpers import (compare, ensure_built, gpu_attention, gpu_inputs, lse_compare)
+from paged_kv_attention_out_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+SCRATCH_BYTES = 64 << 20  # PKV_NOALLOC_SCRATCH_BYTES in include/pkv.h
+
+
+def _noalloc_vs_workspace(case):
+    import paged_kv_attention_out_gb300 as pkv
+    pool, k, v, q, t = gpu_inputs(case)
+    pkv.pkv_kv_store(pool, case.layer, k, v, t["out_loc"])
+    need = pkv.pkv_decode_workspace_size(case.B, case.Hq, case.Hkv, case.D, case.max_seq_len)
+    assert 0 < need <= SCRATCH_BYTES, "the case must exercise the split scratch"
+    want_o, want_lse = gpu_attention(case, pool, q, t)  # caller-provided workspace
+    o = torch.full_like(q, float("nan"))
+    lse = torch.full(q.shape[:2], float("nan"), dtype=torch.float32, device=q.device)
+    pkv.pkv_paged_decode_attn_noalloc(pool, case.layer, q, o, lse, t["page_table"],
+                                      t["seq_lens"], case.scale, case.max_seq_len,
+                                      table_idx=t.get("table_idx"))
+    torch.cuda.synchronize()
+    compare(o.double().cpu().numpy(), want_o.double().cpu().numpy())
+    lse_compare(lse.double().cpu().numpy(), want_lse.double().cpu().numpy())
+
+
+def test_noalloc_matches_workspace_decode_on_two_calls_in_a_row():
+    ensure_built()
+    first = W.random_case(71, seq_lens=[3000, 17, 1200, 4096, 640], Hq=32, Hkv=8, D=128,
+                          P=1)
+    second = W.random_case(72, seq_lens=[9000, 33, 2500], Hq=32, Hkv=4, D=128, P=16,
+                           use_table_idx=True)
+    _noalloc_vs_workspace(first)
+    _noalloc_vs_workspace(second)
+
+
+def test_noalloc_refuses_a_plan_larger_than_its_scratch():
+    ensure_built()
+    import paged_kv_attention_out_gb300 as pkv
+    batch, need = None, 0
+    for b in range(1000, 8192, 100):
+        need = pkv.pkv_decode_workspace_size(b, 32, 4, 128, 4096)
+        if need > SCRATCH_BYTES:
+            batch = b
+            break
+    assert batch is not None, "no batch size needs more scratch than the array holds"
+    dev = "cuda"
+    pool = torch.zeros(2, 1, 16, 16, 4, 128, dtype=torch.bfloat16, device=dev)
+    q = torch.zeros(batch, 32, 128, dtype=torch.bfloat16, device=dev)
+    o = torch.zeros_like(q)
+    pt = torch.zeros(batch, 1, dtype=torch.int32, device=dev)
+    sl = torch.ones(batch, dtype=torch.int32, device=dev)
+    with pytest.raises(pkv.PkvError) as ei:
+        pkv.pkv_paged_decode_attn_noalloc(pool, 0, q, o, None, pt, sl, 0.1, 4096)
+    assert ei.value.status == 3 and "static scratch" in str(ei.value)
+    torch.cuda.synchronize()
+    assert torch.all(o == 0)  # nothing was launched
