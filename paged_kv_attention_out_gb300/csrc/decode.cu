@@ -9,7 +9,7 @@
 //  * Grid (kv-head group, split, request). A CTA of 4 warps covers up to 4
 //    kv heads of one request over one split (a contiguous key range), so the
 //    CTA's loads of one token are one contiguous 1 KB (4 heads x 256 B) run.
-//  * Each warp streams 16-key tiles of its kv head through its own 3-stage
+//  * Each warp streams 16-key tiles of its kv head through its own 2-stage
 //    cp.async pipeline (16-byte chunks, zero-filled past the end, slots
 //    resolved from the page table one key per lane) into XOR-swizzled shared
 //    memory. No CTA-wide barrier inside the loop.
@@ -32,10 +32,21 @@
 namespace pkv {
 namespace {
 
+// Tuning constants (compile-time; the defaults are the measured best on GB300).
+#ifndef PKV_DECODE_STAGES
+#define PKV_DECODE_STAGES 2  // cp.async pipeline depth per warp
+#endif
+#ifndef PKV_DECODE_UNITS_PER_SM
+#define PKV_DECODE_UNITS_PER_SM 16  // split sizing: CTAs of work per SM at max length
+#endif
+#ifndef PKV_DECODE_MIN_SPLIT_TILES
+#define PKV_DECODE_MIN_SPLIT_TILES 8  // smallest split, in 16-key tiles
+#endif
+
 constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
 constexpr int kTileKeys = 16;
-constexpr int kStages = 3;
+constexpr int kStages = PKV_DECODE_STAGES;
 
 template <int D>
 struct DecodeSmem {
@@ -113,7 +124,7 @@ __device__ __forceinline__ RowInfo row_info(const DecodeArgs &a, int b, bool rep
 }
 
 template <int D>
-__global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeArgs a) {
+__global__ void __launch_bounds__(kThreads, (kStages <= 3 ? 2 : 1)) decode_kernel(const DecodeArgs a) {
   using S = DecodeSmem<D>;
   extern __shared__ __align__(128) uint8_t smem[];
   const int warp = threadIdx.x >> 5;
@@ -121,6 +132,8 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeArgs a)
   const int split = blockIdx.y;
   const int b = blockIdx.z;
 
+  grid_dependency_wait();    // inputs may come from the previous kernel (store_kv)
+  grid_dependents_launch();  // the split merge may be scheduled as CTAs drain
   const RowInfo ri = row_info(a, b, split == 0 && blockIdx.x == 0 && threadIdx.x == 0);
   if (split >= ri.nsplit) return;
   const int key_begin = split * a.chunk;
@@ -162,21 +175,28 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeArgs a)
       static_cast<int64_t>(kvh) * D;
   const int P = a.page_size;
 
-  auto issue = [&](int j, int stage) {
+  // Page-table entry of this lane's key of warp tile j (lanes 0..15), or -1
+  // past the end. Loaded one tile before its copies are issued, so the index
+  // load is off the critical path of the copy stream.
+  auto load_entry = [&](int j) -> int {
+    int e = -1;
+    if (lane < kTileKeys && j < my_tiles) {
+      const int key = key_begin + (sub + j * a.warps_per_head) * kTileKeys + lane;
+      if (key < key_end) e = __ldg(ri.row + ((P == 1) ? key : key / P));
+    }
+    return e;
+  };
+  auto issue = [&](int j, int entry, int stage) {
     const int k0 = key_begin + (sub + j * a.warps_per_head) * kTileKeys;
     long long slot = -1;
-    if (lane < kTileKeys) {
+    if (lane < kTileKeys && k0 + lane < key_end) {
       const int key = k0 + lane;
-      if (key < key_end) {
-        const int pi = (P == 1) ? key : key / P;
-        const int off = (P == 1) ? 0 : key - pi * P;
-        const long long pg = ri.row[pi];
-        const long long s = pg * P + off;
-        if (pg < 0 || s >= a.slots) {
-          flag_error(a.err, kErrPage);
-        } else {
-          slot = s;
-        }
+      const int off = (P == 1) ? 0 : key % P;
+      const long long s = static_cast<long long>(entry) * P + off;
+      if (entry < 0 || s >= a.slots) {
+        flag_error(a.err, kErrPage);
+      } else {
+        slot = s;
       }
     }
     constexpr int CPK = D / 8;      // 16-byte chunks per key row
@@ -195,17 +215,25 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeArgs a)
     }
   };
 
+  int next_entry;
+  {
+    int e[kStages - 1];
 #pragma unroll
-  for (int j = 0; j < kStages - 1; ++j) {
-    if (j < my_tiles) issue(j, j);
-    cp_async_commit();
+    for (int j = 0; j < kStages - 1; ++j) e[j] = load_entry(j);
+    next_entry = load_entry(kStages - 1);
+#pragma unroll
+    for (int j = 0; j < kStages - 1; ++j) {
+      if (j < my_tiles) issue(j, e[j], j);
+      cp_async_commit();
+    }
   }
 
   const int r0 = lane >> 2;
   for (int j = 0; j < my_tiles; ++j) {
     const int jn = j + kStages - 1;
-    if (jn < my_tiles) issue(jn, jn % kStages);
+    if (jn < my_tiles) issue(jn, next_entry, jn % kStages);
     cp_async_commit();
+    next_entry = load_entry(jn + 1);
     cp_async_wait<kStages - 1>();
     __syncwarp();
 
@@ -352,6 +380,7 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs a, i
   const int64_t bh = static_cast<int64_t>(blockIdx.x) * 4 + warp;
   if (bh >= static_cast<int64_t>(batch) * a.hq) return;
   const int b = static_cast<int>(bh / a.hq);
+  grid_dependency_wait();  // the partial states come from decode_kernel
   const RowInfo ri = row_info(a, b, false);
   const int n = ri.nsplit;
   if (n <= 1) return;
@@ -369,6 +398,7 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs a, i
   if (lane < D / 4) {
     float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
     const float *po = a.part_o + bh * a.splits * D + lane * 4;
+#pragma unroll 4
     for (int s = 0; s < n; ++s) {
       const float w = expf(pl[s] - ref) * inv;
       const float4 v = *reinterpret_cast<const float4 *>(po + static_cast<int64_t>(s) * D);
@@ -400,9 +430,9 @@ DecodePlan plan_decode(int32_t batch, int32_t hq, int32_t hkv, int32_t d, int32_
   // with at least 8 tiles (128 keys) per split so partial states stay a few
   // percent of the KV bytes.
   const int64_t units = static_cast<int64_t>(batch) * p.head_groups * tiles;
-  const int64_t target = static_cast<int64_t>(sm_count > 0 ? sm_count : 1) * 16;
+  const int64_t target = static_cast<int64_t>(sm_count > 0 ? sm_count : 1) * PKV_DECODE_UNITS_PER_SM;
   int64_t chunk_tiles = (units + target - 1) / target;
-  if (chunk_tiles < 8) chunk_tiles = 8;
+  if (chunk_tiles < PKV_DECODE_MIN_SPLIT_TILES) chunk_tiles = PKV_DECODE_MIN_SPLIT_TILES;
   int64_t splits = (tiles + chunk_tiles - 1) / chunk_tiles;
   while (splits > 65535) {
     chunk_tiles *= 2;
@@ -461,22 +491,21 @@ cudaError_t launch_decode(const PoolGeom &g, int32_t layer, const void *q, void 
     e = cudaFuncSetAttribute(decode_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              DecodeSmem<128>::kTotal);
     if (e != cudaSuccess) return e;
-    decode_kernel<128><<<grid, kThreads, DecodeSmem<128>::kTotal, stream>>>(a);
+    e = launch_pdl(decode_kernel<128>, grid, dim3(kThreads), DecodeSmem<128>::kTotal, stream, a);
   } else {
     e = cudaFuncSetAttribute(decode_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              DecodeSmem<64>::kTotal);
     if (e != cudaSuccess) return e;
-    decode_kernel<64><<<grid, kThreads, DecodeSmem<64>::kTotal, stream>>>(a);
+    e = launch_pdl(decode_kernel<64>, grid, dim3(kThreads), DecodeSmem<64>::kTotal, stream, a);
   }
-  e = cudaGetLastError();
   if (e != cudaSuccess || plan.splits <= 1) return e;
   const int64_t pairs = static_cast<int64_t>(batch) * hq;
-  const unsigned mblocks = static_cast<unsigned>((pairs + 3) / 4);
+  const dim3 mgrid(static_cast<unsigned>((pairs + 3) / 4));
   if (g.d == 128)
-    decode_merge_kernel<128><<<mblocks, 128, 0, stream>>>(a, batch);
+    e = launch_pdl(decode_merge_kernel<128>, mgrid, dim3(128), 0, stream, a, batch);
   else
-    decode_merge_kernel<64><<<mblocks, 128, 0, stream>>>(a, batch);
-  return cudaGetLastError();
+    e = launch_pdl(decode_merge_kernel<64>, mgrid, dim3(128), 0, stream, a, batch);
+  return e;
 }
 
 }  // namespace pkv

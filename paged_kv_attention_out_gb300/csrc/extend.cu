@@ -80,6 +80,7 @@ __global__ void __launch_bounds__(kThreads, 2) extend_kernel(const ExtendArgs a)
   const int lane = tid & 31;
   const int kvh = blockIdx.x;
 
+  grid_dependency_wait();  // the chunk's K/V may come from the previous kernel (store_kv)
   // Which (request, token tile) this CTA owns; tiles are taken from the end.
   if (tid == 0) {
     const int tile = static_cast<int>(gridDim.y) - 1 - static_cast<int>(blockIdx.y);
@@ -346,14 +347,14 @@ cudaError_t launch_extend(const PoolGeom &g, int32_t layer, const void *q,
     e = cudaFuncSetAttribute(extend_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              ExtendSmem<128>::kTotal);
     if (e != cudaSuccess) return e;
-    extend_kernel<128><<<grid, kThreads, ExtendSmem<128>::kTotal, stream>>>(a);
+    e = launch_pdl(extend_kernel<128>, grid, dim3(kThreads), ExtendSmem<128>::kTotal, stream, a);
   } else {
     e = cudaFuncSetAttribute(extend_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              ExtendSmem<64>::kTotal);
     if (e != cudaSuccess) return e;
-    extend_kernel<64><<<grid, kThreads, ExtendSmem<64>::kTotal, stream>>>(a);
+    e = launch_pdl(extend_kernel<64>, grid, dim3(kThreads), ExtendSmem<64>::kTotal, stream, a);
   }
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace pkv

@@ -21,6 +21,8 @@ __global__ void __launch_bounds__(256)
                     const __nv_bfloat16 *__restrict__ v, int64_t row_stride,
                     const int32_t *__restrict__ out_loc, int64_t n, int32_t chunks_per_row,
                     unsigned *err) {
+  grid_dependency_wait();    // k, v, out_loc may come from the previous kernel
+  grid_dependents_launch();  // let the attention kernel that follows get scheduled
   const int64_t total = n * 2 * chunks_per_row;
   const int64_t row_elems = static_cast<int64_t>(chunks_per_row) * 8;
   for (int64_t w = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; w < total;
@@ -53,11 +55,10 @@ cudaError_t launch_kv_store(const PoolGeom &g, int32_t layer, const void *k, con
   const int64_t cap = static_cast<int64_t>(sm_count) * 8;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  kv_store_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
-      static_cast<__nv_bfloat16 *>(const_cast<void *>(g.base)), g.plane, g.slots, layer,
-      g.num_layers, static_cast<const __nv_bfloat16 *>(k), static_cast<const __nv_bfloat16 *>(v),
-      row_stride, out_loc, n, chunks, err);
-  return cudaGetLastError();
+  return launch_pdl(kv_store_kernel, dim3(static_cast<unsigned>(blocks)), dim3(threads), 0,
+                    stream, static_cast<__nv_bfloat16 *>(const_cast<void *>(g.base)), g.plane,
+                    g.slots, layer, g.num_layers, static_cast<const __nv_bfloat16 *>(k),
+                    static_cast<const __nv_bfloat16 *>(v), row_stride, out_loc, n, chunks, err);
 }
 
 }  // namespace pkv

@@ -19,6 +19,7 @@ __global__ void __launch_bounds__(256)
     merge_kernel(const float *__restrict__ o_a, const float *__restrict__ lse_a,
                  const float *__restrict__ o_b, const float *__restrict__ lse_b, void *o_out,
                  int out_bf16, float *lse_out, int64_t pairs, int32_t head_dim) {
+  grid_dependency_wait();  // the states may come from the previous kernel
   const int lane = threadIdx.x & 31;
   const int64_t warps_total = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
   for (int64_t rh = blockIdx.x * static_cast<int64_t>(blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -81,9 +82,8 @@ cudaError_t launch_merge(const float *o_a, const float *lse_a, const float *o_b,
   const int64_t cap = static_cast<int64_t>(sm_count) * 16;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  merge_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
-      o_a, lse_a, o_b, lse_b, o_out, out_bf16 ? 1 : 0, lse_out, pairs, head_dim);
-  return cudaGetLastError();
+  return launch_pdl(merge_kernel, dim3(static_cast<unsigned>(blocks)), dim3(threads), 0, stream,
+                    o_a, lse_a, o_b, lse_b, o_out, out_bf16 ? 1 : 0, lse_out, pairs, head_dim);
 }
 
 }  // namespace pkv

@@ -85,6 +85,36 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t *>(&v);
 }
 
+// Programmatic dependent launch. A kernel launched with launch_pdl may be
+// scheduled while the previous kernel on its stream is still finishing; it
+// must call grid_dependency_wait() before reading anything that kernel may
+// have written (the wait returns once that grid has completed and its memory
+// is visible). grid_dependents_launch() lets the next such kernel be
+// scheduled early.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void grid_dependents_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...);
+}
+
 // Shared-memory tile of rows x (D bf16): 16-byte chunks XOR-swizzled by
 // row % 8, so ldmatrix over 8 consecutive rows of one logical chunk hits 8
 // distinct bank groups.
