@@ -37,13 +37,16 @@ namespace {
 #define PKV_DECODE_STAGES 2  // cp.async pipeline depth per warp
 #endif
 #ifndef PKV_DECODE_UNITS_PER_SM
-#define PKV_DECODE_UNITS_PER_SM 16  // split sizing: CTAs of work per SM at max length
+#define PKV_DECODE_UNITS_PER_SM 8  // split sizing: CTAs of work per SM at max length
+#endif
+#ifndef PKV_DECODE_WARPS
+#define PKV_DECODE_WARPS 4  // warps per CTA (each on one kv head)
 #endif
 #ifndef PKV_DECODE_MIN_SPLIT_TILES
 #define PKV_DECODE_MIN_SPLIT_TILES 8  // smallest split, in 16-key tiles
 #endif
 
-constexpr int kWarps = 4;
+constexpr int kWarps = PKV_DECODE_WARPS;
 constexpr int kThreads = kWarps * 32;
 constexpr int kTileKeys = 16;
 constexpr int kStages = PKV_DECODE_STAGES;
@@ -426,9 +429,9 @@ DecodePlan plan_decode(int32_t batch, int32_t hq, int32_t hkv, int32_t d, int32_
   p.head_groups = hkv / p.heads_per_cta;
   const int64_t max_seq = max_seq_len < 1 ? 1 : max_seq_len;
   const int64_t tiles = (max_seq + kTileKeys - 1) / kTileKeys;
-  // Aim for about 16 CTAs of work per SM if every request were max_seq long,
-  // with at least 8 tiles (128 keys) per split so partial states stay a few
-  // percent of the KV bytes.
+  // Aim for about PKV_DECODE_UNITS_PER_SM CTAs of work per SM if every
+  // request were max_seq long, with at least PKV_DECODE_MIN_SPLIT_TILES tiles
+  // per split so partial states stay a few percent of the KV bytes.
   const int64_t units = static_cast<int64_t>(batch) * p.head_groups * tiles;
   const int64_t target = static_cast<int64_t>(sm_count > 0 ? sm_count : 1) * PKV_DECODE_UNITS_PER_SM;
   int64_t chunk_tiles = (units + target - 1) / target;
