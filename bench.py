@@ -353,6 +353,12 @@ def run_pkv(args):
     pkv.pkv_init()
     peaks, peak_src = load_peaks()
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    if args.only not in (None, "llama3-8b-decode"):
+        # one named workload alone (used for profiling): prints its JSON object
+        if rank == 0:
+            print(json.dumps(other_workloads(args, dev, peaks, peak_src, flush, args.only)),
+                  flush=True)
+        return
 
     # ---- main workload: Llama-3-8B-shaped decode -----------------------------
     case = W.llama8b_decode(args.seed + rank)
@@ -450,11 +456,24 @@ def _measure(wl: Workload, steps: int, warmup: int, flush):
     return statistics.mean(step_ms), statistics.mean(attn_ms)
 
 
-def other_workloads(args, dev, peaks, peak_src, flush):
+def other_workloads(args, dev, peaks, peak_src, flush, only=None):
     out = {}
-    steps = max(5, min(args.steps, 100))
+    steps = max(5, min(args.steps, 100)) if only is None else args.steps
     warm = max(3, args.warmup)
-    # chunked-prefill extend
+    want = (lambda name: only is None or only == name)
+    if want("chunked-prefill-extend"):
+        out.update(_extend_workload(args, dev, peaks, peak_src, flush, steps, warm))
+    if want("long-context-decode"):
+        out.update(_long_workload(args, dev, peaks, peak_src, flush, steps, warm))
+    if want("radix-shared-decode"):
+        out.update(_radix_workload(args, dev, peaks, peak_src, flush, steps, warm))
+    if want("tiny-decode"):
+        out.update(_tiny_workload(args, dev, flush, steps, warm))
+    return out
+
+
+def _extend_workload(args, dev, peaks, peak_src, flush, steps, warm):
+    out = {}
     case = W.chunked_prefill_extend(args.seed)
     wl = Workload(case, dev)
     st, at = _measure(wl, steps, warm, flush)
@@ -467,7 +486,11 @@ def other_workloads(args, dev, peaks, peak_src, flush):
                      "kernel": "extend_kernel", "traffic": args.extend_traffic}}
     del wl
     torch.cuda.empty_cache()
-    # long-context decode (page_size 16, split-KV)
+    return out
+
+
+def _long_workload(args, dev, peaks, peak_src, flush, steps, warm):
+    out = {}
     case = W.long_context_decode(args.seed)
     wl = Workload(case, dev)
     st, at = _measure(wl, steps, warm, flush)
@@ -480,7 +503,12 @@ def other_workloads(args, dev, peaks, peak_src, flush):
                      "kernel": "decode_kernel + decode_merge_kernel"}}
     del wl
     torch.cuda.empty_cache()
-    # radix-shared-prefix decode: unique bytes (roofline) and logical bytes
+    return out
+
+
+def _radix_workload(args, dev, peaks, peak_src, flush, steps, warm):
+    """Radix-shared-prefix decode: unique bytes (roofline) and logical bytes."""
+    out = {}
     case = W.radix_shared_decode(args.seed)
     wl = Workload(case, dev)
     st, at = _measure(wl, steps, warm, flush)
@@ -494,7 +522,11 @@ def other_workloads(args, dev, peaks, peak_src, flush):
                      "kernel": "decode_kernel + decode_merge_kernel"}}
     del wl
     torch.cuda.empty_cache()
-    # tiny decode: latency
+    return out
+
+
+def _tiny_workload(args, dev, flush, steps, warm):
+    out = {}
     case = W.tiny_decode(args.seed)
     wl = Workload(case, dev)
     st, at = _measure(wl, steps, warm, flush)
@@ -565,6 +597,11 @@ def parse_args(argv=None):
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--main-only", action="store_true",
                     help="skip the other named workloads")
+    ap.add_argument("--only", choices=["llama3-8b-decode", "chunked-prefill-extend",
+                                       "long-context-decode", "radix-shared-decode",
+                                       "tiny-decode"], default=None,
+                    help="run one named workload alone and print its JSON object "
+                         "(for profiling); llama3-8b-decode = the main line")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0,
                     help="seconds of oracle time for cpu_baseline")

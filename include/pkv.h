@@ -73,6 +73,7 @@ typedef enum {
 #define PKV_DEVERR_SEQ_LEN_RANGE 0x4    /* seq_len < 0 or past the row's stride */
 #define PKV_DEVERR_INDPTR 0x8           /* qo_indptr not monotone / prefix < 0 */
 #define PKV_DEVERR_TABLE_IDX_RANGE 0x10 /* table_idx negative                  */
+#define PKV_DEVERR_TIMEOUT 0x20         /* a bounded in-kernel wait gave up     */
 
 /* The KV pool (one tensor, see the layout above). base: device, bf16,
  * 16-byte aligned. Passed by pointer; the library does not keep it. */
@@ -151,7 +152,7 @@ pkv_status pkv_paged_decode_attn(const pkv_pool *pool, int32_t layer, const void
                                  size_t workspace_bytes, cudaStream_t stream);
 
 /* Size of the library-owned scratch used by pkv_paged_decode_attn_noalloc. */
-#define PKV_NOALLOC_SCRATCH_BYTES (64u << 20)
+#define PKV_NOALLOC_SCRATCH_BYTES (32u << 20)
 
 /*
  * Decode attention that allocates nothing and takes no workspace. The pages
@@ -164,7 +165,7 @@ pkv_status pkv_paged_decode_attn(const pkv_pool *pool, int32_t layer, const void
  *
  * Same arguments and results as pkv_paged_decode_attn, minus the workspace:
  * the split-KV partial states go to a fixed scratch array in device memory
- * that the library owns (PKV_NOALLOC_SCRATCH_BYTES = 64 MiB, held by every
+ * that the library owns (PKV_NOALLOC_SCRATCH_BYTES = 32 MiB, held by every
  * GPU that loads the library until the process exits).
  *  - If the split plan for these sizes needs more than that
  *    (pkv_decode_workspace_size(...) > PKV_NOALLOC_SCRATCH_BYTES), the call

@@ -182,7 +182,7 @@ def pkv_paged_decode_attn_noalloc(pool, layer: int, q, o, lse, page_table, seq_l
                                   stream=None) -> None:
     """Decode attention with no workspace, for callers that cannot allocate.
 
-    The split-KV scratch is a fixed library-owned device array (64 MiB), so
+    The split-KV scratch is a fixed library-owned device array (32 MiB), so
     nothing is allocated; calls whose kernels overlap on the GPU race on it.
     """
     ps = pool_struct(pool)

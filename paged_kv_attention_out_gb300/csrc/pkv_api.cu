@@ -244,7 +244,7 @@ pkv_status pkv_paged_extend_attn(const pkv_pool *pool, int32_t layer, const void
   if (!aligned(page_table, 4) || !aligned(seq_lens, 4) || !aligned(lse, 4) ||
       !aligned(table_idx, 4) || !aligned(qo_indptr, 4))
     return fail(PKV_ERR_INVALID_ARG, "int32/fp32 tables must be 4-byte aligned");
-  const int64_t tpc = 64 / group;
+  const int64_t tpc = 128 / group;  // chunk tokens per 128-row query tile
   if ((static_cast<int64_t>(total_q) + tpc - 1) / tpc + batch > 65535)
     return fail(PKV_ERR_UNSUPPORTED, "extend: too many query tiles in one call");
   DevInfo *d = nullptr;
