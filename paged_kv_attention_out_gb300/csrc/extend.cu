@@ -1,4 +1,4 @@
-// extend.cu - paged extend (chunked-prefill) attention on tcgen05 / TMEM.
+// extend.cu - paged extend (chunked-prefill) attention on tcgen05 / TMEM / TMA.
 //
 // What it computes ("Code Notes: mini-sglang", Scheduler Layer table,
 // PrefillManager row; "Introduction", Key Features, Chunked Prefill and Radix
@@ -10,23 +10,29 @@
 // tokens x the g q heads that read that kv head, so every gathered K/V tile
 // feeds g heads. It walks the visible keys in tiles of 128:
 //   S_j  = Q K_j^T            tcgen05.mma, M=128 N=128 K=D, fp32 in TMEM
-//   P_j  = exp2(scale*S_j - m) softmax warps, one thread per query row, bf16
-//                             into shared memory
+//   P_j  = exp2(scale*S_j - m) softmax warps, bf16 into shared memory
 //   O   += P_j V_j            tcgen05.mma, M=128 N=D K=128, fp32 in TMEM
-// Roles (288 threads):
-//   warps 0-3  softmax: thread r owns row r of S and O (TMEM lane r); online
+// Roles (416 threads):
+//   warps 0-7  softmax: warp w owns TMEM lanes 32 (w % 4) .. + 31 (query
+//              rows) and half w / 4 of each row's key columns; online
 //              softmax in the log2 domain with a lazy rescale (O is rescaled
-//              only when the row max grows by more than 2^8), causal and
-//              range masks only on tiles that cross a row's last key, then
-//              the epilogue O / l -> bf16 and lse.
-//   warp 4     TMEM allocation and the single MMA-issuing thread; S is
+//              only when a row max grows by more than 2^8), masks only on
+//              tiles that cross a row's last key, then O / l -> bf16 and lse.
+//   warp 8     TMEM allocation and the single MMA-issuing thread; S is
 //              double-buffered in TMEM so QK^T of tile j+1 runs while the
 //              softmax works on tile j.
-//   warps 5-8  producers: gather K_j and V_j rows through the page table
-//              with 16-byte cp.async into the SW128 shared layout (zero fill
-//              past the end), two stages deep.
+//   warps 9-12 producers: TMA tile::gather4 loads (4 rows per instruction,
+//              128-byte swizzle, zeros for keys past the end) of the Q rows
+//              and, through the page table, of the K rows (warps 9-10) and V
+//              rows (warps 11-12) of each tile. TMA issue is serialised per
+//              warp, so four warps issue; a K buffer is refilled once its
+//              QK^T is done, a V buffer once its PV is done.
 // Every hand-off is an mbarrier; every wait is bounded (tc_common.cuh).
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <math.h>
+
+#include <mutex>
 
 #include "pkv_common.cuh"
 #include "pkv_internal.h"
@@ -39,10 +45,9 @@ constexpr int kM = 128;  // query rows per CTA
 constexpr int kN = 128;  // keys per K/V tile
 constexpr int kSoftmaxWarps = 8;  // two per SM sub-partition: a row's columns are split
 constexpr int kMmaWarp = kSoftmaxWarps;
+constexpr int kProducerWarp = kSoftmaxWarps + 1;  // warps +0, +1: K (and Q); +2, +3: V
 constexpr int kProducerWarps = 4;
-constexpr int kProducerBase = (kSoftmaxWarps + 1) * 32;
 constexpr int kThreads = (kSoftmaxWarps + 1 + kProducerWarps) * 32;
-constexpr int kProducers = kProducerWarps * 32;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
@@ -55,10 +60,9 @@ struct Smem {
   static constexpr int kP = kKV + 4 * kTileBytes;
   static constexpr int kPBytes = kM * kN * 2;
   static constexpr int kBars = kP + kPBytes;
-  static constexpr int kBarCount = 17;
   // + alignment slack; never below 116 KB, so one CTA (and one 512-column
   // TMEM allocation) per SM even for head_dim 64
-  static constexpr int kNeed = kBars + kBarCount * 8 + 16 + 1024;
+  static constexpr int kNeed = kBars + 32 * 8 + 16 + 1024;
   static constexpr int kTotal = kNeed > 116 * 1024 ? kNeed : 116 * 1024;
 };
 
@@ -68,26 +72,25 @@ constexpr uint32_t kTmemO = 256;
 
 // Barrier indices.
 enum : int {
-  kBarKFull = 0,   // [2] producers: K tile landed
-  kBarVFull = 2,   // [2] producers: V tile landed
-  kBarKVEmpty = 4, // [2] MMA: stage consumed (after PV)
-  kBarSFull = 6,   // [2] MMA: S tile ready
-  kBarSFree = 8,   // [2] softmax: S tile read
-  kBarPFull = 10,  // softmax: P written
-  kBarODone = 11,  // MMA: PV finished
-  kBarTeardown = 12,  // MMA: everything issued has finished (abort path)
-  kBarPair = 13,      // [4] softmax: the two warps of a lane quarter exchanged a value
+  kBarKFull = 0,      // [2] producer: K tile landed (TMA bytes)
+  kBarVFull = 2,      // [2] producer: V tile landed (TMA bytes)
+  kBarKEmpty = 4,     // [2] MMA: K buffer consumed (after QK^T)
+  kBarVEmpty = 6,     // [2] MMA: V buffer consumed (after PV)
+  kBarSFull = 8,      // [2] MMA: S tile ready
+  kBarSFree = 10,     // [2] softmax: S tile read
+  kBarPFull = 12,     // softmax: P written
+  kBarODone = 13,     // MMA: PV finished
+  kBarTeardown = 14,  // MMA: everything issued has finished (abort path)
+  kBarPair = 15,      // [4] softmax: the two warps of a lane quarter exchanged a value
+  kBarQFull = 19,     // producer: Q tile landed (TMA bytes)
+  kBarCount = 20,
 };
 
 struct ExtendArgs {
-  const __nv_bfloat16 *pool;
-  int64_t plane;
-  int64_t slots;
+  int64_t slots;         // pool slots per (c, layer) plane
   int32_t num_layers;
   int32_t layer;
   int32_t page_size;
-  int32_t hkv;
-  const __nv_bfloat16 *q;
   const int32_t *qo_indptr;
   __nv_bfloat16 *o;
   float *lse;
@@ -110,8 +113,13 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
+// pool_map: the pool as a 2-D bf16 tensor [2 * L * slots rows][Hkv * D]
+// (row (c * L + layer) * slots + slot); q_map: q as [total_q * Hq rows][D].
+// Both with box {64, 1} and 128-byte swizzle.
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const ExtendArgs a) {
+__global__ void __launch_bounds__(kThreads, 1)
+    extend_tc_kernel(const __grid_constant__ CUtensorMap pool_map,
+                     const __grid_constant__ CUtensorMap q_map, const ExtendArgs a) {
   using S = Smem<D>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ int s_req, s_j0, s_c, s_p, s_row;
@@ -183,20 +191,19 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const ExtendArgs
   const int n_tiles = (n_keys + kN - 1) / kN;
 
   if (tid == 0) {
-    mbar_init(bar(kBarKFull + 0), kProducers);
-    mbar_init(bar(kBarKFull + 1), kProducers);
-    mbar_init(bar(kBarVFull + 0), kProducers);
-    mbar_init(bar(kBarVFull + 1), kProducers);
-    mbar_init(bar(kBarKVEmpty + 0), 1);
-    mbar_init(bar(kBarKVEmpty + 1), 1);
-    mbar_init(bar(kBarSFull + 0), 1);
-    mbar_init(bar(kBarSFull + 1), 1);
-    mbar_init(bar(kBarSFree + 0), kSoftmaxWarps * 32);
-    mbar_init(bar(kBarSFree + 1), kSoftmaxWarps * 32);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(kBarKFull + i), 2);  // one expect_tx arrival per issuing warp
+      mbar_init(bar(kBarVFull + i), 2);
+      mbar_init(bar(kBarKEmpty + i), 1);
+      mbar_init(bar(kBarVEmpty + i), 1);
+      mbar_init(bar(kBarSFull + i), 1);
+      mbar_init(bar(kBarSFree + i), kSoftmaxWarps * 32);
+    }
     mbar_init(bar(kBarPFull), kSoftmaxWarps * 32);
     mbar_init(bar(kBarODone), 1);
     mbar_init(bar(kBarTeardown), 1);
     for (int q = 0; q < 4; ++q) mbar_init(bar(kBarPair + q), 64);
+    mbar_init(bar(kBarQFull), 2);
     mbar_init_fence();
   }
   if (warp == kMmaWarp) tmem_alloc(smem_addr(&s_tmem), kTmemCols);
@@ -205,115 +212,142 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const ExtendArgs
   tc_fence_after_sync();
   const uint32_t tmem = s_tmem;
 
-  if (warp >= kSoftmaxWarps + 1) {
+  if (warp >= kProducerWarp) {
     // ------------------------------------------------------------ producers
-    const int pt = tid - kProducerBase;
-    constexpr int CPK = D / 8;                 // 16-byte chunks per row
-    constexpr int kRowsPerPass = kProducers / CPK;
-    constexpr int kPasses = kN / kRowsPerPass;  // rows handled per thread per tile
-    const int ch = pt % CPK;
-    const int r0 = pt / CPK;
-    const int64_t slot_stride = static_cast<int64_t>(a.hkv) * D;
-    const __nv_bfloat16 *kbase =
-        a.pool + static_cast<int64_t>(a.layer) * a.plane + static_cast<int64_t>(kvh) * D + ch * 8;
-    const __nv_bfloat16 *vbase = a.pool + (static_cast<int64_t>(a.num_layers) + a.layer) * a.plane +
-                                 static_cast<int64_t>(kvh) * D + ch * 8;
+    // Producer warp pw (0..3): pw 0-1 load Q and K tiles, pw 2-3 V tiles.
+    // In a tile, warp w2 = pw & 1 covers row groups 16 w2 .. 16 w2 + 15
+    // (4 rows each); lane l takes group 16 w2 + (l & 15) and 64-column half
+    // l >> 4. Rows that must read as zero (past the end, bad page ids) get
+    // row -1.
+    const int pw = warp - kProducerWarp;
+    const bool is_k = pw < 2;
+    const int grp = 16 * (pw & 1) + (lane & 15);
+    const int h = lane >> 4;
+    constexpr int kHalves = D / 64;
+    const bool active = h < kHalves;
     const int P = a.page_size;
-    // Q tile: row r -> token j0 + r / g, q head kvh * g + r % g.
-    for (int i = 0; i < kM / kRowsPerPass; ++i) {
-      const int r = r0 + i * kRowsPerPass;
-      const int t = r / a.group, hh = r % a.group;
-      const bool ok = t < tokens;
-      const __nv_bfloat16 *src =
-          ok ? a.q + (static_cast<int64_t>(t_base + j0 + t) * a.hq + kvh * a.group + hh) * D + ch * 8
-             : a.q;
-      cp_async_16(sbase + S::kQ + sw128_offset(kM, r, ch * 8), src, ok ? 16 : 0);
-    }
-    cp_async_commit();
-    // Page-table entries of this thread's rows, loaded one tile ahead.
-    int entry[kPasses];
+    const int plane = (is_k ? 0 : a.num_layers) + a.layer;
+    const int plane_base = plane * static_cast<int>(a.slots);
+    const int xcol = kvh * D + h * 64;
+    // destination of rows 4 grp .. 4 grp + 3 inside a SW128 region
+    const uint32_t row_off =
+        static_cast<uint32_t>(h * (kN * 128) + (grp >> 1) * 1024 + (grp & 1) * 512);
+    constexpr uint32_t kWarpBytes = S::kTileBytes / 2;  // each of the two warps' share
+    bool ok = true;
+    if (is_k) {
+      int qr[4];
 #pragma unroll
-    for (int i = 0; i < kPasses; ++i) {
-      const int key = r0 + i * kRowsPerPass;
-      entry[i] = key < n_keys ? __ldg(row_pages + ((P == 1) ? key : key / P)) : -1;
+      for (int e = 0; e < 4; ++e) {
+        const int r = 4 * grp + e;
+        const int t = r / a.group;
+        qr[e] = t < tokens ? (t_base + j0 + t) * a.hq + kvh * a.group + (r % a.group) : -1;
+      }
+      if (lane == 0) mbar_arrive_expect_tx(bar(kBarQFull), S::kQBytes / 2);
+      __syncwarp();
+      if (active)
+        tma_gather4(sbase + S::kQ + static_cast<uint32_t>(h * (kM * 128) + (grp >> 1) * 1024 +
+                                                         (grp & 1) * 512),
+                    &q_map, h * 64, qr[0], qr[1], qr[2], qr[3], bar(kBarQFull));
     }
+    // Pool rows of this lane's 4 keys of tile j (-1 where the key is past
+    // the end or its page id is out of range): one division per tile, then
+    // the keys walk through the page.
+    auto rows_of = [&](int j, int (&rr)[4]) {
+      const int k0 = j * kN + 4 * grp;
+      int pidx = k0 / P;
+      int off = k0 - pidx * P;
+      int ent = -1, ent_idx = -1;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        if (off == P) {
+          ++pidx;
+          off = 0;
+        }
+        rr[e] = -1;
+        if (k0 + e < n_keys) {
+          if (pidx != ent_idx) {
+            ent = __ldg(row_pages + pidx);
+            ent_idx = pidx;
+          }
+          const long long sl = static_cast<long long>(ent) * P + off;
+          if (ent >= 0 && sl < a.slots) {
+            rr[e] = plane_base + static_cast<int>(sl);
+          } else if (is_k && h == 0) {
+            flag_error(a.err, kErrPage);
+          }
+        }
+        ++off;
+      }
+    };
+    const int full_bar = is_k ? kBarKFull : kBarVFull;
+    const int empty_bar = is_k ? kBarKEmpty : kBarVEmpty;
+    const int buf_off = is_k ? 0 : S::kTileBytes;
+    int rr[4];
+    rows_of(0, rr);
+    int issued = 0;
     for (int j = 0; j < n_tiles; ++j) {
       const int s = j & 1;
-      if (j >= 2 && !mbar_wait(bar(kBarKVEmpty + s), ((j >> 1) - 1) & 1, abort)) {
-        *abort = 1;
-        break;
-      }
-      int64_t off[kPasses];
-#pragma unroll
-      for (int i = 0; i < kPasses; ++i) {
-        const int key = j * kN + r0 + i * kRowsPerPass;
-        const long long sl = static_cast<long long>(entry[i]) * P + ((P == 1) ? 0 : key % P);
-        const bool ok = key < n_keys && entry[i] >= 0 && sl < a.slots;
-        if (key < n_keys && !ok) flag_error(a.err, kErrPage);
-        off[i] = ok ? sl * slot_stride : -1;
-        const int nkey = key + kN;  // same row of tile j + 1
-        entry[i] = nkey < n_keys ? __ldg(row_pages + ((P == 1) ? nkey : nkey / P)) : -1;
-      }
-      const uint32_t kst = sbase + S::kKV + s * 2 * S::kTileBytes;
-      const uint32_t vst = kst + S::kTileBytes;
-#pragma unroll
-      for (int i = 0; i < kPasses; ++i) {
-        const int r = r0 + i * kRowsPerPass;
-        cp_async_16(kst + sw128_offset(kN, r, ch * 8), off[i] >= 0 ? kbase + off[i] : a.pool,
-                    off[i] >= 0 ? 16 : 0);
-      }
-      cp_async_commit();
-#pragma unroll
-      for (int i = 0; i < kPasses; ++i) {
-        const int r = r0 + i * kRowsPerPass;
-        cp_async_16(vst + sw128_offset(kN, r, ch * 8), off[i] >= 0 ? vbase + off[i] : a.pool,
-                    off[i] >= 0 ? 16 : 0);
-      }
-      cp_async_commit();
-      cp_async_wait<1>();  // K_j (and V_{j-1}, Q) landed
-      fence_async_shared();
-      mbar_arrive(bar(kBarKFull + s));
-      if (j >= 1) mbar_arrive(bar(kBarVFull + (s ^ 1)));
+      if (j >= 2 && !(ok = mbar_wait_warp(bar(empty_bar + s), ((j >> 1) - 1) & 1, abort))) break;
+      if (lane == 0) mbar_arrive_expect_tx(bar(full_bar + s), kWarpBytes);
+      __syncwarp();
+      if (active)
+        tma_gather4(sbase + S::kKV + s * 2 * S::kTileBytes + buf_off + row_off, &pool_map, xcol,
+                    rr[0], rr[1], rr[2], rr[3], bar(full_bar + s));
+      ++issued;
+      if (j + 1 < n_tiles) rows_of(j + 1, rr);
     }
-    cp_async_wait<0>();
-    fence_async_shared();
-    if (!*abort && n_tiles > 0) mbar_arrive(bar(kBarVFull + ((n_tiles - 1) & 1)));
+    if (!ok) *abort = 1;
+    if (*abort && lane == 0) {
+      // Let every issued copy land before the CTA can exit: TMA writes to
+      // this CTA's shared memory need no other input to finish.
+      int never = 0;
+      if (is_k) mbar_wait(bar(kBarQFull), 0, &never);
+      for (int t = issued > 2 ? issued - 2 : 0; t < issued; ++t)
+        mbar_wait(bar(full_bar + (t & 1)), (t >> 1) & 1, &never);
+    }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc_qk = umma_idesc_bf16(kM, kN, 0, 0);
       constexpr uint32_t idesc_pv = umma_idesc_bf16(kM, D, 0, 1);
+      // Descriptors are built once; a k-step adds its byte offset / 16 to the
+      // start-address field (addresses stay below 256 KB, so no carry).
+      const uint64_t dq = umma_desc_sw128(sbase + S::kQ, 16, 1024);
+      const uint64_t dp = umma_desc_sw128(sbase + S::kP, 16, 1024);
+      const uint64_t dk0 = umma_desc_sw128(sbase + S::kKV, 16, 1024);
+      const uint64_t dv0 = umma_desc_sw128(sbase + S::kKV + S::kTileBytes, kN * 128, 1024);
+      constexpr uint64_t kStageStep = (2 * S::kTileBytes) >> 4;
+      auto kstep = [](int ks, int rows) -> uint64_t {
+        return static_cast<uint64_t>(((ks >> 2) * (rows * 128) + (ks & 3) * 32) >> 4);
+      };
       auto pv = [&](int i) -> bool {
         const int s = i & 1;
         if (!mbar_wait(bar(kBarPFull), i & 1, abort)) return false;
         if (!mbar_wait(bar(kBarVFull + s), (i >> 1) & 1, abort)) return false;
         tc_fence_after_sync();
-        const uint32_t vst = sbase + S::kKV + s * 2 * S::kTileBytes + S::kTileBytes;
+        const uint64_t dv = dv0 + s * kStageStep;
 #pragma unroll
-        for (int ks = 0; ks < kN / 16; ++ks) {
-          const uint64_t da = umma_desc_sw128(sbase + S::kP + (ks >> 2) * (kM * 128) + (ks & 3) * 32, 16, 1024);
-          const uint64_t db = umma_desc_sw128(vst + ks * 2048, kN * 128, 1024);
-          umma_bf16_ss(tmem + kTmemO, da, db, idesc_pv, (i > 0 || ks > 0) ? 1u : 0u);
-        }
+        for (int ks = 0; ks < kN / 16; ++ks)
+          umma_bf16_ss(tmem + kTmemO, dp + kstep(ks, kM), dv + ks * (2048 >> 4), idesc_pv,
+                       (i > 0 || ks > 0) ? 1u : 0u);
         umma_commit(bar(kBarODone));
-        umma_commit(bar(kBarKVEmpty + s));
+        umma_commit(bar(kBarVEmpty + s));
         return true;
       };
-      bool ok = true;
+      bool ok = mbar_wait(bar(kBarQFull), 0, abort);
       for (int j = 0; j < n_tiles && ok; ++j) {
         const int s = j & 1;
         ok = mbar_wait(bar(kBarKFull + s), (j >> 1) & 1, abort);
         if (ok && j >= 2) ok = mbar_wait(bar(kBarSFree + s), ((j >> 1) - 1) & 1, abort);
         if (!ok) break;
         tc_fence_after_sync();
-        const uint32_t kst = sbase + S::kKV + s * 2 * S::kTileBytes;
+        const uint64_t dk = dk0 + s * kStageStep;
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint64_t da = umma_desc_sw128(sbase + S::kQ + (ks >> 2) * (kM * 128) + (ks & 3) * 32, 16, 1024);
-          const uint64_t db = umma_desc_sw128(kst + (ks >> 2) * (kN * 128) + (ks & 3) * 32, 16, 1024);
-          umma_bf16_ss(tmem + kTmemS + s * kN, da, db, idesc_qk, ks > 0 ? 1u : 0u);
-        }
+        for (int ks = 0; ks < D / 16; ++ks)
+          umma_bf16_ss(tmem + kTmemS + s * kN, dq + kstep(ks, kM), dk + kstep(ks, kN), idesc_qk,
+                       ks > 0 ? 1u : 0u);
         umma_commit(bar(kBarSFull + s));
+        umma_commit(bar(kBarKEmpty + s));
         if (j >= 1) ok = pv(j - 1);
       }
       if (ok && n_tiles > 0) ok = pv(n_tiles - 1);
@@ -356,34 +390,20 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const ExtendArgs
       if (!(ok = mbar_wait_warp(bar(kBarSFull + s), (j >> 1) & 1, abort))) break;
       tc_fence_after_sync();
       const int key0 = j * kN + hc * kCols;
-      const bool full = key0 + kCols - 1 <= limit;
-      float v[kCols];
-      {
-        float a0[32], a1[32];
-        tmem_ld32(tmem + lane_base + kTmemS + s * kN + hc * kCols, a0);
-        tmem_ld32(tmem + lane_base + kTmemS + s * kN + hc * kCols + 32, a1);
+      const uint32_t srow = tmem + lane_base + kTmemS + s * kN + hc * kCols;
+      // Pass 1: row max of the raw scores (scale > 0 commutes with max).
+      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll 1
+      for (int cb = 0; cb < kCols / 16; ++cb) {
+        float v[16];
+        tmem_ld16(srow + cb * 16, v);
         tmem_ld_wait();
+        const int kb = key0 + cb * 16;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          v[i] = a0[i];
-          v[32 + i] = a1[i];
-        }
+        for (int i = 0; i < 16; ++i)
+          mx[i & 3] = fmaxf(mx[i & 3], kb + i <= limit ? v[i] : -INFINITY);
       }
-      tc_fence_before_sync();
-      mbar_arrive(bar(kBarSFree + s));  // S tile read: QK^T of tile j + 2 may overwrite it
-      if (!full) {
-#pragma unroll
-        for (int i = 0; i < kCols; ++i)
-          if (key0 + i > limit) v[i] = -INFINITY;
-      }
-      // Row max of the raw scores (scale > 0 commutes with max), 8 chains.
-      float mx[8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) mx[k] = v[k];
-#pragma unroll
-      for (int i = 8; i < kCols; ++i) mx[i & 7] = fmaxf(mx[i & 7], v[i]);
-      float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                       fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+      float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
       mt = fmaxf(mt, exchange(mt, ok));
       if (!ok) break;
       mt *= a.scale_log2;
@@ -412,32 +432,39 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const ExtendArgs
         }
         tmem_st_wait();
       }
-      // P = exp2(s * scale - m) as bf16 into P region hc (keys hc*64 .. +63).
+      // Pass 2: P = exp2(s * scale - m) as bf16 into P region hc.
       const float neg_m = -m_used;
-      float sum[8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) sum[k] = 0.f;
+      float sum[4] = {0.f, 0.f, 0.f, 0.f};
       const uint32_t prow = sbase + S::kP;
+#pragma unroll 1
+      for (int cb = 0; cb < kCols / 16; ++cb) {
+        float v[16];
+        tmem_ld16(srow + cb * 16, v);
+        tmem_ld_wait();
+        const int kb = key0 + cb * 16;
+        uint32_t w[8];
 #pragma unroll
-      for (int c8 = 0; c8 < kCols / 8; ++c8) {
-        uint32_t w[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int i0 = c8 * 8 + 2 * e;
-          const float p0 = fast_exp2(fmaf(v[i0], a.scale_log2, neg_m));
-          const float p1 = fast_exp2(fmaf(v[i0 + 1], a.scale_log2, neg_m));
-          sum[(2 * e) & 7] += p0;
-          sum[(2 * e + 1) & 7] += p1;
+        for (int e = 0; e < 8; ++e) {
+          const float p0 = kb + 2 * e <= limit ? fast_exp2(fmaf(v[2 * e], a.scale_log2, neg_m)) : 0.f;
+          const float p1 =
+              kb + 2 * e + 1 <= limit ? fast_exp2(fmaf(v[2 * e + 1], a.scale_log2, neg_m)) : 0.f;
+          sum[(2 * e) & 3] += p0;
+          sum[(2 * e + 1) & 3] += p1;
           w[e] = pack_bf16(p0, p1);
         }
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
-                         prow + sw128_offset(kM, r, hc * kCols + c8 * 8)),
+        const int col = hc * kCols + cb * 16;
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(prow + sw128_offset(kM, r, col)),
                      "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3])
                      : "memory");
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
+                         prow + sw128_offset(kM, r, col + 8)),
+                     "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+                     : "memory");
       }
-      l += ((sum[0] + sum[1]) + (sum[2] + sum[3])) + ((sum[4] + sum[5]) + (sum[6] + sum[7]));
-      fence_async_shared();
+      l += (sum[0] + sum[1]) + (sum[2] + sum[3]);
       tc_fence_before_sync();
+      mbar_arrive(bar(kBarSFree + s));  // S tile read: QK^T of tile j + 2 may overwrite it
+      fence_async_shared();
       mbar_arrive(bar(kBarPFull));
     }
     if (ok) l += exchange(l, ok);  // row sum over both column halves
@@ -450,7 +477,7 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const ExtendArgs
       const float inv = l > 0.f ? 1.f / l : 0.f;
       const int64_t orow =
           static_cast<int64_t>(t_base + j0 + t) * a.hq + kvh * a.group + (r % a.group);
-#pragma unroll
+#pragma unroll 1
       for (int cb = 0; cb < kOCols / 32; ++cb) {
         float o[32];
         tmem_ld32(tmem + lane_base + kTmemO + hc * kOCols + cb * 32, o);
@@ -474,10 +501,8 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const ExtendArgs
   }
 
   // Teardown: every role has left its loop (normally or through the abort
-  // flag); wait for this thread's copies, then free TMEM once no MMA is in
-  // flight (the MMA thread's last commit was waited on by the softmax, or
-  // the abort path below waits for it).
-  cp_async_wait<0>();
+  // flag); free TMEM once no MMA is in flight (the MMA thread's last commit
+  // was waited on by the softmax, or the abort path below waits for it).
   if (warp == kMmaWarp && lane == 0 && *abort) {
     // Tracks every MMA this thread issued; they need no other input to finish.
     umma_commit(bar(kBarTeardown));
@@ -492,6 +517,35 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const ExtendArgs
   }
 }
 
+// cuTensorMapEncodeTiled from the driver, looked up once per process.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// A 2-D bf16 tensor of `rows` rows of `cols` elements (row-major), read 4
+// rows x 64 columns at a time with 128-byte swizzle; zeros outside.
+bool gather_map(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {64, 1};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace
 
 cudaError_t launch_extend(const PoolGeom &g, int32_t layer, const void *q,
@@ -502,14 +556,10 @@ cudaError_t launch_extend(const PoolGeom &g, int32_t layer, const void *q,
                           unsigned *err, cudaStream_t stream) {
   (void)sm_count;
   ExtendArgs a{};
-  a.pool = static_cast<const __nv_bfloat16 *>(g.base);
-  a.plane = g.plane;
   a.slots = g.slots;
   a.num_layers = g.num_layers;
   a.layer = layer;
   a.page_size = g.page_size;
-  a.hkv = g.hkv;
-  a.q = static_cast<const __nv_bfloat16 *>(q);
   a.qo_indptr = qo_indptr;
   a.o = static_cast<__nv_bfloat16 *>(o);
   a.lse = lse;
@@ -524,6 +574,13 @@ cudaError_t launch_extend(const PoolGeom &g, int32_t layer, const void *q,
   a.tokens_per_cta = kM / a.group;
   a.scale_log2 = scale * kLog2e;
   a.err = err;
+  const uint64_t pool_rows = 2ull * static_cast<uint64_t>(g.num_layers) * g.slots;
+  const uint64_t q_rows = static_cast<uint64_t>(total_q) * hq;
+  if (pool_rows >= (1ull << 31) || q_rows >= (1ull << 31)) return cudaErrorInvalidValue;
+  CUtensorMap pool_map, q_map;
+  if (!gather_map(&pool_map, g.base, pool_rows, static_cast<uint64_t>(g.hkv) * g.d) ||
+      !gather_map(&q_map, q, q_rows, static_cast<uint64_t>(g.d)))
+    return cudaErrorInvalidValue;
   const int64_t tiles =
       (static_cast<int64_t>(total_q) + a.tokens_per_cta - 1) / a.tokens_per_cta + batch;
   if (tiles > 65535) return cudaErrorInvalidConfiguration;
@@ -533,12 +590,14 @@ cudaError_t launch_extend(const PoolGeom &g, int32_t layer, const void *q,
     e = cudaFuncSetAttribute(extend_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              Smem<128>::kTotal);
     if (e != cudaSuccess) return e;
-    e = launch_pdl(extend_tc_kernel<128>, grid, dim3(kThreads), Smem<128>::kTotal, stream, a);
+    e = launch_pdl(extend_tc_kernel<128>, grid, dim3(kThreads), Smem<128>::kTotal, stream,
+                   pool_map, q_map, a);
   } else {
     e = cudaFuncSetAttribute(extend_tc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              Smem<64>::kTotal);
     if (e != cudaSuccess) return e;
-    e = launch_pdl(extend_tc_kernel<64>, grid, dim3(kThreads), Smem<64>::kTotal, stream, a);
+    e = launch_pdl(extend_tc_kernel<64>, grid, dim3(kThreads), Smem<64>::kTotal, stream,
+                   pool_map, q_map, a);
   }
   return e;
 }

@@ -168,6 +168,12 @@ __device__ __forceinline__ void mbar_init_fence() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
 
+// Arrive on `bar` once every cp.async this thread issued so far has landed
+// (the barrier's expected count already includes this arrival).
+__device__ __forceinline__ void cp_async_mbar_arrive(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
@@ -181,7 +187,7 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
 // Waits until the phase of `bar` with the given parity has completed. Gives
 // up (returns false) after ~2 s or as soon as *abort becomes non-zero, so a
 // broken pipeline ends the kernel with an error flag instead of a hang.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort) {
+__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort) {
   uint64_t t0 = 0;
   for (uint32_t i = 0;; ++i) {
     uint32_t done;
@@ -202,6 +208,26 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
       }
     }
   }
+}
+
+// Arrive on `bar` and add `bytes` to the transaction count its current phase
+// waits for (TMA completions count those bytes down).
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+// TMA gather: rows y0..y3 of a 2-D tensor (box {width, 1}), columns x ..
+// x + width - 1, into shared memory at dst (4 consecutive 128-byte rows with
+// the map's swizzle); out-of-range rows (e.g. -1) read zeros. Completion
+// counts 4 * width * 2 bytes down on `bar`.
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const void *tmap, int x, int y0, int y1,
+                                            int y2, int y3, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(bar)
+      : "memory");
 }
 
 // mbar_wait by every lane of a warp, with a warp-uniform result: code after
