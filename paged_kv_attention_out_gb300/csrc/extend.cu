@@ -10,7 +10,8 @@
 // tokens x the g q heads that read that kv head, so every gathered K/V tile
 // feeds g heads. It walks the visible keys in tiles of 128:
 //   S_j  = Q K_j^T            tcgen05.mma, M=128 N=128 K=D, fp32 in TMEM
-//   P_j  = exp2(scale*S_j - m) softmax warps, bf16 into shared memory
+//   P_j  = exp2(scale*S_j - m) softmax warps, bf16 into one of two shared
+//                             P buffers (the softmax runs a tile ahead of PV)
 //   O   += P_j V_j            tcgen05.mma, M=128 N=D K=128, fp32 in TMEM
 // Roles (416 threads):
 //   warps 0-7  softmax: warp w owns TMEM lanes 32 (w % 4) .. + 31 (query
@@ -57,33 +58,37 @@ struct Smem {
   static constexpr int kQBytes = kM * D * 2;
   static constexpr int kTileBytes = kN * D * 2;
   static constexpr int kKV = kQ + kQBytes;  // stage s: K at kKV + s*2*tile, V after it
-  static constexpr int kP = kKV + 4 * kTileBytes;
+  static constexpr int kP = kKV + 4 * kTileBytes;  // P buffer b at kP + b * kPBytes
   static constexpr int kPBytes = kM * kN * 2;
-  static constexpr int kBars = kP + kPBytes;
+  static constexpr int kBars = kP + 2 * kPBytes;
   // + alignment slack; never below 116 KB, so one CTA (and one 512-column
   // TMEM allocation) per SM even for head_dim 64
   static constexpr int kNeed = kBars + 32 * 8 + 16 + 1024;
   static constexpr int kTotal = kNeed > 116 * 1024 ? kNeed : 116 * 1024;
 };
 
-// TMEM columns: S buffers at 0 and 128, O at 256.
+// TMEM columns: S buffers at 0 and 128, O at 256, and 4 scratch columns at
+// 384 where the two softmax warps of a lane quarter exchange row values.
 constexpr uint32_t kTmemS = 0;
 constexpr uint32_t kTmemO = 256;
+constexpr uint32_t kTmemX = 384;
 
-// Barrier indices.
+// Barrier indices. Every barrier that is waited on with a parity completes
+// at most once between two waits of the same waiter (so a waiter is never
+// two phases behind): per-buffer barriers for everything double-buffered.
 enum : int {
-  kBarKFull = 0,      // [2] producer: K tile landed (TMA bytes)
-  kBarVFull = 2,      // [2] producer: V tile landed (TMA bytes)
+  kBarKFull = 0,      // [2] producers: K tile landed (TMA bytes)
+  kBarVFull = 2,      // [2] producers: V tile landed (TMA bytes)
   kBarKEmpty = 4,     // [2] MMA: K buffer consumed (after QK^T)
   kBarVEmpty = 6,     // [2] MMA: V buffer consumed (after PV)
   kBarSFull = 8,      // [2] MMA: S tile ready
   kBarSFree = 10,     // [2] softmax: S tile read
-  kBarPFull = 12,     // softmax: P written
-  kBarODone = 13,     // MMA: PV finished
-  kBarTeardown = 14,  // MMA: everything issued has finished (abort path)
-  kBarPair = 15,      // [4] softmax: the two warps of a lane quarter exchanged a value
-  kBarQFull = 19,     // producer: Q tile landed (TMA bytes)
-  kBarCount = 20,
+  kBarPFull = 12,     // [2] softmax: P buffer written
+  kBarPFree = 14,     // [2] MMA: PV that read P buffer b finished (and all before it)
+  kBarTeardown = 16,  // MMA: everything issued has finished (abort path)
+  kBarPair = 17,      // [4] softmax: the two warps of a lane quarter exchanged a value
+  kBarQFull = 21,     // producers: Q tile landed (TMA bytes)
+  kBarCount = 22,
 };
 
 struct ExtendArgs {
@@ -125,7 +130,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ int s_req, s_j0, s_c, s_p, s_row;
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
-  __shared__ float s_pair[2][2][kM];  // [parity][column half][row] values exchanged in a pair
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
@@ -199,8 +203,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(kBarSFull + i), 1);
       mbar_init(bar(kBarSFree + i), kSoftmaxWarps * 32);
     }
-    mbar_init(bar(kBarPFull), kSoftmaxWarps * 32);
-    mbar_init(bar(kBarODone), 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(kBarPFull + i), kSoftmaxWarps * 32);
+      mbar_init(bar(kBarPFree + i), 1);
+    }
     mbar_init(bar(kBarTeardown), 1);
     for (int q = 0; q < 4; ++q) mbar_init(bar(kBarPair + q), 64);
     mbar_init(bar(kBarQFull), 2);
@@ -322,15 +328,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       auto pv = [&](int i) -> bool {
         const int s = i & 1;
-        if (!mbar_wait(bar(kBarPFull), i & 1, abort)) return false;
+        if (!mbar_wait(bar(kBarPFull + s), (i >> 1) & 1, abort)) return false;
         if (!mbar_wait(bar(kBarVFull + s), (i >> 1) & 1, abort)) return false;
         tc_fence_after_sync();
         const uint64_t dv = dv0 + s * kStageStep;
+        const uint64_t dpb = dp + s * static_cast<uint64_t>(S::kPBytes >> 4);
 #pragma unroll
         for (int ks = 0; ks < kN / 16; ++ks)
-          umma_bf16_ss(tmem + kTmemO, dp + kstep(ks, kM), dv + ks * (2048 >> 4), idesc_pv,
+          umma_bf16_ss(tmem + kTmemO, dpb + kstep(ks, kM), dv + ks * (2048 >> 4), idesc_pv,
                        (i > 0 || ks > 0) ? 1u : 0u);
-        umma_commit(bar(kBarODone));
+        umma_commit(bar(kBarPFree + s));
         umma_commit(bar(kBarVEmpty + s));
         return true;
       };
@@ -361,7 +368,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Warp w owns TMEM lanes 32 * (w % 4) .. + 31 (query rows) and half
     // hc = w / 4 of the key columns of each S tile (and of the O columns).
     // The two warps of a lane quarter combine their row maxima through
-    // s_pair and an mbarrier each tile.
+    // spare TMEM columns and an mbarrier each tile.
     const int quarter = warp & 3;
     const int hc = warp >> 2;
     const int r = quarter * 32 + lane;  // query row == TMEM lane
@@ -375,13 +382,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     float m_used = -INFINITY, l = 0.f;
     bool ok = true;
     int pair_phase = 0;
-    // Exchange one float with the partner warp (bounded wait; warp-uniform ok).
+    // Exchange one float with the partner warp through a TMEM scratch column
+    // (bounded wait; warp-uniform ok).
     auto exchange = [&](float mine, bool &good) -> float {
-      float *slot = s_pair[pair_phase & 1][0];
-      slot[hc * kM + r] = mine;
+      const uint32_t col = tmem + lane_base + kTmemX + 2 * (pair_phase & 1);
+      tmem_st1(col + hc, mine);
+      tmem_st_wait();
+      tc_fence_before_sync();
       mbar_arrive(pair_bar);
       good = mbar_wait_warp(pair_bar, pair_phase & 1, abort);
-      const float other = good ? slot[(hc ^ 1) * kM + r] : mine;
+      float other = mine;
+      if (good) {
+        tc_fence_after_sync();
+        other = tmem_ld1(col + (hc ^ 1));
+        tmem_ld_wait();
+      }
       ++pair_phase;
       return other;
     };
@@ -407,13 +422,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       mt = fmaxf(mt, exchange(mt, ok));
       if (!ok) break;
       mt *= a.scale_log2;
-      if (j >= 1) {
-        if (!(ok = mbar_wait_warp(bar(kBarODone), (j - 1) & 1, abort))) break;
-        tc_fence_after_sync();
-      }
       if (j == 0) {
         m_used = mt;  // first tile: key 0 is always visible, so mt is finite
       } else if (__any_sync(0xffffffffu, mt > m_used + kRescaleThreshold)) {
+        // O may only change once every PV so far is done: PV_{j-1} finished
+        // implies all earlier ones did (commits track all prior MMAs).
+        if (!(ok = mbar_wait_warp(bar(kBarPFree + ((j - 1) & 1)), ((j - 1) >> 1) & 1, abort)))
+          break;
+        tc_fence_after_sync();
         // Warp-uniform (tcgen05.ld/st are .sync.aligned): every lane rescales
         // its row by its own factor, 1 where the row max did not move.
         const float m_new = fmaxf(m_used, mt);
@@ -432,10 +448,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tmem_st_wait();
       }
-      // Pass 2: P = exp2(s * scale - m) as bf16 into P region hc.
+      // Pass 2: P = exp2(s * scale - m) as bf16 into region hc of P buffer
+      // j & 1, once the PV that last read that buffer (tile j - 2) is done.
+      if (j >= 2) {
+        if (!(ok = mbar_wait_warp(bar(kBarPFree + s), ((j >> 1) - 1) & 1, abort))) break;
+      }
       const float neg_m = -m_used;
       float sum[4] = {0.f, 0.f, 0.f, 0.f};
-      const uint32_t prow = sbase + S::kP;
+      const uint32_t prow = sbase + S::kP + s * S::kPBytes;
 #pragma unroll 1
       for (int cb = 0; cb < kCols / 16; ++cb) {
         float v[16];
@@ -465,10 +485,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before_sync();
       mbar_arrive(bar(kBarSFree + s));  // S tile read: QK^T of tile j + 2 may overwrite it
       fence_async_shared();
-      mbar_arrive(bar(kBarPFull));
+      mbar_arrive(bar(kBarPFull + s));
     }
     if (ok) l += exchange(l, ok);  // row sum over both column halves
-    if (ok && n_tiles > 0) ok = mbar_wait_warp(bar(kBarODone), (n_tiles - 1) & 1, abort);
+    if (ok && n_tiles > 0)
+      ok = mbar_wait_warp(bar(kBarPFree + ((n_tiles - 1) & 1)), ((n_tiles - 1) >> 1) & 1, abort);
     if (!ok) {
       *abort = 1;
       flag_error(a.err, kErrTimeout);
