@@ -206,7 +206,9 @@ class Workload:
         self.ws = None
         if case.kind == "decode":
             n = pkv.pkv_decode_workspace_size(case.B, case.Hq, case.Hkv, case.D, self.hint)
-            self.ws = torch.empty(max(n, 256), dtype=torch.uint8, device=dev)
+        else:
+            n = pkv.pkv_extend_workspace_size(case.B, case.Hkv, case.D, self.hint)
+        self.ws = torch.empty(max(n, 256), dtype=torch.uint8, device=dev)
         self.launches_per_step = None
 
     def store(self):
@@ -222,15 +224,14 @@ class Workload:
         else:
             self.pkv.pkv_paged_extend_attn(self.pool, c.layer, self.q, t["qo_indptr"], self.o,
                                            self.lse, t["page_table"], t["seq_lens"], c.scale,
-                                           table_idx=t.get("table_idx"),
-                                           max_chunk_hint=c.max_chunk)
+                                           self.hint, self.ws, table_idx=t.get("table_idx"))
 
     def kernels_per_step(self) -> int:
         c = self.case
         if c.kind == "extend":
-            return 2
+            return 3  # store, gather, attention
         from paged_kv_attention_out_gb300.binding import load
-        split = self.ws is not None and load().pkv_decode_workspace_size(
+        split = load().pkv_decode_workspace_size(
             c.B, c.Hq, c.Hkv, c.D, self.hint) > 0
         return 3 if split else 2
 

@@ -187,6 +187,17 @@ pkv_status pkv_paged_decode_attn_noalloc(const pkv_pool *pool, int32_t layer, co
                                          int32_t max_seq_len_hint, cudaStream_t stream);
 
 /*
+ * Bytes of device workspace pkv_paged_extend_attn needs: the visible K and V
+ * rows of every request, gathered once out of the paged pool into
+ * contiguous per-(request, kv head) runs, [2][batch][Hkv][S][head_dim] bf16
+ * with S = max_seq_len_hint rounded up to a multiple of 128. Depends only on
+ * these host-side sizes. max_seq_len_hint < 1: no bound known, pass the row
+ * capacity table_stride * page_size instead.
+ */
+size_t pkv_extend_workspace_size(int32_t batch, int32_t num_kv_heads, int32_t head_dim,
+                                 int32_t max_seq_len_hint);
+
+/*
  * Extend (chunked-prefill) attention ("Code Notes: mini-sglang", Scheduler
  * Layer table, PrefillManager row; "Introduction", Key Features, Chunked
  * Prefill and Radix Cache). Request r < batch owns queries qo_indptr[r] ..
@@ -199,14 +210,20 @@ pkv_status pkv_paged_decode_attn_noalloc(const pkv_pool *pool, int32_t layer, co
  * q, o: device bf16 [total_q, Hq, D], 16-byte aligned; lse: device fp32
  * [total_q, Hq] or NULL; qo_indptr: device int32 [batch + 1], qo_indptr[0]
  * = 0, non-decreasing, qo_indptr[batch] = total_q. Other tables as for
- * decode. max_chunk_hint: an upper bound on every c_r, or 0 if unknown.
+ * decode. max_seq_len_hint: a bound on every seq_len of the call (< 1: the
+ * row capacity table_stride * page_size); a request above it is not
+ * computed (its outputs are unspecified) and PKV_DEVERR_SEQ_LEN_RANGE is
+ * flagged. workspace: device, 256-byte aligned, at least
+ * pkv_extend_workspace_size(batch, Hkv, D, max_seq_len_hint) bytes (with the
+ * same effective bound), contents irrelevant on entry.
  */
 pkv_status pkv_paged_extend_attn(const pkv_pool *pool, int32_t layer, const void *q,
                                  const int32_t *qo_indptr, void *o, float *lse,
                                  const int32_t *page_table, int64_t table_stride,
                                  const int32_t *table_idx, const int32_t *seq_lens,
                                  int32_t batch, int32_t total_q, int32_t num_q_heads,
-                                 float scale, int32_t max_chunk_hint, cudaStream_t stream);
+                                 float scale, int32_t max_seq_len_hint, void *workspace,
+                                 size_t workspace_bytes, cudaStream_t stream);
 
 /*
  * Merge of two attention states over disjoint key sets (the log-sum-exp

@@ -70,10 +70,12 @@ def load() -> ctypes.CDLL:
     L.pkv_paged_decode_attn_noalloc.argtypes = [pool_p, _c_int32, _p, _p, _p, _p, _c_int64, _p,
                                                 _p, _c_int32, _c_int32, ctypes.c_float,
                                                 _c_int32, _p]
+    L.pkv_extend_workspace_size.restype = ctypes.c_size_t
+    L.pkv_extend_workspace_size.argtypes = [_c_int32] * 4
     L.pkv_paged_extend_attn.restype = ctypes.c_int
     L.pkv_paged_extend_attn.argtypes = [pool_p, _c_int32, _p, _p, _p, _p, _p, _c_int64, _p, _p,
                                         _c_int32, _c_int32, _c_int32, ctypes.c_float,
-                                        _c_int32, _p]
+                                        _c_int32, _p, ctypes.c_size_t, _p]
     L.pkv_merge_lse.restype = ctypes.c_int
     L.pkv_merge_lse.argtypes = [_p, _p, _p, _p, _p, _c_int32, _p, _c_int64, _c_int32,
                                 _c_int32, _p]
@@ -207,10 +209,17 @@ def pkv_paged_decode_attn_noalloc(pool, layer: int, q, o, lse, page_table, seq_l
         int(max_seq_len_hint), _stream(stream)))
 
 
+def pkv_extend_workspace_size(batch: int, num_kv_heads: int, head_dim: int,
+                              max_seq_len_hint: int) -> int:
+    return int(load().pkv_extend_workspace_size(batch, num_kv_heads, head_dim,
+                                                max_seq_len_hint))
+
+
 def pkv_paged_extend_attn(pool, layer: int, q, qo_indptr, o, lse, page_table, seq_lens,
-                          scale: float, table_idx=None, max_chunk_hint: int = 0,
+                          scale: float, max_seq_len_hint: int, workspace, table_idx=None,
                           stream=None) -> None:
-    """Extend attention; q, o [T, Hq, D] bf16; qo_indptr [B+1]; lse [T, Hq] fp32 or None."""
+    """Extend attention; q, o [T, Hq, D] bf16; qo_indptr [B+1]; lse [T, Hq] fp32 or None;
+    workspace: device tensor of at least pkv_extend_workspace_size(...) bytes."""
     ps = pool_struct(pool)
     _want(q, torch.bfloat16, "q", 3)
     _want(o, torch.bfloat16, "o", 3)
@@ -229,10 +238,13 @@ def pkv_paged_extend_attn(pool, layer: int, q, qo_indptr, o, lse, page_table, se
         _contig(lse, "lse")
     if table_idx is not None:
         _want(table_idx, torch.int32, "table_idx", 1)
+    if workspace is not None:
+        _contig(workspace, "workspace")
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(load().pkv_paged_extend_attn(
         ctypes.byref(ps), int(layer), _ptr(q), _ptr(qo_indptr), _ptr(o), _ptr(lse),
         _ptr(page_table), page_table.shape[1], _ptr(table_idx), _ptr(seq_lens), B, T, Hq,
-        float(scale), int(max_chunk_hint), _stream(stream)))
+        float(scale), int(max_seq_len_hint), _ptr(workspace), ws_bytes, _stream(stream)))
 
 
 def pkv_merge_lse(o_a, lse_a, o_b, lse_b, o_out, lse_out=None, stream=None) -> None:

@@ -6,14 +6,22 @@
 // p_r = seq_len[r] - c_r keys; chunk query j attends to keys 0 .. p_r + j of
 // the request's page_table row (full prefix, causal within the chunk).
 //
+// Two kernels per call:
+//   extend_gather_kernel  copies each request's visible K and V rows, for
+//       every kv head, out of the paged pool into a contiguous run of the
+//       workspace ([2][batch][Hkv][S_pad][D], zero rows up to the next
+//       multiple of 128 keys), reading the pool once per call;
+//   extend_tc_kernel      the attention, which then reads every 128-key K or
+//       V tile with plain 2-D TMA boxes instead of row gathers.
+//
 // Tiling. A CTA owns one 128-row query tile of one kv head: 128 / g chunk
-// tokens x the g q heads that read that kv head, so every gathered K/V tile
-// feeds g heads. It walks the visible keys in tiles of 128:
+// tokens x the g q heads that read that kv head, so every K/V tile feeds g
+// heads. It walks the visible keys in tiles of 128:
 //   S_j  = Q K_j^T            tcgen05.mma, M=128 N=128 K=D, fp32 in TMEM
 //   P_j  = exp2(scale*S_j - m) softmax warps, bf16 into one of two shared
 //                             P buffers (the softmax runs a tile ahead of PV)
 //   O   += P_j V_j            tcgen05.mma, M=128 N=D K=128, fp32 in TMEM
-// Roles (416 threads):
+// Roles (352 threads):
 //   warps 0-7  softmax: warp w owns TMEM lanes 32 (w % 4) .. + 31 (query
 //              rows) and half w / 4 of each row's key columns; online
 //              softmax in the log2 domain with a lazy rescale (O is rescaled
@@ -22,12 +30,11 @@
 //   warp 8     TMEM allocation and the single MMA-issuing thread; S is
 //              double-buffered in TMEM so QK^T of tile j+1 runs while the
 //              softmax works on tile j.
-//   warps 9-12 producers: TMA tile::gather4 loads (4 rows per instruction,
-//              128-byte swizzle, zeros for keys past the end) of the Q rows
-//              and, through the page table, of the K rows (warps 9-10) and V
-//              rows (warps 11-12) of each tile. TMA issue is serialised per
-//              warp, so four warps issue; a K buffer is refilled once its
-//              QK^T is done, a V buffer once its PV is done.
+//   warps 9-10 producers: warp 9 loads the Q rows (TMA tile::gather4, 4 rows
+//              per instruction) and the K tiles, warp 10 the V tiles (2-D
+//              TMA boxes of 128 keys x 64 columns, 128-byte swizzle). A K
+//              buffer is refilled once its QK^T is done, a V buffer once its
+//              PV is done.
 // Every hand-off is an mbarrier; every wait is bounded (tc_common.cuh).
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -46,8 +53,8 @@ constexpr int kM = 128;  // query rows per CTA
 constexpr int kN = 128;  // keys per K/V tile
 constexpr int kSoftmaxWarps = 8;  // two per SM sub-partition: a row's columns are split
 constexpr int kMmaWarp = kSoftmaxWarps;
-constexpr int kProducerWarp = kSoftmaxWarps + 1;  // warps +0, +1: K (and Q); +2, +3: V
-constexpr int kProducerWarps = 4;
+constexpr int kProducerWarp = kSoftmaxWarps + 1;  // warp +0: Q and K; +1: V
+constexpr int kProducerWarps = 2;
 constexpr int kThreads = (kSoftmaxWarps + 1 + kProducerWarps) * 32;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
@@ -77,8 +84,8 @@ constexpr uint32_t kTmemX = 384;
 // at most once between two waits of the same waiter (so a waiter is never
 // two phases behind): per-buffer barriers for everything double-buffered.
 enum : int {
-  kBarKFull = 0,      // [2] producers: K tile landed (TMA bytes)
-  kBarVFull = 2,      // [2] producers: V tile landed (TMA bytes)
+  kBarKFull = 0,      // [2] producer: K tile landed (TMA bytes)
+  kBarVFull = 2,      // [2] producer: V tile landed (TMA bytes)
   kBarKEmpty = 4,     // [2] MMA: K buffer consumed (after QK^T)
   kBarVEmpty = 6,     // [2] MMA: V buffer consumed (after PV)
   kBarSFull = 8,      // [2] MMA: S tile ready
@@ -87,30 +94,113 @@ enum : int {
   kBarPFree = 14,     // [2] MMA: PV that read P buffer b finished (and all before it)
   kBarTeardown = 16,  // MMA: everything issued has finished (abort path)
   kBarPair = 17,      // [4] softmax: the two warps of a lane quarter exchanged a value
-  kBarQFull = 21,     // producers: Q tile landed (TMA bytes)
+  kBarQFull = 21,     // producer: Q tile landed (TMA bytes)
   kBarCount = 22,
 };
 
-struct ExtendArgs {
-  int64_t slots;         // pool slots per (c, layer) plane
+struct GatherArgs {
+  const __nv_bfloat16 *pool;  // plane (c, layer) starts at ((c * L + layer) * slots) rows
+  int64_t slots;
   int32_t num_layers;
   int32_t layer;
   int32_t page_size;
-  const int32_t *qo_indptr;
-  __nv_bfloat16 *o;
-  float *lse;
+  int32_t hkv;
   const int32_t *page_table;
   int64_t table_stride;
   const int32_t *table_idx;
   const int32_t *seq_lens;
   int32_t batch;
+  int32_t capacity;  // bound on every seq_len of the call
+  int32_t s_pad;     // capacity rounded up to 128: keys per workspace run
+  __nv_bfloat16 *ws;
+  unsigned *err;
+};
+
+struct ExtendArgs {
+  const int32_t *qo_indptr;
+  __nv_bfloat16 *o;
+  float *lse;
+  const int32_t *seq_lens;
+  int32_t batch;
+  int32_t hkv;
   int32_t total_q;
   int32_t hq;
   int32_t group;
   int32_t tokens_per_cta;  // floor(128 / group)
+  int32_t capacity;
+  int32_t s_pad;
   float scale_log2;
   unsigned *err;
 };
+
+constexpr int kGatherKeys = 32;     // keys per gather CTA
+constexpr int kGatherThreads = 256;
+
+// Workspace run of request r, kv head h, K (c = 0) or V (c = 1): s_pad rows
+// of D elements starting at row ((c * batch + r) * hkv + h) * s_pad. Rows
+// seq_len .. (seq_len rounded up to 128) - 1 are written as zeros so a tile
+// never holds stale bits (a NaN there would survive P = 0 in P V).
+template <int D>
+__global__ void __launch_bounds__(kGatherThreads)
+    extend_gather_kernel(const GatherArgs a) {
+  grid_dependency_wait();  // the chunk's K/V may come from the previous kernel (store_kv)
+  grid_dependents_launch();
+  const int r = blockIdx.y;
+  const int seq = a.seq_lens[r];
+  if (seq < 0 || seq > a.capacity) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) flag_error(a.err, kErrSeqLen);
+    return;
+  }
+  const int key0 = static_cast<int>(blockIdx.x) * kGatherKeys;
+  const int n_pad = (seq + 127) & ~127;
+  if (key0 >= n_pad) return;
+  const int row = a.table_idx ? a.table_idx[r] : r;
+  if (row < 0) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) flag_error(a.err, kErrTableIdx);
+    return;
+  }
+  const int32_t *row_pages = a.page_table + static_cast<int64_t>(row) * a.table_stride;
+  constexpr int kChunks = D / 8;  // 16-byte chunks per head row
+  const int per_kc = a.hkv * kChunks;  // chunks per (key, K or V)
+  const int total = kGatherKeys * 2 * per_kc;
+  const int64_t row_elems = static_cast<int64_t>(a.hkv) * D;
+  const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+  constexpr int kUnroll = 4;
+  for (int base = threadIdx.x; base < total; base += kGatherThreads * kUnroll) {
+    uint4 v[kUnroll];
+    uint4 *dst[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int i = base + u * kGatherThreads;
+      dst[u] = nullptr;
+      if (i >= total) continue;
+      const int kc = i / per_kc;  // (key, c) pair
+      const int rem = i - kc * per_kc;
+      const int h = rem / kChunks;
+      const int ch = rem - h * kChunks;
+      const int key = key0 + (kc >> 1);
+      const int c = kc & 1;
+      dst[u] = reinterpret_cast<uint4 *>(
+          a.ws + ((static_cast<int64_t>(c) * a.batch + r) * a.hkv + h) * a.s_pad * D +
+          static_cast<int64_t>(key) * D + ch * 8);
+      v[u] = zero;
+      if (key < seq) {
+        const int pidx = key / a.page_size;
+        const int ent = __ldg(row_pages + pidx);
+        const int64_t slot = static_cast<int64_t>(ent) * a.page_size + (key - pidx * a.page_size);
+        if (ent >= 0 && slot < a.slots) {
+          const int64_t prow = (static_cast<int64_t>(c) * a.num_layers + a.layer) * a.slots + slot;
+          v[u] = __ldg(reinterpret_cast<const uint4 *>(a.pool + prow * row_elems + h * D + ch * 8));
+        } else if (c == 0 && h == 0 && ch == 0) {
+          flag_error(a.err, kErrPage);
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u)
+      if (dst[u]) *dst[u] = v[u];
+  }
+}
 
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;
@@ -118,16 +208,16 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
-// pool_map: the pool as a 2-D bf16 tensor [2 * L * slots rows][Hkv * D]
-// (row (c * L + layer) * slots + slot); q_map: q as [total_q * Hq rows][D].
-// Both with box {64, 1} and 128-byte swizzle.
+// kv_map: the workspace as a 2-D bf16 tensor [2 * batch * Hkv * s_pad rows][D],
+// box {64, 128}; q_map: q as [total_q * Hq rows][D], box {64, 1}. Both with
+// 128-byte swizzle.
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
-    extend_tc_kernel(const __grid_constant__ CUtensorMap pool_map,
+    extend_tc_kernel(const __grid_constant__ CUtensorMap kv_map,
                      const __grid_constant__ CUtensorMap q_map, const ExtendArgs a) {
   using S = Smem<D>;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ int s_req, s_j0, s_c, s_p, s_row;
+  __shared__ int s_req, s_j0, s_c, s_p;
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
   const int tid = threadIdx.x;
@@ -135,12 +225,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = tid & 31;
   const int kvh = blockIdx.x;
 
-  grid_dependency_wait();  // the chunk's K/V may come from the previous kernel (store_kv)
+  grid_dependency_wait();  // K/V come from the gather kernel
   if (tid == 0) {
     // Which (request, token tile) this CTA owns; tiles are taken from the end.
     const int tile = static_cast<int>(gridDim.y) - 1 - static_cast<int>(blockIdx.y);
     int acc = 0;
-    int req = -1, j0 = 0, c = 0, p = 0, row = 0;
+    int req = -1, j0 = 0, c = 0, p = 0;
     for (int r = 0; r < a.batch; ++r) {
       const int beg = a.qo_indptr[r];
       const int end = a.qo_indptr[r + 1];
@@ -155,17 +245,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         j0 = (tile - acc) * a.tokens_per_cta;
         c = cr;
         p = a.seq_lens[r] - cr;
-        row = a.table_idx ? a.table_idx[r] : r;
         break;
       }
       acc += nt;
     }
     if (req >= 0) {
-      const int64_t max_keys = a.table_stride * a.page_size;
-      if (p < 0 || static_cast<int64_t>(p) + c > max_keys || row < 0) {
-        if (kvh == 0) {
-          flag_error(a.err, p < 0 ? kErrIndptr : (row < 0 ? kErrTableIdx : kErrSeqLen));
-        }
+      // seq_len above the workspace capacity: flagged by the gather kernel
+      if (p < 0 || p + c > a.capacity) {
+        if (kvh == 0 && p < 0) flag_error(a.err, kErrIndptr);
         req = -1;
       }
     }
@@ -173,7 +260,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     s_j0 = j0;
     s_c = c;
     s_p = p;
-    s_row = row;
     s_abort = 0;
   }
   __syncthreads();
@@ -188,7 +274,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int *abort = &s_abort;
 
   const int j0 = s_j0, c = s_c, p = s_p;
-  const int32_t *row_pages = a.page_table + static_cast<int64_t>(s_row) * a.table_stride;
   const int t_base = a.qo_indptr[req];
   const int tokens = min(a.tokens_per_cta, c - j0);
   const int n_keys = p + j0 + tokens;  // keys the last token of the tile sees
@@ -196,8 +281,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (tid == 0) {
     for (int i = 0; i < 2; ++i) {
-      mbar_init(bar(kBarKFull + i), 2);  // one expect_tx arrival per issuing warp
-      mbar_init(bar(kBarVFull + i), 2);
+      mbar_init(bar(kBarKFull + i), 1);  // the producer's expect_tx arrival
+      mbar_init(bar(kBarVFull + i), 1);
       mbar_init(bar(kBarKEmpty + i), 1);
       mbar_init(bar(kBarVEmpty + i), 1);
       mbar_init(bar(kBarSFull + i), 1);
@@ -209,7 +294,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(bar(kBarTeardown), 1);
     for (int q = 0; q < 4; ++q) mbar_init(bar(kBarPair + q), 64);
-    mbar_init(bar(kBarQFull), 2);
+    mbar_init(bar(kBarQFull), 1);
     mbar_init_fence();
   }
   if (warp == kMmaWarp) tmem_alloc(smem_addr(&s_tmem), kTmemCols);
@@ -220,87 +305,48 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp >= kProducerWarp) {
     // ------------------------------------------------------------ producers
-    // Producer warp pw (0..3): pw 0-1 load Q and K tiles, pw 2-3 V tiles.
-    // In a tile, warp w2 = pw & 1 covers row groups 16 w2 .. 16 w2 + 15
-    // (4 rows each); lane l takes group 16 w2 + (l & 15) and 64-column half
-    // l >> 4. Rows that must read as zero (past the end, bad page ids) get
-    // row -1.
+    // Warp 0 of the two loads Q (lane l: rows 4 l .. 4 l + 3, all 64-column
+    // halves; rows past the tile's tokens read as zeros) and then the K
+    // tiles; warp 1 the V tiles. Lane 0 issues the tile loads.
     const int pw = warp - kProducerWarp;
-    const bool is_k = pw < 2;
-    const int grp = 16 * (pw & 1) + (lane & 15);
-    const int h = lane >> 4;
+    const bool is_k = pw == 0;
     constexpr int kHalves = D / 64;
-    const bool active = h < kHalves;
-    const int P = a.page_size;
-    const int plane = (is_k ? 0 : a.num_layers) + a.layer;
-    const int plane_base = plane * static_cast<int>(a.slots);
-    const int xcol = kvh * D + h * 64;
-    // destination of rows 4 grp .. 4 grp + 3 inside a SW128 region
-    const uint32_t row_off =
-        static_cast<uint32_t>(h * (kN * 128) + (grp >> 1) * 1024 + (grp & 1) * 512);
-    constexpr uint32_t kWarpBytes = S::kTileBytes / 2;  // each of the two warps' share
     bool ok = true;
     if (is_k) {
       int qr[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const int r = 4 * grp + e;
+        const int r = 4 * lane + e;
         const int t = r / a.group;
         qr[e] = t < tokens ? (t_base + j0 + t) * a.hq + kvh * a.group + (r % a.group) : -1;
       }
-      if (lane == 0) mbar_arrive_expect_tx(bar(kBarQFull), S::kQBytes / 2);
+      if (lane == 0) mbar_arrive_expect_tx(bar(kBarQFull), S::kQBytes);
       __syncwarp();
-      if (active)
-        tma_gather4(sbase + S::kQ + static_cast<uint32_t>(h * (kM * 128) + (grp >> 1) * 1024 +
-                                                         (grp & 1) * 512),
+#pragma unroll
+      for (int h = 0; h < kHalves; ++h)
+        tma_gather4(sbase + S::kQ + static_cast<uint32_t>(h * (kM * 128) + (lane >> 1) * 1024 +
+                                                         (lane & 1) * 512),
                     &q_map, h * 64, qr[0], qr[1], qr[2], qr[3], bar(kBarQFull));
     }
-    // Pool rows of this lane's 4 keys of tile j (-1 where the key is past
-    // the end or its page id is out of range): one division per tile, then
-    // the keys walk through the page.
-    auto rows_of = [&](int j, int (&rr)[4]) {
-      const int k0 = j * kN + 4 * grp;
-      int pidx = k0 / P;
-      int off = k0 - pidx * P;
-      int ent = -1, ent_idx = -1;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        if (off == P) {
-          ++pidx;
-          off = 0;
-        }
-        rr[e] = -1;
-        if (k0 + e < n_keys) {
-          if (pidx != ent_idx) {
-            ent = __ldg(row_pages + pidx);
-            ent_idx = pidx;
-          }
-          const long long sl = static_cast<long long>(ent) * P + off;
-          if (ent >= 0 && sl < a.slots) {
-            rr[e] = plane_base + static_cast<int>(sl);
-          } else if (is_k && h == 0) {
-            flag_error(a.err, kErrPage);
-          }
-        }
-        ++off;
-      }
-    };
     const int full_bar = is_k ? kBarKFull : kBarVFull;
     const int empty_bar = is_k ? kBarKEmpty : kBarVEmpty;
-    const int buf_off = is_k ? 0 : S::kTileBytes;
-    int rr[4];
-    rows_of(0, rr);
+    const uint32_t buf_off = is_k ? 0u : static_cast<uint32_t>(S::kTileBytes);
+    // first workspace row of this (K or V, request, kv head) run
+    const int run0 =
+        ((is_k ? 0 : a.batch) + req) * a.hkv * a.s_pad + kvh * a.s_pad;
     int issued = 0;
     for (int j = 0; j < n_tiles; ++j) {
       const int s = j & 1;
       if (j >= 2 && !(ok = mbar_wait_warp(bar(empty_bar + s), ((j >> 1) - 1) & 1, abort))) break;
-      if (lane == 0) mbar_arrive_expect_tx(bar(full_bar + s), kWarpBytes);
+      if (lane == 0) {
+        const uint32_t dst = sbase + S::kKV + s * 2 * S::kTileBytes + buf_off;
+        mbar_arrive_expect_tx(bar(full_bar + s), S::kTileBytes);
+#pragma unroll
+        for (int h = 0; h < kHalves; ++h)
+          tma_load_2d(dst + h * (kN * 128), &kv_map, h * 64, run0 + j * kN, bar(full_bar + s));
+      }
       __syncwarp();
-      if (active)
-        tma_gather4(sbase + S::kKV + s * 2 * S::kTileBytes + buf_off + row_off, &pool_map, xcol,
-                    rr[0], rr[1], rr[2], rr[3], bar(full_bar + s));
       ++issued;
-      if (j + 1 < n_tiles) rows_of(j + 1, rr);
     }
     if (!ok) *abort = 1;
     if (*abort && lane == 0) {
@@ -553,14 +599,15 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-// A 2-D bf16 tensor of `rows` rows of `cols` elements (row-major), read 4
-// rows x 64 columns at a time with 128-byte swizzle; zeros outside.
-bool gather_map(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols) {
+// A 2-D bf16 tensor of `rows` rows of `cols` elements (row-major), read in
+// boxes of box_rows rows x 64 columns with 128-byte swizzle (box_rows = 1 for
+// tile::gather4); zeros outside.
+bool bf16_map(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
   if (!enc) return false;
   cuuint64_t dims[2] = {cols, rows};
   cuuint64_t strides[1] = {cols * 2};
-  cuuint32_t box[2] = {64, 1};
+  cuuint32_t box[2] = {64, box_rows};
   cuuint32_t estr[2] = {1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box,
              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -569,56 +616,84 @@ bool gather_map(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols) 
 
 }  // namespace
 
+int64_t extend_s_pad(int32_t capacity) { return (static_cast<int64_t>(capacity) + 127) & ~int64_t(127); }
+
+size_t extend_workspace_bytes(int32_t batch, int32_t hkv, int32_t d, int32_t capacity) {
+  return 2ull * static_cast<uint64_t>(batch) * static_cast<uint64_t>(hkv) *
+         static_cast<uint64_t>(extend_s_pad(capacity)) * static_cast<uint64_t>(d) * 2ull;
+}
+
 cudaError_t launch_extend(const PoolGeom &g, int32_t layer, const void *q,
                           const int32_t *qo_indptr, void *o, float *lse,
                           const int32_t *page_table, int64_t table_stride,
                           const int32_t *table_idx, const int32_t *seq_lens, int32_t batch,
-                          int32_t total_q, int32_t hq, float scale, int32_t sm_count,
-                          unsigned *err, cudaStream_t stream) {
+                          int32_t total_q, int32_t hq, float scale, int32_t capacity,
+                          void *workspace, int32_t sm_count, unsigned *err, cudaStream_t stream) {
   (void)sm_count;
+  const int64_t s_pad = extend_s_pad(capacity);
+  const uint64_t ws_rows = 2ull * static_cast<uint64_t>(batch) * g.hkv * s_pad;
+  const uint64_t q_rows = static_cast<uint64_t>(total_q) * hq;
+  if (ws_rows >= (1ull << 31) || q_rows >= (1ull << 31)) return cudaErrorInvalidValue;
+
+  GatherArgs ga{};
+  ga.pool = static_cast<const __nv_bfloat16 *>(g.base);
+  ga.slots = g.slots;
+  ga.num_layers = g.num_layers;
+  ga.layer = layer;
+  ga.page_size = g.page_size;
+  ga.hkv = g.hkv;
+  ga.page_table = page_table;
+  ga.table_stride = table_stride;
+  ga.table_idx = table_idx;
+  ga.seq_lens = seq_lens;
+  ga.batch = batch;
+  ga.capacity = capacity;
+  ga.s_pad = static_cast<int32_t>(s_pad);
+  ga.ws = static_cast<__nv_bfloat16 *>(workspace);
+  ga.err = err;
+
   ExtendArgs a{};
-  a.slots = g.slots;
-  a.num_layers = g.num_layers;
-  a.layer = layer;
-  a.page_size = g.page_size;
   a.qo_indptr = qo_indptr;
   a.o = static_cast<__nv_bfloat16 *>(o);
   a.lse = lse;
-  a.page_table = page_table;
-  a.table_stride = table_stride;
-  a.table_idx = table_idx;
   a.seq_lens = seq_lens;
   a.batch = batch;
+  a.hkv = g.hkv;
   a.total_q = total_q;
   a.hq = hq;
   a.group = hq / g.hkv;
   a.tokens_per_cta = kM / a.group;
+  a.capacity = capacity;
+  a.s_pad = static_cast<int32_t>(s_pad);
   a.scale_log2 = scale * kLog2e;
   a.err = err;
-  const uint64_t pool_rows = 2ull * static_cast<uint64_t>(g.num_layers) * g.slots;
-  const uint64_t q_rows = static_cast<uint64_t>(total_q) * hq;
-  if (pool_rows >= (1ull << 31) || q_rows >= (1ull << 31)) return cudaErrorInvalidValue;
-  CUtensorMap pool_map, q_map;
-  if (!gather_map(&pool_map, g.base, pool_rows, static_cast<uint64_t>(g.hkv) * g.d) ||
-      !gather_map(&q_map, q, q_rows, static_cast<uint64_t>(g.d)))
+  CUtensorMap kv_map, q_map;
+  if (!bf16_map(&kv_map, workspace, ws_rows, static_cast<uint64_t>(g.d), kN) ||
+      !bf16_map(&q_map, q, q_rows, static_cast<uint64_t>(g.d), 1))
     return cudaErrorInvalidValue;
   const int64_t tiles =
       (static_cast<int64_t>(total_q) + a.tokens_per_cta - 1) / a.tokens_per_cta + batch;
-  if (tiles > 65535) return cudaErrorInvalidConfiguration;
+  if (tiles > 65535 || batch > 65535) return cudaErrorInvalidConfiguration;
+  const dim3 ggrid(static_cast<unsigned>((s_pad + kGatherKeys - 1) / kGatherKeys),
+                   static_cast<unsigned>(batch));
   const dim3 grid(g.hkv, static_cast<unsigned>(tiles));
   cudaError_t e;
   if (g.d == 128) {
+    e = launch_pdl(extend_gather_kernel<128>, ggrid, dim3(kGatherThreads), 0, stream, ga);
+    if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(extend_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              Smem<128>::kTotal);
     if (e != cudaSuccess) return e;
     e = launch_pdl(extend_tc_kernel<128>, grid, dim3(kThreads), Smem<128>::kTotal, stream,
-                   pool_map, q_map, a);
+                   kv_map, q_map, a);
   } else {
+    e = launch_pdl(extend_gather_kernel<64>, ggrid, dim3(kGatherThreads), 0, stream, ga);
+    if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(extend_tc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              Smem<64>::kTotal);
     if (e != cudaSuccess) return e;
     e = launch_pdl(extend_tc_kernel<64>, grid, dim3(kThreads), Smem<64>::kTotal, stream,
-                   pool_map, q_map, a);
+                   kv_map, q_map, a);
   }
   return e;
 }

@@ -217,13 +217,19 @@ pkv_status pkv_paged_decode_attn(const pkv_pool *pool, int32_t layer, const void
   return e == cudaSuccess ? PKV_OK : cuda_fail(e, "decode launch");
 }
 
+size_t pkv_extend_workspace_size(int32_t batch, int32_t num_kv_heads, int32_t head_dim,
+                                 int32_t max_seq_len_hint) {
+  if (batch <= 0 || num_kv_heads <= 0 || head_dim <= 0 || max_seq_len_hint < 1) return 0;
+  return pkv::extend_workspace_bytes(batch, num_kv_heads, head_dim, max_seq_len_hint);
+}
+
 pkv_status pkv_paged_extend_attn(const pkv_pool *pool, int32_t layer, const void *q,
                                  const int32_t *qo_indptr, void *o, float *lse,
                                  const int32_t *page_table, int64_t table_stride,
                                  const int32_t *table_idx, const int32_t *seq_lens,
                                  int32_t batch, int32_t total_q, int32_t num_q_heads,
-                                 float scale, int32_t max_chunk_hint, cudaStream_t stream) {
-  (void)max_chunk_hint;
+                                 float scale, int32_t max_seq_len_hint, void *workspace,
+                                 size_t workspace_bytes, cudaStream_t stream) {
   pkv::PoolGeom g;
   pkv_status s = check_pool(pool, layer, &g);
   if (s != PKV_OK) return s;
@@ -244,6 +250,20 @@ pkv_status pkv_paged_extend_attn(const pkv_pool *pool, int32_t layer, const void
   if (!aligned(page_table, 4) || !aligned(seq_lens, 4) || !aligned(lse, 4) ||
       !aligned(table_idx, 4) || !aligned(qo_indptr, 4))
     return fail(PKV_ERR_INVALID_ARG, "int32/fp32 tables must be 4-byte aligned");
+  const int64_t row_capacity = table_stride * g.page_size;
+  int64_t cap = max_seq_len_hint >= 1 ? max_seq_len_hint : row_capacity;
+  if (cap > row_capacity) cap = row_capacity;
+  if (cap > (int64_t(1) << 30)) return fail(PKV_ERR_UNSUPPORTED, "sequence capacity too large");
+  const size_t need = pkv::extend_workspace_bytes(batch, g.hkv, g.d, static_cast<int32_t>(cap));
+  if (!workspace)
+    return fail(PKV_ERR_WORKSPACE_TOO_SMALL, "workspace is NULL, %zu bytes needed", need);
+  if (workspace_bytes < need)
+    return fail(PKV_ERR_WORKSPACE_TOO_SMALL, "workspace %zu bytes, %zu needed", workspace_bytes,
+                need);
+  if (!aligned(workspace, 256)) return fail(PKV_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  if (2 * static_cast<int64_t>(batch) * g.hkv * pkv::extend_s_pad(static_cast<int32_t>(cap)) >=
+      (int64_t(1) << 31))
+    return fail(PKV_ERR_UNSUPPORTED, "extend: batch x kv heads x capacity too large");
   const int64_t tpc = 128 / group;  // chunk tokens per 128-row query tile
   if ((static_cast<int64_t>(total_q) + tpc - 1) / tpc + batch > 65535)
     return fail(PKV_ERR_UNSUPPORTED, "extend: too many query tiles in one call");
@@ -251,7 +271,8 @@ pkv_status pkv_paged_extend_attn(const pkv_pool *pool, int32_t layer, const void
   if ((s = device_info(&d)) != PKV_OK) return s;
   cudaError_t e = pkv::launch_extend(g, layer, q, qo_indptr, o, lse, page_table, table_stride,
                                      table_idx, seq_lens, batch, total_q, num_q_heads, scale,
-                                     d->sm_count, d->err, stream);
+                                     static_cast<int32_t>(cap), workspace, d->sm_count, d->err,
+                                     stream);
   return e == cudaSuccess ? PKV_OK : cuda_fail(e, "extend launch");
 }
 

@@ -42,12 +42,17 @@ cudaError_t launch_decode(const PoolGeom &g, int32_t layer, const void *q, void 
                           int32_t hq, float scale, const DecodePlan &plan, void *workspace,
                           unsigned *err, cudaStream_t stream);
 
+// Gathered-K/V workspace of the extend call: [2][batch][hkv][s_pad][d] bf16,
+// s_pad = capacity rounded up to 128.
+int64_t extend_s_pad(int32_t capacity);
+size_t extend_workspace_bytes(int32_t batch, int32_t hkv, int32_t d, int32_t capacity);
+
 cudaError_t launch_extend(const PoolGeom &g, int32_t layer, const void *q,
                           const int32_t *qo_indptr, void *o, float *lse,
                           const int32_t *page_table, int64_t table_stride,
                           const int32_t *table_idx, const int32_t *seq_lens, int32_t batch,
-                          int32_t total_q, int32_t hq, float scale, int32_t sm_count,
-                          unsigned *err, cudaStream_t stream);
+                          int32_t total_q, int32_t hq, float scale, int32_t capacity,
+                          void *workspace, int32_t sm_count, unsigned *err, cudaStream_t stream);
 
 cudaError_t launch_merge(const float *o_a, const float *lse_a, const float *o_b,
                          const float *lse_b, void *o_out, bool out_bf16, float *lse_out,

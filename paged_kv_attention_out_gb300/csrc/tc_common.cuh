@@ -243,6 +243,18 @@ __device__ __forceinline__ void tma_gather4(uint32_t dst, const void *tmap, int 
       : "memory");
 }
 
+// TMA tile load: the box at column x, row y of a 2-D tensor into shared
+// memory at dst (box rows of 128 bytes with the map's swizzle). Completion
+// counts the box's bytes down on `bar`.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, int x, int y,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
 // mbar_wait by every lane of a warp, with a warp-uniform result: code after
 // it may use .sync.aligned instructions (tcgen05.ld/st) safely.
 __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, volatile int *abort) {

@@ -117,9 +117,11 @@ def gpu_attention(case: W.Case, pool, q, t, hint=None, with_lse=True, table_idx=
         pkv.pkv_paged_decode_attn(pool, case.layer, q, o, lse, t["page_table"], t["seq_lens"],
                                   case.scale, h, ws, table_idx=ti)
     else:
+        h = case.max_seq_len if hint is None else hint
+        n = pkv.pkv_extend_workspace_size(case.B, case.Hkv, case.D, h)
+        ws = torch.empty(max(n, 1), dtype=torch.uint8, device=q.device)
         pkv.pkv_paged_extend_attn(pool, case.layer, q, t["qo_indptr"], o, lse, t["page_table"],
-                                  t["seq_lens"], case.scale, table_idx=ti,
-                                  max_chunk_hint=case.max_chunk)
+                                  t["seq_lens"], case.scale, h, ws, table_idx=ti)
     return o, lse
 
 

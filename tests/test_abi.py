@@ -31,7 +31,8 @@ def lib():
 def test_header_declares_the_entry_points():
     names = declared_functions()
     for want in ("pkv_kv_store", "pkv_paged_decode_attn", "pkv_paged_extend_attn",
-                 "pkv_merge_lse", "pkv_decode_workspace_size", "pkv_status_string",
+                 "pkv_merge_lse", "pkv_decode_workspace_size", "pkv_extend_workspace_size",
+                 "pkv_status_string",
                  "pkv_last_error", "pkv_init", "pkv_read_device_errors"):
         assert want in names
 
@@ -44,7 +45,8 @@ def test_library_exports_every_declared_symbol(lib):
 def test_python_binding_has_the_same_names(lib):
     import paged_kv_attention_out_gb300 as pkv
     for n in ("pkv_kv_store", "pkv_paged_decode_attn", "pkv_paged_extend_attn",
-              "pkv_merge_lse", "pkv_decode_workspace_size", "pkv_init",
+              "pkv_merge_lse", "pkv_decode_workspace_size", "pkv_extend_workspace_size",
+              "pkv_init",
               "pkv_read_device_errors"):
         assert callable(getattr(pkv, n))
 
