@@ -16,20 +16,23 @@
 //
 // Tiling. A CTA owns one 128-row query tile of one kv head: 128 / g chunk
 // tokens x the g q heads that read that kv head, so every K/V tile feeds g
-// heads. It walks the visible keys in tiles of 128:
-//   S_j  = Q K_j^T            tcgen05.mma, M=128 N=128 K=D, fp32 in TMEM
-//   P_j  = exp2(scale*S_j - m) softmax warps, bf16 into one of two shared
-//                             P buffers (the softmax runs a tile ahead of PV)
-//   O   += P_j V_j            tcgen05.mma, M=128 N=D K=128, fp32 in TMEM
+// heads. It walks the visible keys in tiles of 128, alternating between two
+// independent online-softmax states ("groups"), so the two never wait on
+// each other and their softmax work overlaps the tensor core's:
+//   S_j  = Q K_j^T            tcgen05.mma, M=128 N=128 K=D, fp32 into TMEM
+//                             buffer j % 2
+//   P_j  = exp2(scale*S_j - m) softmax group j % 2, bf16 into shared P
+//                             buffer j % 2
+//   O_{j%2} += P_j V_j         tcgen05.mma, M=128 N=D K=128, fp32 in TMEM
+// and at the end merges the two (m, l, O) states like a two-way split.
 // Roles (352 threads):
-//   warps 0-7  softmax: warp w owns TMEM lanes 32 (w % 4) .. + 31 (query
-//              rows) and half w / 4 of each row's key columns; online
-//              softmax in the log2 domain with a lazy rescale (O is rescaled
-//              only when a row max grows by more than 2^8), masks only on
-//              tiles that cross a row's last key, then O / l -> bf16 and lse.
-//   warp 8     TMEM allocation and the single MMA-issuing thread; S is
-//              double-buffered in TMEM so QK^T of tile j+1 runs while the
-//              softmax works on tile j.
+//   warps 0-7  softmax: group g = warp / 4; warp w owns TMEM lanes
+//              32 (w % 4) .. + 31 (query rows), one whole row per thread;
+//              log2-domain online softmax with a lazy rescale (O_g is
+//              rescaled only when a row max grows by more than 2^8), masks
+//              only on tiles that cross some row's last key; then the
+//              merge, O / l -> bf16, lse.
+//   warp 8     TMEM allocation and the single MMA-issuing thread.
 //   warps 9-10 producers: warp 9 loads the Q rows (TMA tile::gather4, 4 rows
 //              per instruction) and the K tiles, warp 10 the V tiles (2-D
 //              TMA boxes of 128 keys x 64 columns, 128-byte swizzle). A K
@@ -74,11 +77,10 @@ struct Smem {
   static constexpr int kTotal = kNeed > 116 * 1024 ? kNeed : 116 * 1024;
 };
 
-// TMEM columns: S buffers at 0 and 128, O at 256, and 4 scratch columns at
-// 384 where the two softmax warps of a lane quarter exchange row values.
+// TMEM columns: S buffer g at 128 g, O accumulator g at 256 + D g (one per
+// softmax group).
 constexpr uint32_t kTmemS = 0;
 constexpr uint32_t kTmemO = 256;
-constexpr uint32_t kTmemX = 384;
 
 // Barrier indices. Every barrier that is waited on with a parity completes
 // at most once between two waits of the same waiter (so a waiter is never
@@ -88,14 +90,13 @@ enum : int {
   kBarVFull = 2,      // [2] producer: V tile landed (TMA bytes)
   kBarKEmpty = 4,     // [2] MMA: K buffer consumed (after QK^T)
   kBarVEmpty = 6,     // [2] MMA: V buffer consumed (after PV)
-  kBarSFull = 8,      // [2] MMA: S tile ready
-  kBarSFree = 10,     // [2] softmax: S tile read
-  kBarPFull = 12,     // [2] softmax: P buffer written
-  kBarPFree = 14,     // [2] MMA: PV that read P buffer b finished (and all before it)
+  kBarSFull = 8,      // [2] MMA: S tile ready in TMEM buffer g
+  kBarSFree = 10,     // [2] softmax group g: S buffer g read
+  kBarPFull = 12,     // [2] softmax group g: P buffer g written (and O_g rescaled)
+  kBarPFree = 14,     // [2] MMA: the PV that read P buffer g finished (and all MMAs before it)
   kBarTeardown = 16,  // MMA: everything issued has finished (abort path)
-  kBarPair = 17,      // [4] softmax: the two warps of a lane quarter exchanged a value
-  kBarQFull = 21,     // producer: Q tile landed (TMA bytes)
-  kBarCount = 22,
+  kBarQFull = 17,     // producer: Q tile landed (TMA bytes)
+  kBarCount = 18,
 };
 
 struct GatherArgs {
@@ -208,6 +209,33 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
+__device__ __forceinline__ float max3f(float x, float y, float z) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(x), "f"(y), "f"(z));
+  return r;
+}
+
+// (y0, y1) = (x0, x1) * s + c, one packed fp32 instruction.
+__device__ __forceinline__ void fma2(float &y0, float &y1, float x0, float x1, float s, float c) {
+  asm("{\n .reg .b64 x, m, a, y;\n mov.b64 x, {%2, %3};\n mov.b64 m, {%4, %4};\n"
+      " mov.b64 a, {%5, %5};\n fma.rn.f32x2 y, x, m, a;\n mov.b64 {%0, %1}, y;\n}"
+      : "=f"(y0), "=f"(y1)
+      : "f"(x0), "f"(x1), "f"(s), "f"(c));
+}
+
+// (s0, s1) += (x0, x1), one packed fp32 instruction.
+__device__ __forceinline__ void add2(float &s0, float &s1, float x0, float x1) {
+  asm("{\n .reg .b64 s, x;\n mov.b64 s, {%0, %1};\n mov.b64 x, {%2, %3};\n"
+      " add.rn.f32x2 s, s, x;\n mov.b64 {%0, %1}, s;\n}"
+      : "+f"(s0), "+f"(s1)
+      : "f"(x0), "f"(x1));
+}
+
+// Barrier among the 256 softmax threads only (hardware barrier 1).
+__device__ __forceinline__ void softmax_barrier() {
+  asm volatile("bar.sync 1, %0;" ::"r"(kSoftmaxWarps * 32) : "memory");
+}
+
 // kv_map: the workspace as a 2-D bf16 tensor [2 * batch * Hkv * s_pad rows][D],
 // box {64, 128}; q_map: q as [total_q * Hq rows][D], box {64, 1}. Both with
 // 128-byte swizzle.
@@ -286,14 +314,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(kBarKEmpty + i), 1);
       mbar_init(bar(kBarVEmpty + i), 1);
       mbar_init(bar(kBarSFull + i), 1);
-      mbar_init(bar(kBarSFree + i), kSoftmaxWarps * 32);
-    }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(bar(kBarPFull + i), kSoftmaxWarps * 32);
+      mbar_init(bar(kBarSFree + i), kSoftmaxWarps * 16);  // one softmax group
+      mbar_init(bar(kBarPFull + i), kSoftmaxWarps * 16);
       mbar_init(bar(kBarPFree + i), 1);
     }
     mbar_init(bar(kBarTeardown), 1);
-    for (int q = 0; q < 4; ++q) mbar_init(bar(kBarPair + q), 64);
     mbar_init(bar(kBarQFull), 1);
     mbar_init_fence();
   }
@@ -359,6 +384,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
+    // Issue order QK(0), QK(1), PV(0), QK(2), PV(1), ...: tile j's scores go
+    // to S buffer j & 1 and its P V into O accumulator j & 1, so the two
+    // softmax groups never wait on each other.
     if (lane == 0) {
       constexpr uint32_t idesc_qk = umma_idesc_bf16(kM, kN, 0, 0);
       constexpr uint32_t idesc_pv = umma_idesc_bf16(kM, D, 0, 1);
@@ -372,38 +400,38 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto kstep = [](int ks, int rows) -> uint64_t {
         return static_cast<uint64_t>(((ks >> 2) * (rows * 128) + (ks & 3) * 32) >> 4);
       };
-      auto pv = [&](int i) -> bool {
-        const int s = i & 1;
-        if (!mbar_wait(bar(kBarPFull + s), (i >> 1) & 1, abort)) return false;
-        if (!mbar_wait(bar(kBarVFull + s), (i >> 1) & 1, abort)) return false;
+      auto pv = [&](int t) -> bool {
+        const int g = t & 1;
+        if (!mbar_wait(bar(kBarPFull + g), (t >> 1) & 1, abort)) return false;
+        if (!mbar_wait(bar(kBarVFull + g), (t >> 1) & 1, abort)) return false;
         tc_fence_after_sync();
-        const uint64_t dv = dv0 + s * kStageStep;
-        const uint64_t dpb = dp + s * static_cast<uint64_t>(S::kPBytes >> 4);
+        const uint64_t dv = dv0 + g * kStageStep;
+        const uint64_t dpb = dp + g * static_cast<uint64_t>(S::kPBytes >> 4);
 #pragma unroll
         for (int ks = 0; ks < kN / 16; ++ks)
-          umma_bf16_ss(tmem + kTmemO, dpb + kstep(ks, kM), dv + ks * (2048 >> 4), idesc_pv,
-                       (i > 0 || ks > 0) ? 1u : 0u);
-        umma_commit(bar(kBarPFree + s));
-        umma_commit(bar(kBarVEmpty + s));
+          umma_bf16_ss(tmem + kTmemO + g * D, dpb + kstep(ks, kM), dv + ks * (2048 >> 4), idesc_pv,
+                       (t >= 2 || ks > 0) ? 1u : 0u);
+        umma_commit(bar(kBarPFree + g));
+        umma_commit(bar(kBarVEmpty + g));
         return true;
       };
       bool ok = mbar_wait(bar(kBarQFull), 0, abort);
       for (int j = 0; j < n_tiles && ok; ++j) {
-        const int s = j & 1;
-        ok = mbar_wait(bar(kBarKFull + s), (j >> 1) & 1, abort);
-        if (ok && j >= 2) ok = mbar_wait(bar(kBarSFree + s), ((j >> 1) - 1) & 1, abort);
+        const int g = j & 1;
+        ok = mbar_wait(bar(kBarKFull + g), (j >> 1) & 1, abort);
+        if (ok && j >= 2) ok = mbar_wait(bar(kBarSFree + g), ((j >> 1) - 1) & 1, abort);
         if (!ok) break;
         tc_fence_after_sync();
-        const uint64_t dk = dk0 + s * kStageStep;
+        const uint64_t dk = dk0 + g * kStageStep;
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks)
-          umma_bf16_ss(tmem + kTmemS + s * kN, dq + kstep(ks, kM), dk + kstep(ks, kN), idesc_qk,
+          umma_bf16_ss(tmem + kTmemS + g * kN, dq + kstep(ks, kM), dk + kstep(ks, kN), idesc_qk,
                        ks > 0 ? 1u : 0u);
-        umma_commit(bar(kBarSFull + s));
-        umma_commit(bar(kBarKEmpty + s));
+        umma_commit(bar(kBarSFull + g));
+        umma_commit(bar(kBarKEmpty + g));
         if (j >= 1) ok = pv(j - 1);
       }
-      if (ok && n_tiles > 0) ok = pv(n_tiles - 1);
+      if (ok) ok = pv(n_tiles - 1);
       if (!ok) {
         *abort = 1;
         flag_error(a.err, kErrTimeout);
@@ -411,159 +439,166 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ softmax
-    // Warp w owns TMEM lanes 32 * (w % 4) .. + 31 (query rows) and half
-    // hc = w / 4 of the key columns of each S tile (and of the O columns).
-    // The two warps of a lane quarter combine their row maxima through
-    // spare TMEM columns and an mbarrier each tile.
+    // Group g = warp / 4 takes key tiles g, g + 2, g + 4, ... with its own
+    // running max m, sum l and O accumulator; warp w owns TMEM lanes
+    // 32 (w % 4) .. + 31, one query row per thread, whole rows of S. The
+    // two groups' states are merged at the end.
     const int quarter = warp & 3;
-    const int hc = warp >> 2;
+    const int g = warp >> 2;
     const int r = quarter * 32 + lane;  // query row == TMEM lane
     const int t = r / a.group;
     const bool valid = t < tokens;
     const int limit = p + j0 + (valid ? t : 0);  // last key this row may see
+    const int min_limit = p + j0;                // ... for the CTA's first token
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-    constexpr int kCols = kN / 2;  // S columns (keys) per thread
-    constexpr int kOCols = D / 2;  // O columns per thread
-    const uint32_t pair_bar = bar(kBarPair + quarter);
+    const uint32_t srow = tmem + lane_base + kTmemS + g * kN;
+    const uint32_t orow_t = tmem + lane_base + kTmemO + g * D;
+    const uint32_t prow = sbase + S::kP + g * S::kPBytes;
     float m_used = -INFINITY, l = 0.f;
     bool ok = true;
-    int pair_phase = 0;
-    // Exchange one float with the partner warp through a TMEM scratch column
-    // (bounded wait; warp-uniform ok).
-    auto exchange = [&](float mine, bool &good) -> float {
-      const uint32_t col = tmem + lane_base + kTmemX + 2 * (pair_phase & 1);
-      tmem_st1(col + hc, mine);
-      tmem_st_wait();
-      tc_fence_before_sync();
-      mbar_arrive(pair_bar);
-      good = mbar_wait_warp(pair_bar, pair_phase & 1, abort);
-      float other = mine;
-      if (good) {
-        tc_fence_after_sync();
-        other = tmem_ld1(col + (hc ^ 1));
-        tmem_ld_wait();
-      }
-      ++pair_phase;
-      return other;
-    };
-    for (int j = 0; j < n_tiles && ok; ++j) {
-      const int s = j & 1;
-      if (!(ok = mbar_wait_warp(bar(kBarSFull + s), (j >> 1) & 1, abort))) break;
+    int i = 0;  // this group's tile count
+    for (int j = g; j < n_tiles; j += 2, ++i) {
+      if (!(ok = mbar_wait_warp(bar(kBarSFull + g), i & 1, abort))) break;
       tc_fence_after_sync();
-      const int key0 = j * kN + hc * kCols;
-      const uint32_t srow = tmem + lane_base + kTmemS + s * kN + hc * kCols;
-      // Pass 1: row max of the raw scores (scale > 0 commutes with max).
-      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll 1
-      for (int cb = 0; cb < kCols / 16; ++cb) {
-        float v[16];
-        tmem_ld16(srow + cb * 16, v);
-        tmem_ld_wait();
-        const int kb = key0 + cb * 16;
+      float v[kN];
+      tmem_ld32(srow + 0, *reinterpret_cast<float(*)[32]>(&v[0]));
+      tmem_ld32(srow + 32, *reinterpret_cast<float(*)[32]>(&v[32]));
+      tmem_ld32(srow + 64, *reinterpret_cast<float(*)[32]>(&v[64]));
+      tmem_ld32(srow + 96, *reinterpret_cast<float(*)[32]>(&v[96]));
+      tmem_ld_wait();
+      tc_fence_before_sync();
+      mbar_arrive(bar(kBarSFree + g));  // S is in registers: QK^T of tile j + 2 may overwrite it
+      const int key0 = j * kN;
+      if (key0 + kN - 1 > min_limit) {  // tile crosses some row's last key (CTA-uniform)
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          mx[i & 3] = fmaxf(mx[i & 3], kb + i <= limit ? v[i] : -INFINITY);
+        for (int c = 0; c < kN; ++c) v[c] = key0 + c <= limit ? v[c] : -INFINITY;
       }
-      float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-      mt = fmaxf(mt, exchange(mt, ok));
-      if (!ok) break;
-      mt *= a.scale_log2;
-      if (j == 0) {
-        m_used = mt;  // first tile: key 0 is always visible, so mt is finite
-      } else if (__any_sync(0xffffffffu, mt > m_used + kRescaleThreshold)) {
-        // O may only change once every PV so far is done: PV_{j-1} finished
-        // implies all earlier ones did (commits track all prior MMAs).
-        if (!(ok = mbar_wait_warp(bar(kBarPFree + ((j - 1) & 1)), ((j - 1) >> 1) & 1, abort)))
-          break;
-        tc_fence_after_sync();
-        // Warp-uniform (tcgen05.ld/st are .sync.aligned): every lane rescales
-        // its row by its own factor, 1 where the row max did not move.
+      // Row max of the raw scores (scale > 0 commutes with max).
+      float mx0 = fmaxf(v[0], v[1]), mx1 = fmaxf(v[2], v[3]);
+      float mx2 = fmaxf(v[4], v[5]), mx3 = fmaxf(v[6], v[7]);
+#pragma unroll
+      for (int c = 8; c < kN; c += 8) {
+        mx0 = max3f(mx0, v[c], v[c + 1]);
+        mx1 = max3f(mx1, v[c + 2], v[c + 3]);
+        mx2 = max3f(mx2, v[c + 4], v[c + 5]);
+        mx3 = max3f(mx3, v[c + 6], v[c + 7]);
+      }
+      const float mt = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * a.scale_log2;
+      // Lazy rescale: move the reference max only when a row's max grew by
+      // more than 2^kRescaleThreshold (warp-uniform: tcgen05.ld/st are
+      // .sync.aligned, so every lane takes part, with factor 1 where its
+      // row did not move).
+      const bool rescale = i > 0 && __any_sync(0xffffffffu, mt > m_used + kRescaleThreshold);
+      float f = 1.f;
+      if (i == 0) {
+        m_used = mt;  // may be -inf: a row with no visible key in this tile
+      } else if (rescale) {
         const float m_new = fmaxf(m_used, mt);
-        const float f = fast_exp2(m_used - m_new);
-        l *= f;
+        f = m_used == -INFINITY ? 0.f : fast_exp2(m_used - m_new);
         m_used = m_new;
+      }
+      // P buffer g (and O_g) are free once the P V of this group's previous
+      // tile is done.
+      if (i > 0 && !(ok = mbar_wait_warp(bar(kBarPFree + g), (i - 1) & 1, abort))) break;
+      const float nm = m_used == -INFINITY ? 0.f : -m_used;
+      float sa0 = 0.f, sa1 = 0.f, sb0 = 0.f, sb1 = 0.f;
+#pragma unroll
+      for (int c = 0; c < kN; c += 8) {
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          float y0, y1;
+          fma2(y0, y1, v[c + 2 * e], v[c + 2 * e + 1], a.scale_log2, nm);
+          y0 = fast_exp2(y0);
+          y1 = fast_exp2(y1);
+          if (e & 1)
+            add2(sb0, sb1, y0, y1);
+          else
+            add2(sa0, sa1, y0, y1);
+          w[e] = pack_bf16(y0, y1);
+        }
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(prow + sw128_offset(kM, r, c)),
+                     "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3])
+                     : "memory");
+      }
+      l = l * f + ((sa0 + sa1) + (sb0 + sb1));
+      if (rescale) {
+        // O_g stays still: this group's previous P V is done (waited above).
+        tc_fence_after_sync();
 #pragma unroll 1
-        for (int cb = 0; cb < kOCols / 16; ++cb) {
-          float o[16];
-          const uint32_t oaddr = tmem + lane_base + kTmemO + hc * kOCols + cb * 16;
-          tmem_ld16(oaddr, o);
+        for (int cb = 0; cb < D / 32; ++cb) {
+          float o[32];
+          tmem_ld32(orow_t + cb * 32, o);
           tmem_ld_wait();
 #pragma unroll
-          for (int i = 0; i < 16; ++i) o[i] *= f;
-          tmem_st16(oaddr, o);
+          for (int q = 0; q < 32; ++q) o[q] *= f;
+          tmem_st32(orow_t + cb * 32, o);
         }
         tmem_st_wait();
       }
-      // Pass 2: P = exp2(s * scale - m) as bf16 into region hc of P buffer
-      // j & 1, once the PV that last read that buffer (tile j - 2) is done.
-      if (j >= 2) {
-        if (!(ok = mbar_wait_warp(bar(kBarPFree + s), ((j >> 1) - 1) & 1, abort))) break;
-      }
-      const float neg_m = -m_used;
-      float sum[4] = {0.f, 0.f, 0.f, 0.f};
-      const uint32_t prow = sbase + S::kP + s * S::kPBytes;
-#pragma unroll 1
-      for (int cb = 0; cb < kCols / 16; ++cb) {
-        float v[16];
-        tmem_ld16(srow + cb * 16, v);
-        tmem_ld_wait();
-        const int kb = key0 + cb * 16;
-        uint32_t w[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const float p0 = kb + 2 * e <= limit ? fast_exp2(fmaf(v[2 * e], a.scale_log2, neg_m)) : 0.f;
-          const float p1 =
-              kb + 2 * e + 1 <= limit ? fast_exp2(fmaf(v[2 * e + 1], a.scale_log2, neg_m)) : 0.f;
-          sum[(2 * e) & 3] += p0;
-          sum[(2 * e + 1) & 3] += p1;
-          w[e] = pack_bf16(p0, p1);
-        }
-        const int col = hc * kCols + cb * 16;
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(prow + sw128_offset(kM, r, col)),
-                     "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3])
-                     : "memory");
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
-                         prow + sw128_offset(kM, r, col + 8)),
-                     "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
-                     : "memory");
-      }
-      l += (sum[0] + sum[1]) + (sum[2] + sum[3]);
       tc_fence_before_sync();
-      mbar_arrive(bar(kBarSFree + s));  // S tile read: QK^T of tile j + 2 may overwrite it
       fence_async_shared();
-      mbar_arrive(bar(kBarPFull + s));
+      mbar_arrive(bar(kBarPFull + g));
     }
-    if (ok) l += exchange(l, ok);  // row sum over both column halves
-    if (ok && n_tiles > 0)
-      ok = mbar_wait_warp(bar(kBarPFree + ((n_tiles - 1) & 1)), ((n_tiles - 1) >> 1) & 1, abort);
+    // This group's last P V done: O_g final (and, as commits track every
+    // earlier MMA, so is every QK^T).
+    if (ok && i > 0) ok = mbar_wait_warp(bar(kBarPFree + g), (i - 1) & 1, abort);
     if (!ok) {
       *abort = 1;
       flag_error(a.err, kErrTimeout);
-    } else {
+    }
+    // Merge the two groups' (m, l) through shared memory. Every softmax
+    // warp reaches both barriers (every wait above is bounded). After the
+    // first, group 0 has seen its last P V finish, so all MMAs are done and
+    // the Q buffer can hold the exchange.
+    softmax_barrier();
+    float *mrg = reinterpret_cast<float *>(smem + S::kQ);  // [2][2][kM]
+    mrg[(g * 2 + 0) * kM + r] = m_used;
+    mrg[(g * 2 + 1) * kM + r] = l;
+    softmax_barrier();
+    if (!*abort) {
       tc_fence_after_sync();
-      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const float m0 = mrg[r], l0 = mrg[kM + r];
+      const float m1 = mrg[2 * kM + r], l1 = mrg[3 * kM + r];
+      const float m = fmaxf(m0, m1);  // finite: key 0 is in tile 0 (group 0)
+      const float f0 = m0 == -INFINITY ? 0.f : fast_exp2(m0 - m);
+      const float f1 = m1 == -INFINITY ? 0.f : fast_exp2(m1 - m);
+      const float lt = l0 * f0 + l1 * f1;
+      const float inv = lt > 0.f ? 1.f / lt : 0.f;
+      const bool have1 = n_tiles >= 2;  // O_1 was written
+      const float c0 = f0 * inv, c1 = f1 * inv;
       const int64_t orow =
           static_cast<int64_t>(t_base + j0 + t) * a.hq + kvh * a.group + (r % a.group);
+      constexpr int kHalf = D / 2;  // output columns per group
 #pragma unroll 1
-      for (int cb = 0; cb < kOCols / 32; ++cb) {
-        float o[32];
-        tmem_ld32(tmem + lane_base + kTmemO + hc * kOCols + cb * 32, o);
+      for (int cb = 0; cb < kHalf / 32; ++cb) {
+        const int col = g * kHalf + cb * 32;
+        float o[32], o1[32];
+        tmem_ld32(tmem + lane_base + kTmemO + col, o);
+        if (have1) tmem_ld32(tmem + lane_base + kTmemO + D + col, o1);
         tmem_ld_wait();
+        if (have1) {
+#pragma unroll
+          for (int q = 0; q < 32; ++q) o[q] = o[q] * c0 + o1[q] * c1;
+        } else {
+#pragma unroll
+          for (int q = 0; q < 32; ++q) o[q] *= c0;
+        }
         if (valid) {
-          uint4 *dst = reinterpret_cast<uint4 *>(a.o + orow * D + hc * kOCols + cb * 32);
+          uint4 *dst = reinterpret_cast<uint4 *>(a.o + orow * D + col);
 #pragma unroll
           for (int q4 = 0; q4 < 4; ++q4) {
             uint4 u;
-            u.x = pack_bf16(o[q4 * 8 + 0] * inv, o[q4 * 8 + 1] * inv);
-            u.y = pack_bf16(o[q4 * 8 + 2] * inv, o[q4 * 8 + 3] * inv);
-            u.z = pack_bf16(o[q4 * 8 + 4] * inv, o[q4 * 8 + 5] * inv);
-            u.w = pack_bf16(o[q4 * 8 + 6] * inv, o[q4 * 8 + 7] * inv);
+            u.x = pack_bf16(o[q4 * 8 + 0], o[q4 * 8 + 1]);
+            u.y = pack_bf16(o[q4 * 8 + 2], o[q4 * 8 + 3]);
+            u.z = pack_bf16(o[q4 * 8 + 4], o[q4 * 8 + 5]);
+            u.w = pack_bf16(o[q4 * 8 + 6], o[q4 * 8 + 7]);
             dst[q4] = u;
           }
         }
       }
-      if (valid && hc == 0 && a.lse)
-        a.lse[orow] = l > 0.f ? (m_used + __log2f(l)) * kLn2 : -INFINITY;
+      if (valid && g == 0 && a.lse)
+        a.lse[orow] = lt > 0.f ? (m + __log2f(lt)) * kLn2 : -INFINITY;
     }
   }
 
