@@ -52,9 +52,10 @@
 namespace pkv {
 namespace {
 
-constexpr int kM = 128;  // query rows per CTA
-constexpr int kN = 128;  // keys per K/V tile
-constexpr int kSoftmaxWarps = 8;  // two per SM sub-partition: a row's columns are split
+constexpr int kM = 128;       // query rows per query tile (= TMEM lanes)
+constexpr int kQTiles = 2;    // query tiles per CTA, sharing every K/V tile
+constexpr int kN = 128;       // keys per K/V tile
+constexpr int kSoftmaxWarps = 8;  // warps 4X .. 4X + 3 serve query tile X
 constexpr int kMmaWarp = kSoftmaxWarps;
 constexpr int kProducerWarp = kSoftmaxWarps + 1;  // warp +0: Q and K; +1: V
 constexpr int kProducerWarps = 2;
@@ -64,21 +65,21 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 template <int D>
 struct Smem {
-  static constexpr int kQ = 0;
+  static constexpr int kQ = 0;  // query tile X at kQ + X * kQBytes
   static constexpr int kQBytes = kM * D * 2;
   static constexpr int kTileBytes = kN * D * 2;
-  static constexpr int kKV = kQ + kQBytes;  // stage s: K at kKV + s*2*tile, V after it
-  static constexpr int kP = kKV + 4 * kTileBytes;  // P buffer b at kP + b * kPBytes
-  static constexpr int kPBytes = kM * kN * 2;
-  static constexpr int kBars = kP + 2 * kPBytes;
+  static constexpr int kKV = kQ + kQTiles * kQBytes;  // stage s: K at kKV + s*2*tile, V after it
+  static constexpr int kBars = kKV + 4 * kTileBytes;
   // + alignment slack; never below 116 KB, so one CTA (and one 512-column
   // TMEM allocation) per SM even for head_dim 64
-  static constexpr int kNeed = kBars + 32 * 8 + 16 + 1024;
+  static constexpr int kNeed = kBars + 32 * 8 + 1024;
   static constexpr int kTotal = kNeed > 116 * 1024 ? kNeed : 116 * 1024;
 };
 
-// TMEM columns: S buffer g at 128 g, O accumulator g at 256 + D g (one per
-// softmax group).
+// TMEM columns: S_X (fp32 scores of query tile X) at 128 X, O_X at 256 + D X.
+// P_X (bf16 pairs, one 32-bit column per two keys) overwrites the first 64
+// columns of S_X once the softmax has read S_X into registers; the P V MMA
+// takes it from there as its A operand.
 constexpr uint32_t kTmemS = 0;
 constexpr uint32_t kTmemO = 256;
 
@@ -88,15 +89,14 @@ constexpr uint32_t kTmemO = 256;
 enum : int {
   kBarKFull = 0,      // [2] producer: K tile landed (TMA bytes)
   kBarVFull = 2,      // [2] producer: V tile landed (TMA bytes)
-  kBarKEmpty = 4,     // [2] MMA: K buffer consumed (after QK^T)
-  kBarVEmpty = 6,     // [2] MMA: V buffer consumed (after PV)
-  kBarSFull = 8,      // [2] MMA: S tile ready in TMEM buffer g
-  kBarSFree = 10,     // [2] softmax group g: S buffer g read
-  kBarPFull = 12,     // [2] softmax group g: P buffer g written (and O_g rescaled)
-  kBarPFree = 14,     // [2] MMA: the PV that read P buffer g finished (and all MMAs before it)
-  kBarTeardown = 16,  // MMA: everything issued has finished (abort path)
-  kBarQFull = 17,     // producer: Q tile landed (TMA bytes)
-  kBarCount = 18,
+  kBarKEmpty = 4,     // [2] MMA: K buffer consumed (after both QK^T)
+  kBarVEmpty = 6,     // [2] MMA: V buffer consumed (after both PV)
+  kBarSFull = 8,      // [2] MMA: S_X ready (and every earlier MMA done)
+  kBarPFull = 10,     // [2] softmax X: P_X written to TMEM (and O_X rescaled)
+  kBarOFull = 12,     // MMA: every MMA done, O final
+  kBarTeardown = 13,  // MMA: everything issued has finished (abort path)
+  kBarQFull = 14,     // producer: both Q tiles landed (TMA bytes)
+  kBarCount = 15,
 };
 
 struct GatherArgs {
@@ -127,7 +127,7 @@ struct ExtendArgs {
   int32_t total_q;
   int32_t hq;
   int32_t group;
-  int32_t tokens_per_cta;  // floor(128 / group)
+  int32_t tokens_per_tile;  // floor(128 / group) chunk tokens per query tile
   int32_t capacity;
   int32_t s_pad;
   float scale_log2;
@@ -231,11 +231,6 @@ __device__ __forceinline__ void add2(float &s0, float &s1, float x0, float x1) {
       : "f"(x0), "f"(x1));
 }
 
-// Barrier among the 256 softmax threads only (hardware barrier 1).
-__device__ __forceinline__ void softmax_barrier() {
-  asm volatile("bar.sync 1, %0;" ::"r"(kSoftmaxWarps * 32) : "memory");
-}
-
 // kv_map: the workspace as a 2-D bf16 tensor [2 * batch * Hkv * s_pad rows][D],
 // box {64, 128}; q_map: q as [total_q * Hq rows][D], box {64, 1}. Both with
 // 128-byte swizzle.
@@ -252,11 +247,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = tid >> 5;
   const int lane = tid & 31;
   const int kvh = blockIdx.x;
+  const int tpt = a.tokens_per_tile;
 
   grid_dependency_wait();  // K/V come from the gather kernel
   if (tid == 0) {
-    // Which (request, token tile) this CTA owns; tiles are taken from the end.
-    const int tile = static_cast<int>(gridDim.y) - 1 - static_cast<int>(blockIdx.y);
+    // Which (request, 2-tile token block) this CTA owns; blocks are taken
+    // from the end.
+    const int blk = static_cast<int>(gridDim.y) - 1 - static_cast<int>(blockIdx.y);
+    const int per = kQTiles * tpt;
     int acc = 0;
     int req = -1, j0 = 0, c = 0, p = 0;
     for (int r = 0; r < a.batch; ++r) {
@@ -267,15 +265,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (kvh == 0 && blockIdx.y == 0) flag_error(a.err, kErrIndptr);
         break;
       }
-      const int nt = (cr + a.tokens_per_cta - 1) / a.tokens_per_cta;
-      if (tile < acc + nt) {
+      const int nb = (cr + per - 1) / per;
+      if (blk < acc + nb) {
         req = r;
-        j0 = (tile - acc) * a.tokens_per_cta;
+        j0 = (blk - acc) * per;
         c = cr;
         p = a.seq_lens[r] - cr;
         break;
       }
-      acc += nt;
+      acc += nb;
     }
     if (req >= 0) {
       // seq_len above the workspace capacity: flagged by the gather kernel
@@ -303,9 +301,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int j0 = s_j0, c = s_c, p = s_p;
   const int t_base = a.qo_indptr[req];
-  const int tokens = min(a.tokens_per_cta, c - j0);
-  const int n_keys = p + j0 + tokens;  // keys the last token of the tile sees
-  const int n_tiles = (n_keys + kN - 1) / kN;
+  const int tokens = min(kQTiles * tpt, c - j0);  // chunk tokens of this CTA
+  // Query tile X holds tokens X*tpt .. X*tpt + tok_X - 1 of the CTA and
+  // walks key tiles 0 .. n_X - 1 (n_1 = 0 when it holds no token).
+  const int tok1 = max(0, min(tpt, tokens - tpt));
+  const int tok0 = min(tpt, tokens);
+  const int n0 = (p + j0 + tok0 + kN - 1) / kN;
+  const int n1 = tok1 > 0 ? (p + j0 + tpt + tok1 + kN - 1) / kN : 0;
+  const int n_tiles = max(n0, n1);
 
   if (tid == 0) {
     for (int i = 0; i < 2; ++i) {
@@ -314,10 +317,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(kBarKEmpty + i), 1);
       mbar_init(bar(kBarVEmpty + i), 1);
       mbar_init(bar(kBarSFull + i), 1);
-      mbar_init(bar(kBarSFree + i), kSoftmaxWarps * 16);  // one softmax group
-      mbar_init(bar(kBarPFull + i), kSoftmaxWarps * 16);
-      mbar_init(bar(kBarPFree + i), 1);
+      mbar_init(bar(kBarPFull + i), 128);  // the four warps of one query tile
     }
+    mbar_init(bar(kBarOFull), 1);
     mbar_init(bar(kBarTeardown), 1);
     mbar_init(bar(kBarQFull), 1);
     mbar_init_fence();
@@ -330,35 +332,40 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp >= kProducerWarp) {
     // ------------------------------------------------------------ producers
-    // Warp 0 of the two loads Q (lane l: rows 4 l .. 4 l + 3, all 64-column
-    // halves; rows past the tile's tokens read as zeros) and then the K
-    // tiles; warp 1 the V tiles. Lane 0 issues the tile loads.
+    // Warp 0 of the two loads both Q tiles (lane l: rows 4 l .. 4 l + 3 of
+    // each, all 64-column halves; rows past the CTA's tokens read as zeros)
+    // and then the K tiles; warp 1 the V tiles. Lane 0 issues tile loads.
     const int pw = warp - kProducerWarp;
     const bool is_k = pw == 0;
     constexpr int kHalves = D / 64;
     bool ok = true;
     if (is_k) {
-      int qr[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int r = 4 * lane + e;
-        const int t = r / a.group;
-        qr[e] = t < tokens ? (t_base + j0 + t) * a.hq + kvh * a.group + (r % a.group) : -1;
-      }
-      if (lane == 0) mbar_arrive_expect_tx(bar(kBarQFull), S::kQBytes);
+      if (lane == 0) mbar_arrive_expect_tx(bar(kBarQFull), kQTiles * S::kQBytes);
       __syncwarp();
 #pragma unroll
-      for (int h = 0; h < kHalves; ++h)
-        tma_gather4(sbase + S::kQ + static_cast<uint32_t>(h * (kM * 128) + (lane >> 1) * 1024 +
-                                                         (lane & 1) * 512),
-                    &q_map, h * 64, qr[0], qr[1], qr[2], qr[3], bar(kBarQFull));
+      for (int x = 0; x < kQTiles; ++x) {
+        int qr[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int r = 4 * lane + e;
+          const int tt = r / a.group;  // token within the query tile
+          const int tok = x * tpt + tt;
+          qr[e] = (tt < tpt && tok < tokens)
+                      ? (t_base + j0 + tok) * a.hq + kvh * a.group + (r % a.group)
+                      : -1;
+        }
+#pragma unroll
+        for (int h = 0; h < kHalves; ++h)
+          tma_gather4(sbase + S::kQ + static_cast<uint32_t>(x * S::kQBytes + h * (kM * 128) +
+                                                           (lane >> 1) * 1024 + (lane & 1) * 512),
+                      &q_map, h * 64, qr[0], qr[1], qr[2], qr[3], bar(kBarQFull));
+      }
     }
     const int full_bar = is_k ? kBarKFull : kBarVFull;
     const int empty_bar = is_k ? kBarKEmpty : kBarVEmpty;
     const uint32_t buf_off = is_k ? 0u : static_cast<uint32_t>(S::kTileBytes);
     // first workspace row of this (K or V, request, kv head) run
-    const int run0 =
-        ((is_k ? 0 : a.batch) + req) * a.hkv * a.s_pad + kvh * a.s_pad;
+    const int run0 = ((is_k ? 0 : a.batch) + req) * a.hkv * a.s_pad + kvh * a.s_pad;
     int issued = 0;
     for (int j = 0; j < n_tiles; ++j) {
       const int s = j & 1;
@@ -384,81 +391,93 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
-    // Issue order QK(0), QK(1), PV(0), QK(2), PV(1), ...: tile j's scores go
-    // to S buffer j & 1 and its P V into O accumulator j & 1, so the two
-    // softmax groups never wait on each other.
+    // Order: S_0(0), S_1(0), then per key tile j: PV_0(j), S_0(j+1),
+    // PV_1(j), S_1(j+1). tcgen05.mma ops of one thread run in issue order,
+    // so S_X(j+1) overwrites P_X(j) only after PV_X(j) has read it, and a
+    // completed S_X(j+1) implies a completed PV_X(j) (O_X is then stable).
     if (lane == 0) {
       constexpr uint32_t idesc_qk = umma_idesc_bf16(kM, kN, 0, 0);
       constexpr uint32_t idesc_pv = umma_idesc_bf16(kM, D, 0, 1);
       // Descriptors are built once; a k-step adds its byte offset / 16 to the
       // start-address field (addresses stay below 256 KB, so no carry).
-      const uint64_t dq = umma_desc_sw128(sbase + S::kQ, 16, 1024);
-      const uint64_t dp = umma_desc_sw128(sbase + S::kP, 16, 1024);
+      const uint64_t dq0 = umma_desc_sw128(sbase + S::kQ, 16, 1024);
       const uint64_t dk0 = umma_desc_sw128(sbase + S::kKV, 16, 1024);
       const uint64_t dv0 = umma_desc_sw128(sbase + S::kKV + S::kTileBytes, kN * 128, 1024);
       constexpr uint64_t kStageStep = (2 * S::kTileBytes) >> 4;
       auto kstep = [](int ks, int rows) -> uint64_t {
         return static_cast<uint64_t>(((ks >> 2) * (rows * 128) + (ks & 3) * 32) >> 4);
       };
-      auto pv = [&](int t) -> bool {
-        const int g = t & 1;
-        if (!mbar_wait(bar(kBarPFull + g), (t >> 1) & 1, abort)) return false;
-        if (!mbar_wait(bar(kBarVFull + g), (t >> 1) & 1, abort)) return false;
-        tc_fence_after_sync();
-        const uint64_t dv = dv0 + g * kStageStep;
-        const uint64_t dpb = dp + g * static_cast<uint64_t>(S::kPBytes >> 4);
-#pragma unroll
-        for (int ks = 0; ks < kN / 16; ++ks)
-          umma_bf16_ss(tmem + kTmemO + g * D, dpb + kstep(ks, kM), dv + ks * (2048 >> 4), idesc_pv,
-                       (t >= 2 || ks > 0) ? 1u : 0u);
-        umma_commit(bar(kBarPFree + g));
-        umma_commit(bar(kBarVEmpty + g));
-        return true;
-      };
-      bool ok = mbar_wait(bar(kBarQFull), 0, abort);
-      for (int j = 0; j < n_tiles && ok; ++j) {
-        const int g = j & 1;
-        ok = mbar_wait(bar(kBarKFull + g), (j >> 1) & 1, abort);
-        if (ok && j >= 2) ok = mbar_wait(bar(kBarSFree + g), ((j >> 1) - 1) & 1, abort);
-        if (!ok) break;
-        tc_fence_after_sync();
-        const uint64_t dk = dk0 + g * kStageStep;
+      auto qk = [&](int x, int j) {
+        const uint64_t dq = dq0 + static_cast<uint64_t>((x * S::kQBytes) >> 4);
+        const uint64_t dk = dk0 + (j & 1) * kStageStep;
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks)
-          umma_bf16_ss(tmem + kTmemS + g * kN, dq + kstep(ks, kM), dk + kstep(ks, kN), idesc_qk,
+          umma_bf16_ss(tmem + kTmemS + x * kN, dq + kstep(ks, kM), dk + kstep(ks, kN), idesc_qk,
                        ks > 0 ? 1u : 0u);
-        umma_commit(bar(kBarSFull + g));
-        umma_commit(bar(kBarKEmpty + g));
-        if (j >= 1) ok = pv(j - 1);
+        umma_commit(bar(kBarSFull + x));
+      };
+      auto pv = [&](int x, int j) -> bool {
+        if (!mbar_wait(bar(kBarPFull + x), j & 1, abort)) return false;
+        tc_fence_after_sync();
+        const uint64_t dv = dv0 + (j & 1) * kStageStep;
+#pragma unroll
+        for (int ks = 0; ks < kN / 16; ++ks)
+          umma_bf16_ts(tmem + kTmemO + x * D, tmem + kTmemS + x * kN + ks * 8,
+                       dv + ks * (2048 >> 4), idesc_pv, (j > 0 || ks > 0) ? 1u : 0u);
+        return true;
+      };
+      bool ok = mbar_wait(bar(kBarQFull), 0, abort) && mbar_wait(bar(kBarKFull), 0, abort);
+      if (ok) {
+        tc_fence_after_sync();
+        qk(0, 0);
+        if (n1 > 0) qk(1, 0);
+        umma_commit(bar(kBarKEmpty));
       }
-      if (ok) ok = pv(n_tiles - 1);
-      if (!ok) {
+      for (int j = 0; j < n_tiles && ok; ++j) {
+        const int s = j & 1;
+        const bool next = j + 1 < n_tiles;
+        ok = mbar_wait(bar(kBarVFull + s), (j >> 1) & 1, abort);
+        if (ok && j < n0) ok = pv(0, j);
+        if (ok && next) ok = mbar_wait(bar(kBarKFull + (s ^ 1)), ((j + 1) >> 1) & 1, abort);
+        if (!ok) break;
+        tc_fence_after_sync();
+        if (next && j + 1 < n0) qk(0, j + 1);
+        if (j < n1) ok = pv(1, j);
+        if (!ok) break;
+        umma_commit(bar(kBarVEmpty + s));
+        if (next) {
+          tc_fence_after_sync();
+          if (j + 1 < n1) qk(1, j + 1);
+          umma_commit(bar(kBarKEmpty + (s ^ 1)));
+        }
+      }
+      if (ok) {
+        umma_commit(bar(kBarOFull));
+      } else {
         *abort = 1;
         flag_error(a.err, kErrTimeout);
       }
     }
   } else {
     // ------------------------------------------------------------ softmax
-    // Group g = warp / 4 takes key tiles g, g + 2, g + 4, ... with its own
-    // running max m, sum l and O accumulator; warp w owns TMEM lanes
-    // 32 (w % 4) .. + 31, one query row per thread, whole rows of S. The
-    // two groups' states are merged at the end.
+    // Query tile x = warp / 4; warp w owns TMEM lanes 32 (w % 4) .. + 31,
+    // one query row per thread, whole rows of S.
     const int quarter = warp & 3;
-    const int g = warp >> 2;
+    const int x = warp >> 2;
+    const int n_x = x == 0 ? n0 : n1;
     const int r = quarter * 32 + lane;  // query row == TMEM lane
-    const int t = r / a.group;
-    const bool valid = t < tokens;
-    const int limit = p + j0 + (valid ? t : 0);  // last key this row may see
-    const int min_limit = p + j0;                // ... for the CTA's first token
+    const int tt = r / a.group;         // token within the query tile
+    const int tok = x * tpt + tt;       // token within the CTA
+    const bool valid = tt < tpt && tok < tokens;
+    const int min_limit = p + j0 + x * tpt;        // last key of the tile's first token
+    const int limit = min_limit + (valid ? tt : 0);  // last key this row may see
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-    const uint32_t srow = tmem + lane_base + kTmemS + g * kN;
-    const uint32_t orow_t = tmem + lane_base + kTmemO + g * D;
-    const uint32_t prow = sbase + S::kP + g * S::kPBytes;
+    const uint32_t srow = tmem + lane_base + kTmemS + x * kN;
+    const uint32_t orow_t = tmem + lane_base + kTmemO + x * D;
     float m_used = -INFINITY, l = 0.f;
     bool ok = true;
-    int i = 0;  // this group's tile count
-    for (int j = g; j < n_tiles; j += 2, ++i) {
-      if (!(ok = mbar_wait_warp(bar(kBarSFull + g), i & 1, abort))) break;
+    for (int j = 0; j < n_x; ++j) {
+      if (!(ok = mbar_wait_warp(bar(kBarSFull + x), j & 1, abort))) break;
       tc_fence_after_sync();
       float v[kN];
       tmem_ld32(srow + 0, *reinterpret_cast<float(*)[32]>(&v[0]));
@@ -466,49 +485,44 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld32(srow + 64, *reinterpret_cast<float(*)[32]>(&v[64]));
       tmem_ld32(srow + 96, *reinterpret_cast<float(*)[32]>(&v[96]));
       tmem_ld_wait();
-      tc_fence_before_sync();
-      mbar_arrive(bar(kBarSFree + g));  // S is in registers: QK^T of tile j + 2 may overwrite it
       const int key0 = j * kN;
-      if (key0 + kN - 1 > min_limit) {  // tile crosses some row's last key (CTA-uniform)
+      if (key0 + kN - 1 > min_limit) {  // tile crosses some row's last key (warp-uniform)
 #pragma unroll
-        for (int c = 0; c < kN; ++c) v[c] = key0 + c <= limit ? v[c] : -INFINITY;
+        for (int cc = 0; cc < kN; ++cc) v[cc] = key0 + cc <= limit ? v[cc] : -INFINITY;
       }
       // Row max of the raw scores (scale > 0 commutes with max).
       float mx0 = fmaxf(v[0], v[1]), mx1 = fmaxf(v[2], v[3]);
       float mx2 = fmaxf(v[4], v[5]), mx3 = fmaxf(v[6], v[7]);
 #pragma unroll
-      for (int c = 8; c < kN; c += 8) {
-        mx0 = max3f(mx0, v[c], v[c + 1]);
-        mx1 = max3f(mx1, v[c + 2], v[c + 3]);
-        mx2 = max3f(mx2, v[c + 4], v[c + 5]);
-        mx3 = max3f(mx3, v[c + 6], v[c + 7]);
+      for (int cc = 8; cc < kN; cc += 8) {
+        mx0 = max3f(mx0, v[cc], v[cc + 1]);
+        mx1 = max3f(mx1, v[cc + 2], v[cc + 3]);
+        mx2 = max3f(mx2, v[cc + 4], v[cc + 5]);
+        mx3 = max3f(mx3, v[cc + 6], v[cc + 7]);
       }
       const float mt = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * a.scale_log2;
       // Lazy rescale: move the reference max only when a row's max grew by
       // more than 2^kRescaleThreshold (warp-uniform: tcgen05.ld/st are
       // .sync.aligned, so every lane takes part, with factor 1 where its
       // row did not move).
-      const bool rescale = i > 0 && __any_sync(0xffffffffu, mt > m_used + kRescaleThreshold);
+      const bool rescale = j > 0 && __any_sync(0xffffffffu, mt > m_used + kRescaleThreshold);
       float f = 1.f;
-      if (i == 0) {
+      if (j == 0) {
         m_used = mt;  // may be -inf: a row with no visible key in this tile
       } else if (rescale) {
         const float m_new = fmaxf(m_used, mt);
         f = m_used == -INFINITY ? 0.f : fast_exp2(m_used - m_new);
         m_used = m_new;
       }
-      // P buffer g (and O_g) are free once the P V of this group's previous
-      // tile is done.
-      if (i > 0 && !(ok = mbar_wait_warp(bar(kBarPFree + g), (i - 1) & 1, abort))) break;
       const float nm = m_used == -INFINITY ? 0.f : -m_used;
       float sa0 = 0.f, sa1 = 0.f, sb0 = 0.f, sb1 = 0.f;
 #pragma unroll
-      for (int c = 0; c < kN; c += 8) {
-        uint32_t w[4];
+      for (int cc = 0; cc < kN; cc += 32) {
+        uint32_t w[16];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
+        for (int e = 0; e < 16; ++e) {
           float y0, y1;
-          fma2(y0, y1, v[c + 2 * e], v[c + 2 * e + 1], a.scale_log2, nm);
+          fma2(y0, y1, v[cc + 2 * e], v[cc + 2 * e + 1], a.scale_log2, nm);
           y0 = fast_exp2(y0);
           y1 = fast_exp2(y1);
           if (e & 1)
@@ -517,14 +531,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             add2(sa0, sa1, y0, y1);
           w[e] = pack_bf16(y0, y1);
         }
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(prow + sw128_offset(kM, r, c)),
-                     "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3])
-                     : "memory");
+        tmem_st16u(srow + cc / 2, w);  // P_x: keys cc .. cc + 31 -> columns cc/2 ..
       }
       l = l * f + ((sa0 + sa1) + (sb0 + sb1));
       if (rescale) {
-        // O_g stays still: this group's previous P V is done (waited above).
-        tc_fence_after_sync();
+        // O_x is stable: S_x(j) completed, so did PV_x(j - 1) before it.
 #pragma unroll 1
         for (int cb = 0; cb < D / 32; ++cb) {
           float o[32];
@@ -534,77 +545,45 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int q = 0; q < 32; ++q) o[q] *= f;
           tmem_st32(orow_t + cb * 32, o);
         }
-        tmem_st_wait();
       }
+      tmem_st_wait();
       tc_fence_before_sync();
-      fence_async_shared();
-      mbar_arrive(bar(kBarPFull + g));
+      mbar_arrive(bar(kBarPFull + x));
     }
-    // This group's last P V done: O_g final (and, as commits track every
-    // earlier MMA, so is every QK^T).
-    if (ok && i > 0) ok = mbar_wait_warp(bar(kBarPFree + g), (i - 1) & 1, abort);
+    if (ok && n_x > 0) ok = mbar_wait_warp(bar(kBarOFull), 0, abort);
     if (!ok) {
       *abort = 1;
       flag_error(a.err, kErrTimeout);
-    }
-    // Merge the two groups' (m, l) through shared memory. Every softmax
-    // warp reaches both barriers (every wait above is bounded). After the
-    // first, group 0 has seen its last P V finish, so all MMAs are done and
-    // the Q buffer can hold the exchange.
-    softmax_barrier();
-    float *mrg = reinterpret_cast<float *>(smem + S::kQ);  // [2][2][kM]
-    mrg[(g * 2 + 0) * kM + r] = m_used;
-    mrg[(g * 2 + 1) * kM + r] = l;
-    softmax_barrier();
-    if (!*abort) {
+    } else if (n_x > 0) {
       tc_fence_after_sync();
-      const float m0 = mrg[r], l0 = mrg[kM + r];
-      const float m1 = mrg[2 * kM + r], l1 = mrg[3 * kM + r];
-      const float m = fmaxf(m0, m1);  // finite: key 0 is in tile 0 (group 0)
-      const float f0 = m0 == -INFINITY ? 0.f : fast_exp2(m0 - m);
-      const float f1 = m1 == -INFINITY ? 0.f : fast_exp2(m1 - m);
-      const float lt = l0 * f0 + l1 * f1;
-      const float inv = lt > 0.f ? 1.f / lt : 0.f;
-      const bool have1 = n_tiles >= 2;  // O_1 was written
-      const float c0 = f0 * inv, c1 = f1 * inv;
+      const float inv = l > 0.f ? 1.f / l : 0.f;
       const int64_t orow =
-          static_cast<int64_t>(t_base + j0 + t) * a.hq + kvh * a.group + (r % a.group);
-      constexpr int kHalf = D / 2;  // output columns per group
+          static_cast<int64_t>(t_base + j0 + tok) * a.hq + kvh * a.group + (r % a.group);
 #pragma unroll 1
-      for (int cb = 0; cb < kHalf / 32; ++cb) {
-        const int col = g * kHalf + cb * 32;
-        float o[32], o1[32];
-        tmem_ld32(tmem + lane_base + kTmemO + col, o);
-        if (have1) tmem_ld32(tmem + lane_base + kTmemO + D + col, o1);
+      for (int cb = 0; cb < D / 32; ++cb) {
+        float o[32];
+        tmem_ld32(orow_t + cb * 32, o);
         tmem_ld_wait();
-        if (have1) {
-#pragma unroll
-          for (int q = 0; q < 32; ++q) o[q] = o[q] * c0 + o1[q] * c1;
-        } else {
-#pragma unroll
-          for (int q = 0; q < 32; ++q) o[q] *= c0;
-        }
         if (valid) {
-          uint4 *dst = reinterpret_cast<uint4 *>(a.o + orow * D + col);
+          uint4 *dst = reinterpret_cast<uint4 *>(a.o + orow * D + cb * 32);
 #pragma unroll
           for (int q4 = 0; q4 < 4; ++q4) {
             uint4 u;
-            u.x = pack_bf16(o[q4 * 8 + 0], o[q4 * 8 + 1]);
-            u.y = pack_bf16(o[q4 * 8 + 2], o[q4 * 8 + 3]);
-            u.z = pack_bf16(o[q4 * 8 + 4], o[q4 * 8 + 5]);
-            u.w = pack_bf16(o[q4 * 8 + 6], o[q4 * 8 + 7]);
+            u.x = pack_bf16(o[q4 * 8 + 0] * inv, o[q4 * 8 + 1] * inv);
+            u.y = pack_bf16(o[q4 * 8 + 2] * inv, o[q4 * 8 + 3] * inv);
+            u.z = pack_bf16(o[q4 * 8 + 4] * inv, o[q4 * 8 + 5] * inv);
+            u.w = pack_bf16(o[q4 * 8 + 6] * inv, o[q4 * 8 + 7] * inv);
             dst[q4] = u;
           }
         }
       }
-      if (valid && g == 0 && a.lse)
-        a.lse[orow] = lt > 0.f ? (m + __log2f(lt)) * kLn2 : -INFINITY;
+      if (valid && a.lse) a.lse[orow] = l > 0.f ? (m_used + __log2f(l)) * kLn2 : -INFINITY;
     }
   }
 
   // Teardown: every role has left its loop (normally or through the abort
-  // flag); free TMEM once no MMA is in flight (the MMA thread's last commit
-  // was waited on by the softmax, or the abort path below waits for it).
+  // flag); free TMEM once no MMA is in flight (the softmax waited for the
+  // final commit, or the abort path below waits for it).
   if (warp == kMmaWarp && lane == 0 && *abort) {
     // Tracks every MMA this thread issued; they need no other input to finish.
     umma_commit(bar(kBarTeardown));
@@ -697,7 +676,7 @@ cudaError_t launch_extend(const PoolGeom &g, int32_t layer, const void *q,
   a.total_q = total_q;
   a.hq = hq;
   a.group = hq / g.hkv;
-  a.tokens_per_cta = kM / a.group;
+  a.tokens_per_tile = kM / a.group;
   a.capacity = capacity;
   a.s_pad = static_cast<int32_t>(s_pad);
   a.scale_log2 = scale * kLog2e;
@@ -706,8 +685,8 @@ cudaError_t launch_extend(const PoolGeom &g, int32_t layer, const void *q,
   if (!bf16_map(&kv_map, workspace, ws_rows, static_cast<uint64_t>(g.d), kN) ||
       !bf16_map(&q_map, q, q_rows, static_cast<uint64_t>(g.d), 1))
     return cudaErrorInvalidValue;
-  const int64_t tiles =
-      (static_cast<int64_t>(total_q) + a.tokens_per_cta - 1) / a.tokens_per_cta + batch;
+  const int64_t per_cta = static_cast<int64_t>(kQTiles) * a.tokens_per_tile;
+  const int64_t tiles = (static_cast<int64_t>(total_q) + per_cta - 1) / per_cta + batch;
   if (tiles > 65535 || batch > 65535) return cudaErrorInvalidConfiguration;
   const dim3 ggrid(static_cast<unsigned>((s_pad + kGatherKeys - 1) / kGatherKeys),
                    static_cast<unsigned>(batch));
