@@ -14,30 +14,29 @@
 //   extend_tc_kernel      the attention, which then reads every 128-key K or
 //       V tile with plain 2-D TMA boxes instead of row gathers.
 //
-// Tiling. A CTA owns one 128-row query tile of one kv head: 128 / g chunk
-// tokens x the g q heads that read that kv head, so every K/V tile feeds g
-// heads. It walks the visible keys in tiles of 128, alternating between two
-// independent online-softmax states ("groups"), so the two never wait on
-// each other and their softmax work overlaps the tensor core's:
-//   S_j  = Q K_j^T            tcgen05.mma, M=128 N=128 K=D, fp32 into TMEM
-//                             buffer j % 2
-//   P_j  = exp2(scale*S_j - m) softmax group j % 2, bf16 into shared P
-//                             buffer j % 2
-//   O_{j%2} += P_j V_j         tcgen05.mma, M=128 N=D K=128, fp32 in TMEM
-// and at the end merges the two (m, l, O) states like a two-way split.
-// Roles (352 threads):
-//   warps 0-7  softmax: group g = warp / 4; warp w owns TMEM lanes
+// Tiling. A CTA owns two 128-row query tiles X = 0, 1 of one kv head; a
+// tile holds 128 / g chunk tokens x the g q heads that read that kv head, so
+// every K/V tile loaded feeds 2 x 128 query rows. It walks the visible keys
+// in tiles of 128; per key tile j and query tile X:
+//   S_X  = Q_X K_j^T           tcgen05.mma, M=128 N=128 K=D, fp32 in TMEM
+//   P_X  = exp2(scale*S_X - m) softmax warps of tile X, bf16 back into TMEM
+//                              over the first half of S_X
+//   O_X += P_X V_j             tcgen05.mma with A = P_X from TMEM, M=128
+//                              N=D K=128, fp32 in TMEM
+// While the softmax of one query tile runs, the tensor core works on the
+// other's MMAs.
+// Roles (320 threads):
+//   warps 0-7  softmax: query tile X = warp / 4; warp w owns TMEM lanes
 //              32 (w % 4) .. + 31 (query rows), one whole row per thread;
-//              log2-domain online softmax with a lazy rescale (O_g is
+//              log2-domain online softmax with a lazy rescale (O_X is
 //              rescaled only when a row max grows by more than 2^8), masks
-//              only on tiles that cross some row's last key; then the
-//              merge, O / l -> bf16, lse.
+//              only on tiles that cross some row's last key; then O / l ->
+//              bf16 and lse.
 //   warp 8     TMEM allocation and the single MMA-issuing thread.
-//   warps 9-10 producers: warp 9 loads the Q rows (TMA tile::gather4, 4 rows
-//              per instruction) and the K tiles, warp 10 the V tiles (2-D
-//              TMA boxes of 128 keys x 64 columns, 128-byte swizzle). A K
-//              buffer is refilled once its QK^T is done, a V buffer once its
-//              PV is done.
+//   warp 9     producer: the Q rows (TMA tile::gather4, 4 rows per
+//              instruction), then the K and V tiles (2-D TMA boxes of 128
+//              keys x 64 columns, 128-byte swizzle) into two stages; a stage
+//              is refilled once every MMA that reads it is done.
 // Every hand-off is an mbarrier; every wait is bounded (tc_common.cuh).
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -57,8 +56,8 @@ constexpr int kQTiles = 2;    // query tiles per CTA, sharing every K/V tile
 constexpr int kN = 128;       // keys per K/V tile
 constexpr int kSoftmaxWarps = 8;  // warps 4X .. 4X + 3 serve query tile X
 constexpr int kMmaWarp = kSoftmaxWarps;
-constexpr int kProducerWarp = kSoftmaxWarps + 1;  // warp +0: Q and K; +1: V
-constexpr int kProducerWarps = 2;
+constexpr int kProducerWarp = kSoftmaxWarps + 1;  // loads Q, K and V
+constexpr int kProducerWarps = 1;
 constexpr int kThreads = (kSoftmaxWarps + 1 + kProducerWarps) * 32;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
@@ -87,16 +86,14 @@ constexpr uint32_t kTmemO = 256;
 // at most once between two waits of the same waiter (so a waiter is never
 // two phases behind): per-buffer barriers for everything double-buffered.
 enum : int {
-  kBarKFull = 0,      // [2] producer: K tile landed (TMA bytes)
-  kBarVFull = 2,      // [2] producer: V tile landed (TMA bytes)
-  kBarKEmpty = 4,     // [2] MMA: K buffer consumed (after both QK^T)
-  kBarVEmpty = 6,     // [2] MMA: V buffer consumed (after both PV)
-  kBarSFull = 8,      // [2] MMA: S_X ready (and every earlier MMA done)
-  kBarPFull = 10,     // [2] softmax X: P_X written to TMEM (and O_X rescaled)
-  kBarOFull = 12,     // MMA: every MMA done, O final
-  kBarTeardown = 13,  // MMA: everything issued has finished (abort path)
-  kBarQFull = 14,     // producer: both Q tiles landed (TMA bytes)
-  kBarCount = 15,
+  kBarFull = 0,       // [2] producer: K and V tiles of stage s landed (TMA bytes)
+  kBarEmpty = 2,      // [2] MMA: every MMA reading stage s done
+  kBarSFull = 4,      // [2] MMA: S_X ready (and every earlier MMA done)
+  kBarPFull = 6,      // [2] softmax X: P_X written to TMEM (and O_X rescaled)
+  kBarOFull = 8,      // MMA: every MMA done, O final
+  kBarTeardown = 9,   // MMA: everything issued has finished (abort path)
+  kBarQFull = 10,     // producer: both Q tiles landed (TMA bytes)
+  kBarCount = 11,
 };
 
 struct GatherArgs {
@@ -312,10 +309,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (tid == 0) {
     for (int i = 0; i < 2; ++i) {
-      mbar_init(bar(kBarKFull + i), 1);  // the producer's expect_tx arrival
-      mbar_init(bar(kBarVFull + i), 1);
-      mbar_init(bar(kBarKEmpty + i), 1);
-      mbar_init(bar(kBarVEmpty + i), 1);
+      mbar_init(bar(kBarFull + i), 1);  // the producer's expect_tx arrival
+      mbar_init(bar(kBarEmpty + i), 1);
       mbar_init(bar(kBarSFull + i), 1);
       mbar_init(bar(kBarPFull + i), 128);  // the four warps of one query tile
     }
@@ -331,51 +326,49 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = s_tmem;
 
   if (warp >= kProducerWarp) {
-    // ------------------------------------------------------------ producers
-    // Warp 0 of the two loads both Q tiles (lane l: rows 4 l .. 4 l + 3 of
-    // each, all 64-column halves; rows past the CTA's tokens read as zeros)
-    // and then the K tiles; warp 1 the V tiles. Lane 0 issues tile loads.
-    const int pw = warp - kProducerWarp;
-    const bool is_k = pw == 0;
+    // ------------------------------------------------------------ producer
+    // Loads both Q tiles (lane l: rows 4 l .. 4 l + 3 of each, all 64-column
+    // halves; rows past the CTA's tokens read as zeros), then per key tile
+    // the K and V boxes into stage j % 2 once every MMA reading that stage
+    // (tile j - 2) is done. Lane 0 issues the tile loads.
     constexpr int kHalves = D / 64;
     bool ok = true;
-    if (is_k) {
-      if (lane == 0) mbar_arrive_expect_tx(bar(kBarQFull), kQTiles * S::kQBytes);
-      __syncwarp();
+    if (lane == 0) mbar_arrive_expect_tx(bar(kBarQFull), kQTiles * S::kQBytes);
+    __syncwarp();
 #pragma unroll
-      for (int x = 0; x < kQTiles; ++x) {
-        int qr[4];
+    for (int x = 0; x < kQTiles; ++x) {
+      int qr[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int r = 4 * lane + e;
-          const int tt = r / a.group;  // token within the query tile
-          const int tok = x * tpt + tt;
-          qr[e] = (tt < tpt && tok < tokens)
-                      ? (t_base + j0 + tok) * a.hq + kvh * a.group + (r % a.group)
-                      : -1;
-        }
-#pragma unroll
-        for (int h = 0; h < kHalves; ++h)
-          tma_gather4(sbase + S::kQ + static_cast<uint32_t>(x * S::kQBytes + h * (kM * 128) +
-                                                           (lane >> 1) * 1024 + (lane & 1) * 512),
-                      &q_map, h * 64, qr[0], qr[1], qr[2], qr[3], bar(kBarQFull));
+      for (int e = 0; e < 4; ++e) {
+        const int r = 4 * lane + e;
+        const int tt = r / a.group;  // token within the query tile
+        const int tok = x * tpt + tt;
+        qr[e] = (tt < tpt && tok < tokens)
+                    ? (t_base + j0 + tok) * a.hq + kvh * a.group + (r % a.group)
+                    : -1;
       }
+#pragma unroll
+      for (int h = 0; h < kHalves; ++h)
+        tma_gather4(sbase + S::kQ + static_cast<uint32_t>(x * S::kQBytes + h * (kM * 128) +
+                                                         (lane >> 1) * 1024 + (lane & 1) * 512),
+                    &q_map, h * 64, qr[0], qr[1], qr[2], qr[3], bar(kBarQFull));
     }
-    const int full_bar = is_k ? kBarKFull : kBarVFull;
-    const int empty_bar = is_k ? kBarKEmpty : kBarVEmpty;
-    const uint32_t buf_off = is_k ? 0u : static_cast<uint32_t>(S::kTileBytes);
-    // first workspace row of this (K or V, request, kv head) run
-    const int run0 = ((is_k ? 0 : a.batch) + req) * a.hkv * a.s_pad + kvh * a.s_pad;
+    // first workspace rows of this request's K and V runs for this kv head
+    const int k_run = (req * a.hkv + kvh) * a.s_pad;
+    const int v_run = ((a.batch + req) * a.hkv + kvh) * a.s_pad;
     int issued = 0;
     for (int j = 0; j < n_tiles; ++j) {
       const int s = j & 1;
-      if (j >= 2 && !(ok = mbar_wait_warp(bar(empty_bar + s), ((j >> 1) - 1) & 1, abort))) break;
+      if (j >= 2 && !(ok = mbar_wait_warp(bar(kBarEmpty + s), ((j >> 1) - 1) & 1, abort))) break;
       if (lane == 0) {
-        const uint32_t dst = sbase + S::kKV + s * 2 * S::kTileBytes + buf_off;
-        mbar_arrive_expect_tx(bar(full_bar + s), S::kTileBytes);
+        const uint32_t dst = sbase + S::kKV + s * 2 * S::kTileBytes;
+        mbar_arrive_expect_tx(bar(kBarFull + s), 2 * S::kTileBytes);
 #pragma unroll
-        for (int h = 0; h < kHalves; ++h)
-          tma_load_2d(dst + h * (kN * 128), &kv_map, h * 64, run0 + j * kN, bar(full_bar + s));
+        for (int h = 0; h < kHalves; ++h) {
+          tma_load_2d(dst + h * (kN * 128), &kv_map, h * 64, k_run + j * kN, bar(kBarFull + s));
+          tma_load_2d(dst + S::kTileBytes + h * (kN * 128), &kv_map, h * 64, v_run + j * kN,
+                      bar(kBarFull + s));
+        }
       }
       __syncwarp();
       ++issued;
@@ -385,9 +378,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Let every issued copy land before the CTA can exit: TMA writes to
       // this CTA's shared memory need no other input to finish.
       int never = 0;
-      if (is_k) mbar_wait(bar(kBarQFull), 0, &never);
+      mbar_wait(bar(kBarQFull), 0, &never);
       for (int t = issued > 2 ? issued - 2 : 0; t < issued; ++t)
-        mbar_wait(bar(full_bar + (t & 1)), (t >> 1) & 1, &never);
+        mbar_wait(bar(kBarFull + (t & 1)), (t >> 1) & 1, &never);
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
@@ -395,6 +388,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // PV_1(j), S_1(j+1). tcgen05.mma ops of one thread run in issue order,
     // so S_X(j+1) overwrites P_X(j) only after PV_X(j) has read it, and a
     // completed S_X(j+1) implies a completed PV_X(j) (O_X is then stable).
+    // An MMA issue returns about when the tensor core takes it, so the work
+    // between issues is kept small: inline barrier tests, three commits per
+    // key tile.
     if (lane == 0) {
       constexpr uint32_t idesc_qk = umma_idesc_bf16(kM, kN, 0, 0);
       constexpr uint32_t idesc_pv = umma_idesc_bf16(kM, D, 0, 1);
@@ -417,7 +413,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         umma_commit(bar(kBarSFull + x));
       };
       auto pv = [&](int x, int j) -> bool {
-        if (!mbar_wait(bar(kBarPFull + x), j & 1, abort)) return false;
+        if (!mbar_wait_fast(bar(kBarPFull + x), j & 1, abort)) return false;
         tc_fence_after_sync();
         const uint64_t dv = dv0 + (j & 1) * kStageStep;
 #pragma unroll
@@ -426,30 +422,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                        dv + ks * (2048 >> 4), idesc_pv, (j > 0 || ks > 0) ? 1u : 0u);
         return true;
       };
-      bool ok = mbar_wait(bar(kBarQFull), 0, abort) && mbar_wait(bar(kBarKFull), 0, abort);
+      bool ok = mbar_wait_fast(bar(kBarQFull), 0, abort) && mbar_wait_fast(bar(kBarFull), 0, abort);
       if (ok) {
         tc_fence_after_sync();
         qk(0, 0);
         if (n1 > 0) qk(1, 0);
-        umma_commit(bar(kBarKEmpty));
       }
       for (int j = 0; j < n_tiles && ok; ++j) {
         const int s = j & 1;
         const bool next = j + 1 < n_tiles;
-        ok = mbar_wait(bar(kBarVFull + s), (j >> 1) & 1, abort);
-        if (ok && j < n0) ok = pv(0, j);
-        if (ok && next) ok = mbar_wait(bar(kBarKFull + (s ^ 1)), ((j + 1) >> 1) & 1, abort);
+        if (j < n0) ok = pv(0, j);
+        if (ok && next) ok = mbar_wait_fast(bar(kBarFull + (s ^ 1)), ((j + 1) >> 1) & 1, abort);
         if (!ok) break;
         tc_fence_after_sync();
         if (next && j + 1 < n0) qk(0, j + 1);
-        if (j < n1) ok = pv(1, j);
-        if (!ok) break;
-        umma_commit(bar(kBarVEmpty + s));
-        if (next) {
-          tc_fence_after_sync();
-          if (j + 1 < n1) qk(1, j + 1);
-          umma_commit(bar(kBarKEmpty + (s ^ 1)));
-        }
+        if (j < n1 && !(ok = pv(1, j))) break;
+        umma_commit(bar(kBarEmpty + s));
+        if (next && j + 1 < n1) qk(1, j + 1);
       }
       if (ok) {
         umma_commit(bar(kBarOFull));

@@ -276,10 +276,29 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, int 
       : "memory");
 }
 
+// One test of the phase (may suspend the thread briefly in hardware, waking
+// when the phase completes).
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(done)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+// mbar_wait with an inline first test, so a wait that is already satisfied
+// costs no call.
+__device__ __forceinline__ bool mbar_wait_fast(uint32_t bar, uint32_t parity, volatile int *abort) {
+  return mbar_try(bar, parity) || mbar_wait(bar, parity, abort);
+}
+
 // mbar_wait by every lane of a warp, with a warp-uniform result: code after
 // it may use .sync.aligned instructions (tcgen05.ld/st) safely.
 __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, volatile int *abort) {
-  const bool ok = mbar_wait(bar, parity, abort);
+  const bool ok = mbar_wait_fast(bar, parity, abort);
   return __all_sync(0xffffffffu, ok);
 }
 
