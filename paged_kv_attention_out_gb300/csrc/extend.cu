@@ -112,6 +112,11 @@ struct GatherArgs {
   int32_t s_pad;     // capacity rounded up to 128: keys per workspace run
   __nv_bfloat16 *ws;
   unsigned *err;
+  // block schedule (built by the planner CTA, read by the attention)
+  const int32_t *qo_indptr;
+  int32_t total_q;
+  int32_t tokens_per_tile;
+  int32_t *plan;
 };
 
 struct ExtendArgs {
@@ -129,6 +134,7 @@ struct ExtendArgs {
   int32_t s_pad;
   float scale_log2;
   unsigned *err;
+  const int32_t *plan;
 };
 
 constexpr int kGatherKeys = 32;     // keys per gather CTA
@@ -138,11 +144,130 @@ constexpr int kGatherThreads = 256;
 // of D elements starting at row ((c * batch + r) * hkv + h) * s_pad. Rows
 // seq_len .. (seq_len rounded up to 128) - 1 are written as zeros so a tile
 // never holds stale bits (a NaN there would survive P = 0 in P V).
+// Longest-first block schedule. A "block" is one attention CTA's work: two
+// query tiles (2 * tokens_per_tile chunk tokens) of one request. Its cost is
+// the number of (query tile, key tile) pairs it computes plus two for its
+// prologue and epilogue; blocks are counting-sorted by cost, largest first,
+// so the longest CTAs start in the first wave and the tail is short. Layout
+// (int32): plan[0] = block count; the histogram at kPlanHist (plan_buckets
+// entries); then (request, first token, cost) per block in request order;
+// then the sorted (request, first token) pairs.
+constexpr int kPlanHist = 16;
+
+__host__ __device__ inline int64_t plan_buckets(int64_t s_pad) { return 2 * (s_pad / 128) + 4; }
+__host__ __device__ inline int64_t plan_max_blocks(int64_t batch, int64_t s_pad) {
+  return batch * (s_pad / 16 + 1);  // a block holds >= 16 tokens (group <= 16)
+}
+__host__ __device__ inline int64_t plan_ints(int64_t batch, int64_t s_pad) {
+  return kPlanHist + plan_buckets(s_pad) + 5 * plan_max_blocks(batch, s_pad);
+}
+
+__device__ void plan_blocks(const GatherArgs &a) {
+  __shared__ int s_first_bad;
+  __shared__ int s_part[kGatherThreads];
+  const int tid = threadIdx.x;
+  const int per = 2 * a.tokens_per_tile;
+  const int nbuck = static_cast<int>(plan_buckets(a.s_pad));
+  const int64_t maxb = plan_max_blocks(a.batch, a.s_pad);
+  int *hist = a.plan + kPlanHist;
+  int *ent = hist + nbuck;       // 3 per block, request order
+  int *sorted = ent + 3 * maxb;  // 2 per block, by cost
+  if (tid == 0) s_first_bad = a.batch;
+  for (int i = tid; i < nbuck; i += kGatherThreads) hist[i] = 0;
+  __syncthreads();
+  // The schedule covers the requests before the first malformed qo_indptr entry.
+  for (int r = tid; r < a.batch; r += kGatherThreads) {
+    const int beg = a.qo_indptr[r], end = a.qo_indptr[r + 1];
+    if (beg < 0 || end < beg || end > a.total_q) atomicMin(&s_first_bad, r);
+  }
+  __syncthreads();
+  if (tid == 0 && s_first_bad < a.batch) flag_error(a.err, kErrIndptr);
+  const int nreq = s_first_bad;
+  // Block offsets: a running exclusive scan over requests, kGatherThreads at a time.
+  int base = 0;
+  for (int r0 = 0; r0 < nreq; r0 += kGatherThreads) {
+    const int r = r0 + tid;
+    int nb = 0, c = 0, p = 0;
+    if (r < nreq) {
+      c = a.qo_indptr[r + 1] - a.qo_indptr[r];
+      const int seq = a.seq_lens[r];
+      p = seq - c;
+      if (p < 0) {
+        flag_error(a.err, kErrIndptr);
+      } else if (seq <= a.capacity) {  // above capacity: flagged by the gather
+        nb = (c + per - 1) / per;
+      }
+    }
+    s_part[tid] = nb;
+    __syncthreads();
+    for (int off = 1; off < kGatherThreads; off <<= 1) {  // inclusive scan
+      const int v = tid >= off ? s_part[tid - off] : 0;
+      __syncthreads();
+      s_part[tid] += v;
+      __syncthreads();
+    }
+    const int first = base + s_part[tid] - nb;
+    for (int i = 0; i < nb; ++i) {
+      const int j0 = i * per;
+      const int tokens = min(per, c - j0);
+      const int tok0 = min(a.tokens_per_tile, tokens);
+      const int tok1 = max(0, tokens - a.tokens_per_tile);
+      const int n0 = (p + j0 + tok0 + 127) / 128;
+      const int n1 = tok1 > 0 ? (p + j0 + a.tokens_per_tile + tok1 + 127) / 128 : 0;
+      const int cost = min(n0 + n1 + 2, nbuck - 1);
+      const int b = first + i;
+      ent[3 * b] = r;
+      ent[3 * b + 1] = j0;
+      ent[3 * b + 2] = cost;
+      atomicAdd(&hist[cost], 1);
+    }
+    base += s_part[kGatherThreads - 1];
+    __syncthreads();
+  }
+  const int nblk = base;
+  // Exclusive scan of the histogram from the largest cost down gives each
+  // bucket's first rank; thread t owns a contiguous run of buckets.
+  const int run = (nbuck + kGatherThreads - 1) / kGatherThreads;
+  int sum = 0;
+  for (int i = 0; i < run; ++i) {
+    const int k = nbuck - 1 - (tid * run + i);
+    if (k >= 0) sum += hist[k];
+  }
+  s_part[tid] = sum;
+  __syncthreads();
+  for (int off = 1; off < kGatherThreads; off <<= 1) {
+    const int v = tid >= off ? s_part[tid - off] : 0;
+    __syncthreads();
+    s_part[tid] += v;
+    __syncthreads();
+  }
+  int start = s_part[tid] - sum;
+  for (int i = 0; i < run; ++i) {
+    const int k = nbuck - 1 - (tid * run + i);
+    if (k >= 0) {
+      const int h = hist[k];
+      hist[k] = start;
+      start += h;
+    }
+  }
+  __syncthreads();
+  for (int b = tid; b < nblk; b += kGatherThreads) {
+    const int pos = atomicAdd(&hist[ent[3 * b + 2]], 1);
+    sorted[2 * pos] = ent[3 * b];
+    sorted[2 * pos + 1] = ent[3 * b + 1];
+  }
+  if (tid == 0) a.plan[0] = nblk;
+}
+
 template <int D>
 __global__ void __launch_bounds__(kGatherThreads)
     extend_gather_kernel(const GatherArgs a) {
   grid_dependency_wait();  // the chunk's K/V may come from the previous kernel (store_kv)
   grid_dependents_launch();
+  if (static_cast<int>(blockIdx.y) == a.batch) {  // the extra row: one planner CTA
+    if (blockIdx.x == 0) plan_blocks(a);
+    return;
+  }
   const int r = blockIdx.y;
   const int seq = a.seq_lens[r];
   if (seq < 0 || seq > a.capacity) {
@@ -248,36 +373,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   grid_dependency_wait();  // K/V come from the gather kernel
   if (tid == 0) {
-    // Which (request, 2-tile token block) this CTA owns; blocks are taken
-    // from the end.
-    const int blk = static_cast<int>(gridDim.y) - 1 - static_cast<int>(blockIdx.y);
-    const int per = kQTiles * tpt;
-    int acc = 0;
+    // This CTA's (request, first token) from the longest-first schedule;
+    // the schedule holds only well-formed requests.
+    const int rank = blockIdx.y;
+    const int *sorted =
+        a.plan + kPlanHist + plan_buckets(a.s_pad) + 3 * plan_max_blocks(a.batch, a.s_pad);
     int req = -1, j0 = 0, c = 0, p = 0;
-    for (int r = 0; r < a.batch; ++r) {
-      const int beg = a.qo_indptr[r];
-      const int end = a.qo_indptr[r + 1];
-      const int cr = end - beg;
-      if (cr < 0 || end > a.total_q || beg < 0) {
-        if (kvh == 0 && blockIdx.y == 0) flag_error(a.err, kErrIndptr);
-        break;
-      }
-      const int nb = (cr + per - 1) / per;
-      if (blk < acc + nb) {
-        req = r;
-        j0 = (blk - acc) * per;
-        c = cr;
-        p = a.seq_lens[r] - cr;
-        break;
-      }
-      acc += nb;
-    }
-    if (req >= 0) {
-      // seq_len above the workspace capacity: flagged by the gather kernel
-      if (p < 0 || p + c > a.capacity) {
-        if (kvh == 0 && p < 0) flag_error(a.err, kErrIndptr);
-        req = -1;
-      }
+    if (rank < a.plan[0]) {
+      req = sorted[2 * rank];
+      j0 = sorted[2 * rank + 1];
+      c = a.qo_indptr[req + 1] - a.qo_indptr[req];
+      p = a.seq_lens[req] - c;
     }
     s_req = req;
     s_j0 = j0;
@@ -621,9 +727,15 @@ bool bf16_map(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols, ui
 
 int64_t extend_s_pad(int32_t capacity) { return (static_cast<int64_t>(capacity) + 127) & ~int64_t(127); }
 
-size_t extend_workspace_bytes(int32_t batch, int32_t hkv, int32_t d, int32_t capacity) {
+// Gathered K/V, then (256-byte aligned) the block schedule.
+static uint64_t extend_kv_bytes(int32_t batch, int32_t hkv, int32_t d, int32_t capacity) {
   return 2ull * static_cast<uint64_t>(batch) * static_cast<uint64_t>(hkv) *
          static_cast<uint64_t>(extend_s_pad(capacity)) * static_cast<uint64_t>(d) * 2ull;
+}
+
+size_t extend_workspace_bytes(int32_t batch, int32_t hkv, int32_t d, int32_t capacity) {
+  const uint64_t kv = (extend_kv_bytes(batch, hkv, d, capacity) + 255) & ~uint64_t(255);
+  return kv + 4ull * static_cast<uint64_t>(plan_ints(batch, extend_s_pad(capacity)));
 }
 
 cudaError_t launch_extend(const PoolGeom &g, int32_t layer, const void *q,
@@ -654,6 +766,12 @@ cudaError_t launch_extend(const PoolGeom &g, int32_t layer, const void *q,
   ga.s_pad = static_cast<int32_t>(s_pad);
   ga.ws = static_cast<__nv_bfloat16 *>(workspace);
   ga.err = err;
+  ga.qo_indptr = qo_indptr;
+  ga.total_q = total_q;
+  ga.tokens_per_tile = kM / (hq / g.hkv);
+  ga.plan = reinterpret_cast<int32_t *>(
+      static_cast<uint8_t *>(workspace) +
+      ((extend_kv_bytes(batch, g.hkv, g.d, capacity) + 255) & ~uint64_t(255)));
 
   ExtendArgs a{};
   a.qo_indptr = qo_indptr;
@@ -670,15 +788,17 @@ cudaError_t launch_extend(const PoolGeom &g, int32_t layer, const void *q,
   a.s_pad = static_cast<int32_t>(s_pad);
   a.scale_log2 = scale * kLog2e;
   a.err = err;
+  a.plan = ga.plan;
   CUtensorMap kv_map, q_map;
   if (!bf16_map(&kv_map, workspace, ws_rows, static_cast<uint64_t>(g.d), kN) ||
       !bf16_map(&q_map, q, q_rows, static_cast<uint64_t>(g.d), 1))
     return cudaErrorInvalidValue;
   const int64_t per_cta = static_cast<int64_t>(kQTiles) * a.tokens_per_tile;
   const int64_t tiles = (static_cast<int64_t>(total_q) + per_cta - 1) / per_cta + batch;
-  if (tiles > 65535 || batch > 65535) return cudaErrorInvalidConfiguration;
+  if (tiles > 65535 || batch >= 65535) return cudaErrorInvalidConfiguration;
+  // one row of gather CTAs per request, plus one row holding the planner
   const dim3 ggrid(static_cast<unsigned>((s_pad + kGatherKeys - 1) / kGatherKeys),
-                   static_cast<unsigned>(batch));
+                   static_cast<unsigned>(batch + 1));
   const dim3 grid(g.hkv, static_cast<unsigned>(tiles));
   cudaError_t e;
   if (g.d == 128) {

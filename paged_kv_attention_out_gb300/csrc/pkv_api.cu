@@ -239,6 +239,7 @@ pkv_status pkv_paged_extend_attn(const pkv_pool *pool, int32_t layer, const void
                 num_q_heads, g.hkv);
   const int group = num_q_heads / g.hkv;
   if (group > 16) return fail(PKV_ERR_UNSUPPORTED, "extend supports Hq/Hkv <= 16, got %d", group);
+  if (batch >= 65535) return fail(PKV_ERR_UNSUPPORTED, "extend supports batch < 65535");
   if (g.hkv > 65535) return fail(PKV_ERR_UNSUPPORTED, "too many kv heads");
   if (table_stride <= 0) return fail(PKV_ERR_INVALID_ARG, "table_stride must be positive");
   if (!isfinite(scale)) return fail(PKV_ERR_INVALID_ARG, "scale is not finite");
@@ -264,7 +265,7 @@ pkv_status pkv_paged_extend_attn(const pkv_pool *pool, int32_t layer, const void
   if (2 * static_cast<int64_t>(batch) * g.hkv * pkv::extend_s_pad(static_cast<int32_t>(cap)) >=
       (int64_t(1) << 31))
     return fail(PKV_ERR_UNSUPPORTED, "extend: batch x kv heads x capacity too large");
-  const int64_t tpc = 128 / group;  // chunk tokens per 128-row query tile
+  const int64_t tpc = 2 * (128 / group);  // chunk tokens per CTA (two 128-row query tiles)
   if ((static_cast<int64_t>(total_q) + tpc - 1) / tpc + batch > 65535)
     return fail(PKV_ERR_UNSUPPORTED, "extend: too many query tiles in one call");
   DevInfo *d = nullptr;
