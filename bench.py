@@ -41,6 +41,39 @@ sys.path.insert(0, ROOT)
 from paged_kv_attention_out_gb300 import workloads as W  # noqa: E402
 
 L2_FLUSH_BYTES = 320 << 20  # > 2x the 129 MB L2
+CSRC = os.path.join(ROOT, "paged_kv_attention_out_gb300", "csrc")
+
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per call, summed
+# over the call's launches, from the ncu captures summarised under profiles/.
+# Each entry holds the SHA-256 of the kernel sources it was taken on; the
+# bench reports it only while those sources are unchanged (else null).
+MEASURED_TRAFFIC = {
+    # profiles/decode_kernel_llama3-8b-decode.md: decode_kernel + decode_merge_kernel
+    "decode": {"sources": ["decode.cu", "pkv_common.cuh"],
+               "sha256": "a015a442f6f44e5aea7058cdc64bede1ebc910c50fabe05fbbc0f0d2a1f11b20",
+               "bytes": 628803840},
+    "extend": {"sources": ["extend.cu", "tc_common.cuh", "pkv_common.cuh"], "sha256": None,
+               "bytes": None},
+}
+
+
+def sources_sha256(names) -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(CSRC, n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def measured_traffic(kind: str, override=None):
+    """Captured DRAM bytes per call for `kind`, or None if the kernels changed since."""
+    if override is not None:
+        return override
+    e = MEASURED_TRAFFIC[kind]
+    if e["sha256"] is None or sources_sha256(e["sources"]) != e["sha256"]:
+        return None
+    return e["bytes"]
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 METRIC = "paged decode attn KV GB/s"
 
@@ -393,7 +426,7 @@ def run_pkv(args):
     }
     main["roofline"]["kernel"] = ("pkv_paged_decode_attn: decode_kernel + decode_merge_kernel "
                                   "(both launches inside the timed duration)")
-    main["roofline"]["traffic"] = args.decode_traffic
+    main["roofline"]["traffic"] = measured_traffic("decode", args.decode_traffic)
     del wl
     torch.cuda.empty_cache()
 
@@ -484,7 +517,9 @@ def _extend_workload(args, dev, peaks, peak_src, flush, steps, warm):
         "unit": "TFLOP/s", "ms_attention": round(at, 4), "ms_step_with_store": round(st, 4),
         "flops": fl, "tokens_per_s": round(case.total_q / (st * 1e-3), 1),
         "roofline": {**roofline("tensor", fl, at, peaks, peak_src),
-                     "kernel": "extend_kernel", "traffic": args.extend_traffic}}
+                     "kernel": ("pkv_paged_extend_attn: extend_gather_kernel + extend_tc_kernel "
+                                "(both launches inside the timed duration)"),
+                     "traffic": measured_traffic("extend", args.extend_traffic)}}
     del wl
     torch.cuda.empty_cache()
     return out
