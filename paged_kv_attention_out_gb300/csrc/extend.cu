@@ -137,7 +137,7 @@ struct ExtendArgs {
   const int32_t *plan;
 };
 
-constexpr int kGatherKeys = 32;     // keys per gather CTA
+constexpr int kGatherKeys = 16;     // keys per gather CTA (two per warp)
 constexpr int kGatherThreads = 256;
 
 // Workspace run of request r, kv head h, K (c = 0) or V (c = 1): s_pad rows
@@ -283,45 +283,56 @@ __global__ void __launch_bounds__(kGatherThreads)
     return;
   }
   const int32_t *row_pages = a.page_table + static_cast<int64_t>(row) * a.table_stride;
+  // One warp per key: its K row and V row (Hkv * D contiguous elements each
+  // in the pool); 16-byte chunk `ch` of a row goes to kv head ch / (D / 8)'s run.
   constexpr int kChunks = D / 8;  // 16-byte chunks per head row
-  const int per_kc = a.hkv * kChunks;  // chunks per (key, K or V)
-  const int total = kGatherKeys * 2 * per_kc;
+  const int nch = a.hkv * kChunks;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
   const int64_t row_elems = static_cast<int64_t>(a.hkv) * D;
+  const int64_t run_elems = static_cast<int64_t>(a.s_pad) * D;  // one kv head's run
   const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
-  constexpr int kUnroll = 4;
-  for (int base = threadIdx.x; base < total; base += kGatherThreads * kUnroll) {
-    uint4 v[kUnroll];
-    uint4 *dst[kUnroll];
+  constexpr int kUnroll = 4;  // chunks per lane per row in flight (x 2 rows)
+  for (int kk = warp; kk < kGatherKeys; kk += kGatherThreads / 32) {
+    const int key = key0 + kk;
+    // the key's K row (c = 0) and V row (c = 1) are copied together
+    const uint4 *src[2] = {nullptr, nullptr};
+    if (key < seq) {
+      const int pidx = key / a.page_size;
+      const int ent = __ldg(row_pages + pidx);
+      const int64_t slot = static_cast<int64_t>(ent) * a.page_size + (key - pidx * a.page_size);
+      if (ent >= 0 && slot < a.slots) {
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const int i = base + u * kGatherThreads;
-      dst[u] = nullptr;
-      if (i >= total) continue;
-      const int kc = i / per_kc;  // (key, c) pair
-      const int rem = i - kc * per_kc;
-      const int h = rem / kChunks;
-      const int ch = rem - h * kChunks;
-      const int key = key0 + (kc >> 1);
-      const int c = kc & 1;
-      dst[u] = reinterpret_cast<uint4 *>(
-          a.ws + ((static_cast<int64_t>(c) * a.batch + r) * a.hkv + h) * a.s_pad * D +
-          static_cast<int64_t>(key) * D + ch * 8);
-      v[u] = zero;
-      if (key < seq) {
-        const int pidx = key / a.page_size;
-        const int ent = __ldg(row_pages + pidx);
-        const int64_t slot = static_cast<int64_t>(ent) * a.page_size + (key - pidx * a.page_size);
-        if (ent >= 0 && slot < a.slots) {
+        for (int c = 0; c < 2; ++c) {
           const int64_t prow = (static_cast<int64_t>(c) * a.num_layers + a.layer) * a.slots + slot;
-          v[u] = __ldg(reinterpret_cast<const uint4 *>(a.pool + prow * row_elems + h * D + ch * 8));
-        } else if (c == 0 && h == 0 && ch == 0) {
-          flag_error(a.err, kErrPage);
+          src[c] = reinterpret_cast<const uint4 *>(a.pool + prow * row_elems);
+        }
+      } else if (lane == 0) {
+        flag_error(a.err, kErrPage);
+      }
+    }
+    for (int ch0 = lane; ch0 < nch; ch0 += 32 * kUnroll) {
+      uint4 v[2][kUnroll];
+#pragma unroll
+      for (int c = 0; c < 2; ++c)
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+          const int ch = ch0 + 32 * u;
+          v[c][u] = (src[c] != nullptr && ch < nch) ? __ldg(src[c] + ch) : zero;
+        }
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        __nv_bfloat16 *dst = a.ws + (static_cast<int64_t>(c) * a.batch + r) * a.hkv * run_elems +
+                             static_cast<int64_t>(key) * D;
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+          const int ch = ch0 + 32 * u;
+          if (ch < nch)
+            *reinterpret_cast<uint4 *>(dst + (ch / kChunks) * run_elems + (ch % kChunks) * 8) =
+                v[c][u];
         }
       }
     }
-#pragma unroll
-    for (int u = 0; u < kUnroll; ++u)
-      if (dst[u]) *dst[u] = v[u];
   }
 }
 
