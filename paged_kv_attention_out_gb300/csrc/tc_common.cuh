@@ -289,10 +289,23 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
   return done != 0;
 }
 
-// mbar_wait with an inline first test, so a wait that is already satisfied
-// costs no call.
+// mbar_wait, inlined: no call (and no register save around one) on the
+// paths that issue MMAs or copies between waits. Same bound: ~2 s or the
+// abort flag.
 __device__ __forceinline__ bool mbar_wait_fast(uint32_t bar, uint32_t parity, volatile int *abort) {
-  return mbar_try(bar, parity) || mbar_wait(bar, parity, abort);
+  uint64_t t0 = 0;
+  for (uint32_t i = 0;; ++i) {
+    if (mbar_try(bar, parity)) return true;
+    if ((i & 63) == 0) {
+      if (*abort) return false;
+      const uint64_t t = global_timer_ns();
+      if (i == 0) {
+        t0 = t;
+      } else if (t - t0 > 2000000000ull) {
+        return false;
+      }
+    }
+  }
 }
 
 // mbar_wait by every lane of a warp, with a warp-uniform result: code after
