@@ -52,8 +52,10 @@ MEASURED_TRAFFIC = {
     "decode": {"sources": ["decode.cu", "pkv_common.cuh"],
                "sha256": "a015a442f6f44e5aea7058cdc64bede1ebc910c50fabe05fbbc0f0d2a1f11b20",
                "bytes": 628803840},
-    "extend": {"sources": ["extend.cu", "tc_common.cuh", "pkv_common.cuh"], "sha256": None,
-               "bytes": None},
+    # profiles/extend_kernels_chunked-prefill-extend.md: extend_gather_kernel + extend_tc_kernel
+    "extend": {"sources": ["extend.cu", "tc_common.cuh", "pkv_common.cuh"],
+               "sha256": "edfa342202ee7ebb1a80b0f4af7fca8d4a198a175b8ae58c72229c8c7cbabeed",
+               "bytes": 522022912},
 }
 
 
