@@ -271,6 +271,33 @@ class Workload:
         return 3 if split else 2
 
 
+class CascadeWorkload(Workload):
+    """The radix-shared case through pkv_paged_cascade_decode_attn: each
+    group's prefix attended once (tensor cores), merged with every member's
+    suffix decode."""
+
+    def __init__(self, case: W.Case, dev):
+        super().__init__(case, dev)
+        self.ct = {n: torch.as_tensor(a, dtype=torch.int32, device=dev)
+                   for n, a in W.cascade_tables(case).items()}
+        self.pmax = max(int(self.ct["prefix_lens"].max()), 1)
+        self.smax = int(self.ct["seq_lens"].max())
+        G = self.ct["prefix_lens"].shape[0]
+        n = self.pkv.pkv_cascade_workspace_size(case.B, case.Hq, case.Hkv, case.D, G, self.pmax,
+                                                self.smax)
+        self.ws = torch.empty(max(n, 256), dtype=torch.uint8, device=dev)
+
+    def attention(self):
+        c, ct = self.case, self.ct
+        self.pkv.pkv_paged_cascade_decode_attn(
+            self.pool, c.layer, self.q, self.o, self.lse, ct["prefix_page_table"],
+            ct["prefix_lens"], ct["member_indptr"], ct["members"], ct["page_table"],
+            ct["seq_lens"], c.scale, self.pmax, self.smax, self.ws)
+
+    def kernels_per_step(self) -> int:
+        return 5  # store, suffix decode, prefix gather, prefix attention, merge
+
+
 def time_steps(wl: Workload, steps: int, warmup: int, flush: torch.Tensor):
     """Per-step CUDA-event times (ms) of store + attention, and of attention alone."""
     stream = torch.cuda.current_stream()
@@ -558,6 +585,19 @@ def _radix_workload(args, dev, peaks, peak_src, flush, steps, warm):
         "unique_bytes": uniq, "logical_bytes": logical,
         "roofline": {**roofline("hbm", uniq, at, peaks, peak_src),
                      "kernel": "decode_kernel + decode_merge_kernel"}}
+    del wl
+    torch.cuda.empty_cache()
+    wl = CascadeWorkload(case, dev)
+    st, at = _measure(wl, steps, warm, flush)
+    out["radix-shared-decode-cascade"] = {
+        "metric": METRIC + " (unique bytes)", "value": round(uniq / (at * 1e-3) / 1e9, 2),
+        "unit": "GB/s", "logical_gbs": round(logical / (at * 1e-3) / 1e9, 2),
+        "ms_attention": round(at, 4), "ms_step_with_store": round(st, 4),
+        "unique_bytes": uniq, "logical_bytes": logical,
+        "roofline": {**roofline("hbm", uniq, at, peaks, peak_src),
+                     "kernel": ("pkv_paged_cascade_decode_attn: suffix decode_kernel + "
+                                "extend_gather_kernel + extend_tc_kernel (prefix) + "
+                                "decode_merge_kernel, all inside the timed duration")}}
     del wl
     torch.cuda.empty_cache()
     return out

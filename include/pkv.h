@@ -226,6 +226,54 @@ pkv_status pkv_paged_extend_attn(const pkv_pool *pool, int32_t layer, const void
                                  size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * Bytes of device workspace pkv_paged_cascade_decode_attn needs: the split
+ * partial states of the suffix decode plus one slot per (request, q head)
+ * for the shared-prefix state, then the gathered prefix K/V of num_groups
+ * groups with capacity max_prefix_len_hint (>= 1) and their block schedule.
+ * Depends only on these host-side sizes (and the device's SM count).
+ */
+size_t pkv_cascade_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                                  int32_t head_dim, int32_t num_groups,
+                                  int32_t max_prefix_len_hint, int32_t max_suffix_len_hint);
+
+/*
+ * Cascade decode over shared prefixes ("Introduction", Key Features, Radix
+ * Cache: requests that share a prefix share its KV entries; "Code Notes:
+ * mini-sglang", Scheduler Layer table, CacheManager row). Requests are
+ * partitioned into groups: group k's members are requests
+ * members[member_indptr[k]] .. members[member_indptr[k+1] - 1], and every
+ * request is a member of exactly one group. Request b of group k attends,
+ * as in pkv_paged_decode_attn, to the concatenation of
+ *   the group's shared prefix: prefix_lens[k] keys of row k of
+ *     prefix_page_table ([num_groups, prefix_table_stride] int32), then
+ *   its own suffix: seq_lens[b] keys of row table_idx[b] (or b) of page_table,
+ * i.e. o[b,h,:], lse[b,h] = attention of q[b,h,:] over those keys. The
+ * prefix is attended once per group for all its members together (tensor
+ * cores, one 128-row query tile per 128 / (Hq/Hkv) members and kv head), the
+ * suffix per request (split-KV decode), and the two states are merged by
+ * log-sum-exp. A group may have prefix_lens[k] = 0. Requires Hq/Hkv <= 8 and
+ * Hkv in {1, 2} or a multiple of 4 (as decode). Tables and q/o/lse as for
+ * decode; member_indptr: device int32 [num_groups + 1], member_indptr[0] = 0,
+ * non-decreasing, member_indptr[num_groups] <= batch; members: device int32,
+ * a permutation of 0 .. batch - 1 laid out by member_indptr (trusted: a
+ * request in no group gets an unspecified result, one in two groups a racy
+ * one). max_prefix_len_hint: a bound on every prefix_lens entry (< 1: the
+ * row capacity prefix_table_stride * page_size); a group above it is not
+ * computed and PKV_DEVERR_SEQ_LEN_RANGE is flagged. max_suffix_len_hint
+ * sizes the suffix split plan as max_seq_len_hint does for decode. workspace:
+ * device, 256-byte aligned, at least pkv_cascade_workspace_size(...) bytes
+ * (with the same effective prefix bound).
+ */
+pkv_status pkv_paged_cascade_decode_attn(
+    const pkv_pool *pool, int32_t layer, const void *q, void *o, float *lse,
+    const int32_t *prefix_page_table, int64_t prefix_table_stride, const int32_t *prefix_lens,
+    const int32_t *member_indptr, const int32_t *members, int32_t num_groups,
+    const int32_t *page_table, int64_t table_stride, const int32_t *table_idx,
+    const int32_t *seq_lens, int32_t batch, int32_t num_q_heads, float scale,
+    int32_t max_prefix_len_hint, int32_t max_suffix_len_hint, void *workspace,
+    size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * Merge of two attention states over disjoint key sets (the log-sum-exp
  * combination split-KV decode uses internally, exported so callers can
  * compose attention over a shared prefix with attention over a private

@@ -76,6 +76,13 @@ def load() -> ctypes.CDLL:
     L.pkv_paged_extend_attn.argtypes = [pool_p, _c_int32, _p, _p, _p, _p, _p, _c_int64, _p, _p,
                                         _c_int32, _c_int32, _c_int32, ctypes.c_float,
                                         _c_int32, _p, ctypes.c_size_t, _p]
+    L.pkv_cascade_workspace_size.restype = ctypes.c_size_t
+    L.pkv_cascade_workspace_size.argtypes = [_c_int32] * 7
+    L.pkv_paged_cascade_decode_attn.restype = ctypes.c_int
+    L.pkv_paged_cascade_decode_attn.argtypes = [pool_p, _c_int32, _p, _p, _p, _p, _c_int64, _p, _p,
+                                                _p, _c_int32, _p, _c_int64, _p, _p, _c_int32,
+                                                _c_int32, ctypes.c_float, _c_int32, _c_int32, _p,
+                                                ctypes.c_size_t, _p]
     L.pkv_merge_lse.restype = ctypes.c_int
     L.pkv_merge_lse.argtypes = [_p, _p, _p, _p, _p, _c_int32, _p, _c_int64, _c_int32,
                                 _c_int32, _p]
@@ -245,6 +252,51 @@ def pkv_paged_extend_attn(pool, layer: int, q, qo_indptr, o, lse, page_table, se
         ctypes.byref(ps), int(layer), _ptr(q), _ptr(qo_indptr), _ptr(o), _ptr(lse),
         _ptr(page_table), page_table.shape[1], _ptr(table_idx), _ptr(seq_lens), B, T, Hq,
         float(scale), int(max_seq_len_hint), _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def pkv_cascade_workspace_size(batch: int, num_q_heads: int, num_kv_heads: int, head_dim: int,
+                               num_groups: int, max_prefix_len_hint: int,
+                               max_suffix_len_hint: int) -> int:
+    return int(load().pkv_cascade_workspace_size(batch, num_q_heads, num_kv_heads, head_dim,
+                                                 num_groups, max_prefix_len_hint,
+                                                 max_suffix_len_hint))
+
+
+def pkv_paged_cascade_decode_attn(pool, layer: int, q, o, lse, prefix_page_table, prefix_lens,
+                                  member_indptr, members, page_table, seq_lens, scale: float,
+                                  max_prefix_len_hint: int, max_suffix_len_hint: int, workspace,
+                                  table_idx=None, stream=None) -> None:
+    """Cascade decode: q, o [B, Hq, D] bf16; lse [B, Hq] fp32 or None; prefix_page_table
+    [G, stride_p] and prefix_lens [G]; member_indptr [G+1] and members [B] partition the
+    requests into groups; page_table rows and seq_lens [B] hold each request's suffix."""
+    ps = pool_struct(pool)
+    for t, name in ((q, "q"), (o, "o")):
+        _want(t, torch.bfloat16, name, 3)
+        _contig(t, name)
+    for t, name, nd in ((prefix_page_table, "prefix_page_table", 2), (prefix_lens, "prefix_lens", 1),
+                        (member_indptr, "member_indptr", 1), (members, "members", 1),
+                        (page_table, "page_table", 2), (seq_lens, "seq_lens", 1)):
+        _want(t, torch.int32, name, nd)
+        _contig(t, name)
+    B, Hq, D = q.shape
+    G = prefix_lens.shape[0]
+    if o.shape != q.shape or seq_lens.shape[0] != B or member_indptr.shape[0] != G + 1 \
+            or prefix_page_table.shape[0] < G:
+        raise ValueError("inconsistent cascade shapes")
+    if lse is not None:
+        _want(lse, torch.float32, "lse", 2)
+        _contig(lse, "lse")
+    if table_idx is not None:
+        _want(table_idx, torch.int32, "table_idx", 1)
+    if workspace is not None:
+        _contig(workspace, "workspace")
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load().pkv_paged_cascade_decode_attn(
+        ctypes.byref(ps), int(layer), _ptr(q), _ptr(o), _ptr(lse), _ptr(prefix_page_table),
+        prefix_page_table.shape[1], _ptr(prefix_lens), _ptr(member_indptr), _ptr(members), G,
+        _ptr(page_table), page_table.shape[1], _ptr(table_idx), _ptr(seq_lens), B, Hq,
+        float(scale), int(max_prefix_len_hint), int(max_suffix_len_hint), _ptr(workspace),
+        ws_bytes, _stream(stream)))
 
 
 def pkv_merge_lse(o_a, lse_a, o_b, lse_b, o_out, lse_out=None, stream=None) -> None:

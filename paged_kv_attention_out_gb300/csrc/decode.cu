@@ -83,8 +83,11 @@ struct DecodeArgs {
   int32_t warps_per_head;
   int32_t chunk;
   int32_t splits;
-  float *part_o;    // [B, Hq, splits, D]
-  float *part_lse;  // [B, Hq, splits] (natural log)
+  int32_t pstride;        // partial slots per (request, q head): splits, or splits + 1
+                          // when slot `splits` holds a shared-prefix state (cascade)
+  int32_t force_partial;  // write partial states even for one split (cascade)
+  float *part_o;    // [B, Hq, pstride, D]
+  float *part_lse;  // [B, Hq, pstride] (natural log)
   unsigned *err;
 };
 
@@ -330,7 +333,7 @@ __global__ void __launch_bounds__(kThreads, (kStages <= 3 ? 2 : 1)) decode_kerne
   __syncthreads();
 
   // Merge the warps that share a kv head; write the final or the partial state.
-  const bool final_out = ri.nsplit == 1;
+  const bool final_out = ri.nsplit == 1 && !a.force_partial;
   const int items = a.heads_per_cta * a.group * (D / 4);
   for (int it = threadIdx.x; it < items; it += kThreads) {
     const int d4 = it % (D / 4);
@@ -369,13 +372,15 @@ __global__ void __launch_bounds__(kThreads, (kStages <= 3 ? 2 : 1)) decode_kerne
       *reinterpret_cast<uint2 *>(a.o + bh * D + d4 * 4) = packed;
       if (d4 == 0 && a.lse) a.lse[bh] = lse_nat;
     } else {
-      *reinterpret_cast<float4 *>(a.part_o + (bh * a.splits + split) * D + d4 * 4) = O;
-      if (d4 == 0) a.part_lse[bh * a.splits + split] = lse_nat;
+      *reinterpret_cast<float4 *>(a.part_o + (bh * a.pstride + split) * D + d4 * 4) = O;
+      if (d4 == 0) a.part_lse[bh * a.pstride + split] = lse_nat;
     }
   }
 }
 
-// Cross-split merge: one warp per (request, q head) with more than one split.
+// Cross-split merge: one warp per (request, q head) with more than one
+// split; with a cascade's shared-prefix state in slot `splits`, every
+// (request, q head) merges its suffix splits with that slot.
 template <int D>
 __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs a, int32_t batch) {
   const int warp = threadIdx.x >> 5;
@@ -386,25 +391,27 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs a, i
   grid_dependency_wait();  // the partial states come from decode_kernel
   const RowInfo ri = row_info(a, b, false);
   const int n = ri.nsplit;
-  if (n <= 1) return;
-  const float *pl = a.part_lse + bh * a.splits;
+  if (n <= 1 && !a.force_partial) return;
+  const int total = n + (a.pstride > a.splits ? 1 : 0);  // + the shared-prefix slot
+  auto slot = [&](int s) { return s < n ? s : a.splits; };
+  const float *pl = a.part_lse + bh * a.pstride;
   float M = -INFINITY;
-  for (int s = lane; s < n; s += 32) M = fmaxf(M, pl[s]);
+  for (int s = lane; s < total; s += 32) M = fmaxf(M, pl[slot(s)]);
 #pragma unroll
   for (int x = 16; x > 0; x >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, x));
   const float ref = M == -INFINITY ? 0.f : M;
   float L = 0.f;
-  for (int s = lane; s < n; s += 32) L += expf(pl[s] - ref);
+  for (int s = lane; s < total; s += 32) L += expf(pl[slot(s)] - ref);
 #pragma unroll
   for (int x = 16; x > 0; x >>= 1) L += __shfl_xor_sync(0xffffffffu, L, x);
   const float inv = L > 0.f ? 1.f / L : 0.f;
   if (lane < D / 4) {
     float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
-    const float *po = a.part_o + bh * a.splits * D + lane * 4;
+    const float *po = a.part_o + bh * a.pstride * D + lane * 4;
 #pragma unroll 4
-    for (int s = 0; s < n; ++s) {
-      const float w = expf(pl[s] - ref) * inv;
-      const float4 v = *reinterpret_cast<const float4 *>(po + static_cast<int64_t>(s) * D);
+    for (int s = 0; s < total; ++s) {
+      const float w = expf(pl[slot(s)] - ref) * inv;
+      const float4 v = *reinterpret_cast<const float4 *>(po + static_cast<int64_t>(slot(s)) * D);
       O.x += w * v.x;
       O.y += w * v.y;
       O.z += w * v.z;
@@ -454,11 +461,10 @@ DecodePlan plan_decode(int32_t batch, int32_t hq, int32_t hkv, int32_t d, int32_
   return p;
 }
 
-cudaError_t launch_decode(const PoolGeom &g, int32_t layer, const void *q, void *o, float *lse,
-                          const int32_t *page_table, int64_t table_stride,
-                          const int32_t *table_idx, const int32_t *seq_lens, int32_t batch,
-                          int32_t hq, float scale, const DecodePlan &plan, void *workspace,
-                          unsigned *err, cudaStream_t stream) {
+static DecodeArgs decode_args(const PoolGeom &g, int32_t layer, const void *q, void *o,
+                              float *lse, const int32_t *page_table, int64_t table_stride,
+                              const int32_t *table_idx, const int32_t *seq_lens, int32_t hq,
+                              float scale, const DecodePlan &plan, unsigned *err) {
   DecodeArgs a{};
   a.pool = static_cast<const __nv_bfloat16 *>(g.base);
   a.plane = g.plane;
@@ -481,13 +487,14 @@ cudaError_t launch_decode(const PoolGeom &g, int32_t layer, const void *q, void 
   a.warps_per_head = plan.warps_per_head;
   a.chunk = plan.chunk;
   a.splits = plan.splits;
+  a.pstride = plan.splits;
+  a.force_partial = 0;
   a.err = err;
-  if (plan.splits > 1) {
-    const size_t rows = static_cast<size_t>(batch) * hq * plan.splits;
-    const size_t o_bytes = (rows * g.d * sizeof(float) + 255) & ~size_t(255);
-    a.part_o = static_cast<float *>(workspace);
-    a.part_lse = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + o_bytes);
-  }
+  return a;
+}
+
+static cudaError_t launch_decode_main(const DecodeArgs &a, const PoolGeom &g,
+                                      const DecodePlan &plan, int32_t batch, cudaStream_t stream) {
   cudaError_t e;
   const dim3 grid(plan.head_groups, plan.splits, batch);
   if (g.d == 128) {
@@ -501,14 +508,72 @@ cudaError_t launch_decode(const PoolGeom &g, int32_t layer, const void *q, void 
     if (e != cudaSuccess) return e;
     e = launch_pdl(decode_kernel<64>, grid, dim3(kThreads), DecodeSmem<64>::kTotal, stream, a);
   }
-  if (e != cudaSuccess || plan.splits <= 1) return e;
-  const int64_t pairs = static_cast<int64_t>(batch) * hq;
-  const dim3 mgrid(static_cast<unsigned>((pairs + 3) / 4));
-  if (g.d == 128)
-    e = launch_pdl(decode_merge_kernel<128>, mgrid, dim3(128), 0, stream, a, batch);
-  else
-    e = launch_pdl(decode_merge_kernel<64>, mgrid, dim3(128), 0, stream, a, batch);
   return e;
+}
+
+static cudaError_t launch_decode_merge(const DecodeArgs &a, const PoolGeom &g, int32_t batch,
+                                       cudaStream_t stream) {
+  const int64_t pairs = static_cast<int64_t>(batch) * a.hq;
+  const dim3 mgrid(static_cast<unsigned>((pairs + 3) / 4));
+  if (g.d == 128) return launch_pdl(decode_merge_kernel<128>, mgrid, dim3(128), 0, stream, a, batch);
+  return launch_pdl(decode_merge_kernel<64>, mgrid, dim3(128), 0, stream, a, batch);
+}
+
+cudaError_t launch_decode(const PoolGeom &g, int32_t layer, const void *q, void *o, float *lse,
+                          const int32_t *page_table, int64_t table_stride,
+                          const int32_t *table_idx, const int32_t *seq_lens, int32_t batch,
+                          int32_t hq, float scale, const DecodePlan &plan, void *workspace,
+                          unsigned *err, cudaStream_t stream) {
+  DecodeArgs a = decode_args(g, layer, q, o, lse, page_table, table_stride, table_idx, seq_lens,
+                             hq, scale, plan, err);
+  if (plan.splits > 1) {
+    const size_t rows = static_cast<size_t>(batch) * hq * plan.splits;
+    const size_t o_bytes = (rows * g.d * sizeof(float) + 255) & ~size_t(255);
+    a.part_o = static_cast<float *>(workspace);
+    a.part_lse = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + o_bytes);
+  }
+  cudaError_t e = launch_decode_main(a, g, plan, batch, stream);
+  if (e != cudaSuccess || plan.splits <= 1) return e;
+  return launch_decode_merge(a, g, batch, stream);
+}
+
+size_t cascade_partial_bytes(int32_t batch, int32_t hq, int32_t d, int32_t splits) {
+  const size_t rows = static_cast<size_t>(batch) * hq * (static_cast<size_t>(splits) + 1);
+  return ((rows * d * sizeof(float) + 255) & ~size_t(255)) +
+         ((rows * sizeof(float) + 255) & ~size_t(255));
+}
+
+cudaError_t launch_cascade_suffix(const PoolGeom &g, int32_t layer, const void *q, void *o,
+                                  float *lse, const int32_t *page_table, int64_t table_stride,
+                                  const int32_t *table_idx, const int32_t *seq_lens,
+                                  int32_t batch, int32_t hq, float scale, const DecodePlan &plan,
+                                  void *partials, unsigned *err, cudaStream_t stream,
+                                  float **part_o, float **part_lse) {
+  DecodeArgs a = decode_args(g, layer, q, o, lse, page_table, table_stride, table_idx, seq_lens,
+                             hq, scale, plan, err);
+  const size_t rows = static_cast<size_t>(batch) * hq * (static_cast<size_t>(plan.splits) + 1);
+  a.pstride = plan.splits + 1;
+  a.force_partial = 1;
+  a.part_o = static_cast<float *>(partials);
+  a.part_lse = reinterpret_cast<float *>(static_cast<uint8_t *>(partials) +
+                                         ((rows * g.d * sizeof(float) + 255) & ~size_t(255)));
+  *part_o = a.part_o;
+  *part_lse = a.part_lse;
+  return launch_decode_main(a, g, plan, batch, stream);
+}
+
+cudaError_t launch_cascade_merge(const PoolGeom &g, int32_t layer, const void *q, void *o,
+                                 float *lse, const int32_t *page_table, int64_t table_stride,
+                                 const int32_t *table_idx, const int32_t *seq_lens, int32_t batch,
+                                 int32_t hq, float scale, const DecodePlan &plan, float *part_o,
+                                 float *part_lse, unsigned *err, cudaStream_t stream) {
+  DecodeArgs a = decode_args(g, layer, q, o, lse, page_table, table_stride, table_idx, seq_lens,
+                             hq, scale, plan, err);
+  a.pstride = plan.splits + 1;
+  a.force_partial = 1;
+  a.part_o = part_o;
+  a.part_lse = part_lse;
+  return launch_decode_merge(a, g, batch, stream);
 }
 
 }  // namespace pkv

@@ -116,6 +116,7 @@ struct GatherArgs {
   const int32_t *qo_indptr;
   int32_t total_q;
   int32_t tokens_per_tile;
+  int32_t causal;  // 0: every query of request r sees all seq_lens[r] keys
   int32_t *plan;
 };
 
@@ -135,7 +136,23 @@ struct ExtendArgs {
   float scale_log2;
   unsigned *err;
   const int32_t *plan;
+  // query source and result sink (see ExtendMode)
+  int32_t causal;
+  const int32_t *members;
+  float *part_o;
+  float *part_lse;
+  int32_t pstride;
+  int32_t pslot;
 };
+
+// Query token (row of q / o, before the head index) of chunk token `tok` of
+// the CTA's block: the next rows of q for extend, the member request for the
+// shared-prefix attention of a cascade (-1 if that index is out of range).
+__device__ __forceinline__ int query_token(const ExtendArgs &a, int t_base, int j0, int tok) {
+  if (!a.members) return t_base + j0 + tok;
+  const int b = a.members[t_base + j0 + tok];
+  return (b >= 0 && b < a.total_q) ? b : -1;
+}
 
 constexpr int kGatherKeys = 16;     // keys per gather CTA (two per warp)
 constexpr int kGatherThreads = 256;
@@ -191,7 +208,7 @@ __device__ void plan_blocks(const GatherArgs &a) {
     if (r < nreq) {
       c = a.qo_indptr[r + 1] - a.qo_indptr[r];
       const int seq = a.seq_lens[r];
-      p = seq - c;
+      p = a.causal ? seq - c : seq;  // causal: the cached prefix; else the keys every query sees
       if (p < 0) {
         flag_error(a.err, kErrIndptr);
       } else if (seq <= a.capacity) {  // above capacity: flagged by the gather
@@ -212,8 +229,10 @@ __device__ void plan_blocks(const GatherArgs &a) {
       const int tokens = min(per, c - j0);
       const int tok0 = min(a.tokens_per_tile, tokens);
       const int tok1 = max(0, tokens - a.tokens_per_tile);
-      const int n0 = (p + j0 + tok0 + 127) / 128;
-      const int n1 = tok1 > 0 ? (p + j0 + a.tokens_per_tile + tok1 + 127) / 128 : 0;
+      const int n0 = a.causal ? (p + j0 + tok0 + 127) / 128 : (p + 127) / 128;
+      const int n1 = tok1 == 0 ? 0
+                     : a.causal ? (p + j0 + a.tokens_per_tile + tok1 + 127) / 128
+                                : (p + 127) / 128;
       const int cost = min(n0 + n1 + 2, nbuck - 1);
       const int b = first + i;
       ent[3 * b] = r;
@@ -394,7 +413,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       req = sorted[2 * rank];
       j0 = sorted[2 * rank + 1];
       c = a.qo_indptr[req + 1] - a.qo_indptr[req];
-      p = a.seq_lens[req] - c;
+      p = a.causal ? a.seq_lens[req] - c : a.seq_lens[req];
     }
     s_req = req;
     s_j0 = j0;
@@ -420,9 +439,33 @@ __global__ void __launch_bounds__(kThreads, 1)
   // walks key tiles 0 .. n_X - 1 (n_1 = 0 when it holds no token).
   const int tok1 = max(0, min(tpt, tokens - tpt));
   const int tok0 = min(tpt, tokens);
-  const int n0 = (p + j0 + tok0 + kN - 1) / kN;
-  const int n1 = tok1 > 0 ? (p + j0 + tpt + tok1 + kN - 1) / kN : 0;
+  // causal: p is the cached prefix, query tile X's last token sees
+  // p + j0 + X tpt + tok_X keys; otherwise every query sees the p keys.
+  const int n0 = a.causal ? (p + j0 + tok0 + kN - 1) / kN : (p + kN - 1) / kN;
+  const int n1 = tok1 == 0 ? 0 : a.causal ? (p + j0 + tpt + tok1 + kN - 1) / kN : (p + kN - 1) / kN;
   const int n_tiles = max(n0, n1);
+  if (n_tiles == 0) {
+    // No visible key (an empty shared prefix): o = 0, lse = -inf.
+    if (warp < kSoftmaxWarps) {
+      const int r = (warp & 3) * 32 + lane;
+      const int tok = (warp >> 2) * tpt + r / a.group;
+      const int qt = (r / a.group < tpt && tok < tokens) ? query_token(a, t_base, j0, tok) : -1;
+      if (qt >= 0) {
+        const int64_t bh = static_cast<int64_t>(qt) * a.hq + kvh * a.group + (r % a.group);
+        if (a.part_o) {
+          const int64_t prow = bh * a.pstride + a.pslot;
+          for (int d = 0; d < D; d += 4)
+            *reinterpret_cast<float4 *>(a.part_o + prow * D + d) = make_float4(0.f, 0.f, 0.f, 0.f);
+          a.part_lse[prow] = -INFINITY;
+        } else {
+          for (int d = 0; d < D; d += 8)
+            *reinterpret_cast<uint4 *>(a.o + bh * D + d) = make_uint4(0u, 0u, 0u, 0u);
+          if (a.lse) a.lse[bh] = -INFINITY;
+        }
+      }
+    }
+    return;
+  }
 
   if (tid == 0) {
     for (int i = 0; i < 2; ++i) {
@@ -460,9 +503,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int r = 4 * lane + e;
         const int tt = r / a.group;  // token within the query tile
         const int tok = x * tpt + tt;
-        qr[e] = (tt < tpt && tok < tokens)
-                    ? (t_base + j0 + tok) * a.hq + kvh * a.group + (r % a.group)
-                    : -1;
+        const int qt = (tt < tpt && tok < tokens) ? query_token(a, t_base, j0, tok) : -1;
+        qr[e] = qt >= 0 ? qt * a.hq + kvh * a.group + (r % a.group) : -1;
       }
 #pragma unroll
       for (int h = 0; h < kHalves; ++h)
@@ -574,9 +616,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = quarter * 32 + lane;  // query row == TMEM lane
     const int tt = r / a.group;         // token within the query tile
     const int tok = x * tpt + tt;       // token within the CTA
-    const bool valid = tt < tpt && tok < tokens;
-    const int min_limit = p + j0 + x * tpt;        // last key of the tile's first token
-    const int limit = min_limit + (valid ? tt : 0);  // last key this row may see
+    const int qtok = (tt < tpt && tok < tokens) ? query_token(a, t_base, j0, tok) : -1;
+    const bool valid = qtok >= 0;
+    if (!valid && a.members && tt < tpt && tok < tokens) flag_error(a.err, kErrIndptr);
+    // last key of the tile's first token, and the last key this row may see
+    const int min_limit = a.causal ? p + j0 + x * tpt : p - 1;
+    const int limit = a.causal ? min_limit + (valid ? tt : 0) : p - 1;
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t srow = tmem + lane_base + kTmemS + x * kN;
     const uint32_t orow_t = tmem + lane_base + kTmemO + x * D;
@@ -664,13 +709,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after_sync();
       const float inv = l > 0.f ? 1.f / l : 0.f;
       const int64_t orow =
-          static_cast<int64_t>(t_base + j0 + tok) * a.hq + kvh * a.group + (r % a.group);
+          static_cast<int64_t>(valid ? qtok : 0) * a.hq + kvh * a.group + (r % a.group);
+      const int64_t prow = orow * a.pstride + a.pslot;  // cascade partial slot
 #pragma unroll 1
       for (int cb = 0; cb < D / 32; ++cb) {
         float o[32];
         tmem_ld32(orow_t + cb * 32, o);
         tmem_ld_wait();
-        if (valid) {
+        if (valid && a.part_o) {
+          float4 *dst = reinterpret_cast<float4 *>(a.part_o + prow * D + cb * 32);
+#pragma unroll
+          for (int q4 = 0; q4 < 8; ++q4)
+            dst[q4] = make_float4(o[q4 * 4] * inv, o[q4 * 4 + 1] * inv, o[q4 * 4 + 2] * inv,
+                                  o[q4 * 4 + 3] * inv);
+        } else if (valid) {
           uint4 *dst = reinterpret_cast<uint4 *>(a.o + orow * D + cb * 32);
 #pragma unroll
           for (int q4 = 0; q4 < 4; ++q4) {
@@ -683,7 +735,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      if (valid && a.lse) a.lse[orow] = l > 0.f ? (m_used + __log2f(l)) * kLn2 : -INFINITY;
+      const float lse_nat = l > 0.f ? (m_used + __log2f(l)) * kLn2 : -INFINITY;
+      if (valid && a.part_o)
+        a.part_lse[prow] = lse_nat;
+      else if (valid && a.lse)
+        a.lse[orow] = lse_nat;
     }
   }
 
@@ -754,7 +810,8 @@ cudaError_t launch_extend(const PoolGeom &g, int32_t layer, const void *q,
                           const int32_t *page_table, int64_t table_stride,
                           const int32_t *table_idx, const int32_t *seq_lens, int32_t batch,
                           int32_t total_q, int32_t hq, float scale, int32_t capacity,
-                          void *workspace, int32_t sm_count, unsigned *err, cudaStream_t stream) {
+                          void *workspace, int32_t sm_count, unsigned *err, cudaStream_t stream,
+                          const ExtendMode &mode) {
   (void)sm_count;
   const int64_t s_pad = extend_s_pad(capacity);
   const uint64_t ws_rows = 2ull * static_cast<uint64_t>(batch) * g.hkv * s_pad;
@@ -780,6 +837,7 @@ cudaError_t launch_extend(const PoolGeom &g, int32_t layer, const void *q,
   ga.qo_indptr = qo_indptr;
   ga.total_q = total_q;
   ga.tokens_per_tile = kM / (hq / g.hkv);
+  ga.causal = mode.causal;
   ga.plan = reinterpret_cast<int32_t *>(
       static_cast<uint8_t *>(workspace) +
       ((extend_kv_bytes(batch, g.hkv, g.d, capacity) + 255) & ~uint64_t(255)));
@@ -800,6 +858,12 @@ cudaError_t launch_extend(const PoolGeom &g, int32_t layer, const void *q,
   a.scale_log2 = scale * kLog2e;
   a.err = err;
   a.plan = ga.plan;
+  a.causal = mode.causal;
+  a.members = mode.members;
+  a.part_o = mode.part_o;
+  a.part_lse = mode.part_lse;
+  a.pstride = mode.pstride;
+  a.pslot = mode.pslot;
   CUtensorMap kv_map, q_map;
   if (!bf16_map(&kv_map, workspace, ws_rows, static_cast<uint64_t>(g.d), kN) ||
       !bf16_map(&q_map, q, q_rows, static_cast<uint64_t>(g.d), 1))

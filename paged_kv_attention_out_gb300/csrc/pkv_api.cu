@@ -217,6 +217,111 @@ pkv_status pkv_paged_decode_attn(const pkv_pool *pool, int32_t layer, const void
   return e == cudaSuccess ? PKV_OK : cuda_fail(e, "decode launch");
 }
 
+static size_t align256(size_t n) { return (n + 255) & ~size_t(255); }
+
+size_t pkv_cascade_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                                  int32_t head_dim, int32_t num_groups,
+                                  int32_t max_prefix_len_hint, int32_t max_suffix_len_hint) {
+  if (batch <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || num_groups <= 0 ||
+      num_q_heads % num_kv_heads != 0 || max_prefix_len_hint < 1)
+    return 0;
+  DevInfo *d = nullptr;
+  if (device_info(&d) != PKV_OK) return 0;
+  const pkv::DecodePlan plan = pkv::plan_decode(batch, num_q_heads, num_kv_heads, head_dim,
+                                                effective_hint(max_suffix_len_hint), d->sm_count);
+  return align256(pkv::cascade_partial_bytes(batch, num_q_heads, head_dim, plan.splits)) +
+         pkv::extend_workspace_bytes(num_groups, num_kv_heads, head_dim, max_prefix_len_hint);
+}
+
+pkv_status pkv_paged_cascade_decode_attn(
+    const pkv_pool *pool, int32_t layer, const void *q, void *o, float *lse,
+    const int32_t *prefix_page_table, int64_t prefix_table_stride, const int32_t *prefix_lens,
+    const int32_t *member_indptr, const int32_t *members, int32_t num_groups,
+    const int32_t *page_table, int64_t table_stride, const int32_t *table_idx,
+    const int32_t *seq_lens, int32_t batch, int32_t num_q_heads, float scale,
+    int32_t max_prefix_len_hint, int32_t max_suffix_len_hint, void *workspace,
+    size_t workspace_bytes, cudaStream_t stream) {
+  pkv::PoolGeom g;
+  pkv_status s = check_pool(pool, layer, &g);
+  if (s != PKV_OK) return s;
+  if (batch < 0 || num_groups < 0) return fail(PKV_ERR_INVALID_ARG, "batch and num_groups must be >= 0");
+  if (num_q_heads <= 0 || num_q_heads % g.hkv != 0)
+    return fail(PKV_ERR_INVALID_ARG, "num_q_heads %d is not a positive multiple of Hkv %d",
+                num_q_heads, g.hkv);
+  const int group = num_q_heads / g.hkv;
+  if (group > 8) return fail(PKV_ERR_UNSUPPORTED, "cascade decode supports Hq/Hkv <= 8, got %d", group);
+  if (g.hkv < 4 ? (4 % g.hkv != 0) : (g.hkv % 4 != 0))
+    return fail(PKV_ERR_UNSUPPORTED, "decode supports Hkv in {1, 2} or a multiple of 4, got %d",
+                g.hkv);
+  if (batch > 65535 || num_groups >= 65535)
+    return fail(PKV_ERR_UNSUPPORTED, "cascade decode: batch %d or groups %d too large", batch,
+                num_groups);
+  if (table_stride <= 0 || prefix_table_stride <= 0)
+    return fail(PKV_ERR_INVALID_ARG, "table strides must be positive");
+  if (!isfinite(scale)) return fail(PKV_ERR_INVALID_ARG, "scale is not finite");
+  if (batch == 0) return PKV_OK;
+  if (num_groups == 0)
+    return fail(PKV_ERR_INVALID_ARG, "cascade decode needs every request in a group (num_groups 0)");
+  if (!q || !o || !page_table || !seq_lens || !prefix_page_table || !prefix_lens ||
+      !member_indptr || !members)
+    return fail(PKV_ERR_INVALID_ARG, "a required pointer is NULL");
+  if (!aligned(q, 16) || !aligned(o, 16))
+    return fail(PKV_ERR_INVALID_ARG, "q and o must be 16-byte aligned");
+  if (!aligned(page_table, 4) || !aligned(seq_lens, 4) || !aligned(lse, 4) ||
+      !aligned(table_idx, 4) || !aligned(prefix_page_table, 4) || !aligned(prefix_lens, 4) ||
+      !aligned(member_indptr, 4) || !aligned(members, 4))
+    return fail(PKV_ERR_INVALID_ARG, "int32/fp32 tables must be 4-byte aligned");
+  const int64_t prefix_row_capacity = prefix_table_stride * g.page_size;
+  int64_t pcap = max_prefix_len_hint >= 1 ? max_prefix_len_hint : prefix_row_capacity;
+  if (pcap > prefix_row_capacity) pcap = prefix_row_capacity;
+  if (pcap > (int64_t(1) << 30)) return fail(PKV_ERR_UNSUPPORTED, "prefix capacity too large");
+  if (2 * static_cast<int64_t>(num_groups) * g.hkv *
+          pkv::extend_s_pad(static_cast<int32_t>(pcap)) >= (int64_t(1) << 31))
+    return fail(PKV_ERR_UNSUPPORTED, "cascade: groups x kv heads x prefix capacity too large");
+  const int64_t tpc = 2 * (128 / group);  // members per prefix-attention CTA
+  if ((static_cast<int64_t>(batch) + tpc - 1) / tpc + num_groups > 65535)
+    return fail(PKV_ERR_UNSUPPORTED, "cascade: too many member blocks in one call");
+  DevInfo *d = nullptr;
+  if ((s = device_info(&d)) != PKV_OK) return s;
+  const pkv::DecodePlan plan = pkv::plan_decode(batch, num_q_heads, g.hkv, g.d,
+                                                effective_hint(max_suffix_len_hint), d->sm_count);
+  const size_t part_bytes = align256(pkv::cascade_partial_bytes(batch, num_q_heads, g.d, plan.splits));
+  const size_t need = part_bytes + pkv::extend_workspace_bytes(num_groups, g.hkv, g.d,
+                                                               static_cast<int32_t>(pcap));
+  if (!workspace)
+    return fail(PKV_ERR_WORKSPACE_TOO_SMALL, "workspace is NULL, %zu bytes needed", need);
+  if (workspace_bytes < need)
+    return fail(PKV_ERR_WORKSPACE_TOO_SMALL, "workspace %zu bytes, %zu needed", workspace_bytes,
+                need);
+  if (!aligned(workspace, 256)) return fail(PKV_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  // 1. suffix partial states (slots 0 .. splits - 1)
+  float *part_o = nullptr, *part_lse = nullptr;
+  cudaError_t e = pkv::launch_cascade_suffix(g, layer, q, o, lse, page_table, table_stride,
+                                             table_idx, seq_lens, batch, num_q_heads, scale, plan,
+                                             workspace, d->err, stream, &part_o, &part_lse);
+  if (e != cudaSuccess) return cuda_fail(e, "cascade suffix launch");
+  // 2. shared-prefix state of every member (slot `splits`): the extend kernels,
+  //    non-causal, one block of queries per group's members
+  pkv::ExtendMode mode;
+  mode.causal = 0;
+  mode.members = members;
+  mode.part_o = part_o;
+  mode.part_lse = part_lse;
+  mode.pstride = plan.splits + 1;
+  mode.pslot = plan.splits;
+  e = pkv::launch_extend(g, layer, q, member_indptr, o, nullptr, prefix_page_table,
+                         prefix_table_stride, nullptr, prefix_lens, num_groups, batch,
+                         num_q_heads, scale, static_cast<int32_t>(pcap),
+                         static_cast<uint8_t *>(workspace) + part_bytes, d->sm_count, d->err,
+                         stream, mode);
+  if (e != cudaSuccess) return cuda_fail(e, "cascade prefix launch");
+  // 3. merge
+  e = pkv::launch_cascade_merge(g, layer, q, o, lse, page_table, table_stride, table_idx,
+                                seq_lens, batch, num_q_heads, scale, plan, part_o, part_lse,
+                                d->err, stream);
+  return e == cudaSuccess ? PKV_OK : cuda_fail(e, "cascade merge launch");
+}
+
 size_t pkv_extend_workspace_size(int32_t batch, int32_t num_kv_heads, int32_t head_dim,
                                  int32_t max_seq_len_hint) {
   if (batch <= 0 || num_kv_heads <= 0 || head_dim <= 0 || max_seq_len_hint < 1) return 0;

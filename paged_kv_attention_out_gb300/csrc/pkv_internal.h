@@ -42,6 +42,37 @@ cudaError_t launch_decode(const PoolGeom &g, int32_t layer, const void *q, void 
                           int32_t hq, float scale, const DecodePlan &plan, void *workspace,
                           unsigned *err, cudaStream_t stream);
 
+// Cascade decode: suffix partial states for split slots 0 .. splits - 1 of
+// [B, Hq, splits + 1] (decode_kernel, always partial), then the merge of those
+// with slot `splits`, the shared-prefix state written by the extend kernel.
+size_t cascade_partial_bytes(int32_t batch, int32_t hq, int32_t d, int32_t splits);
+cudaError_t launch_cascade_suffix(const PoolGeom &g, int32_t layer, const void *q, void *o,
+                                  float *lse, const int32_t *page_table, int64_t table_stride,
+                                  const int32_t *table_idx, const int32_t *seq_lens,
+                                  int32_t batch, int32_t hq, float scale, const DecodePlan &plan,
+                                  void *partials, unsigned *err, cudaStream_t stream,
+                                  float **part_o, float **part_lse);
+cudaError_t launch_cascade_merge(const PoolGeom &g, int32_t layer, const void *q, void *o,
+                                 float *lse, const int32_t *page_table, int64_t table_stride,
+                                 const int32_t *table_idx, const int32_t *seq_lens, int32_t batch,
+                                 int32_t hq, float scale, const DecodePlan &plan, float *part_o,
+                                 float *part_lse, unsigned *err, cudaStream_t stream);
+
+// Where the extend kernel's queries come from and where its results go. The
+// defaults are the extend call: chunk token t of request r is q row
+// qo_indptr[r] + t, causal, bf16 o and lse. The cascade's shared-prefix
+// attention sets members (token t of group r is request members[qo_indptr[r]
+// + t]), causal = 0 (every member sees all seq_lens[r] prefix keys) and
+// writes fp32 partial states into slot `pslot` of [B, Hq, pstride].
+struct ExtendMode {
+  int32_t causal = 1;
+  const int32_t *members = nullptr;
+  float *part_o = nullptr;
+  float *part_lse = nullptr;
+  int32_t pstride = 0;
+  int32_t pslot = 0;
+};
+
 // Gathered-K/V workspace of the extend call: [2][batch][hkv][s_pad][d] bf16,
 // s_pad = capacity rounded up to 128.
 int64_t extend_s_pad(int32_t capacity);
@@ -52,7 +83,8 @@ cudaError_t launch_extend(const PoolGeom &g, int32_t layer, const void *q,
                           const int32_t *page_table, int64_t table_stride,
                           const int32_t *table_idx, const int32_t *seq_lens, int32_t batch,
                           int32_t total_q, int32_t hq, float scale, int32_t capacity,
-                          void *workspace, int32_t sm_count, unsigned *err, cudaStream_t stream);
+                          void *workspace, int32_t sm_count, unsigned *err, cudaStream_t stream,
+                          const ExtendMode &mode = ExtendMode());
 
 cudaError_t launch_merge(const float *o_a, const float *lse_a, const float *o_b,
                          const float *lse_b, void *o_out, bool out_bf16, float *lse_out,

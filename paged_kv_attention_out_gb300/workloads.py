@@ -439,6 +439,89 @@ def random_case(seed: int, *, kind: str = "decode", seq_lens, chunk_lens=None,
                 table_idx=table_idx, qo_indptr=qo)
 
 
+def cascade_case(seed: int, *, group_sizes, prefix_lens, suffix_lo: int = 1,
+                 suffix_hi: int = 64, Hq: int = 4, Hkv: int = 2, D: int = 64, P: int = 1,
+                 shuffled: bool = True, extra_pages: int = 16,
+                 name: str | None = None) -> Case:
+    """Decode case whose requests come in groups sharing a prefix, as a radix
+    cache hit gives: group k has group_sizes[k] members that share its first
+    prefix_lens[k] keys (a multiple of P, possibly 0); each member then has a
+    private suffix of U[suffix_lo, suffix_hi] keys on pages of its own. The
+    request order is shuffled unless `shuffled` is false; the group of each
+    request and each group's prefix length are kept in `notes`."""
+    rng = np.random.default_rng(seed)
+    sizes = [int(n) for n in group_sizes]
+    plens = [int(n) for n in prefix_lens]
+    if len(sizes) != len(plens) or any(n < 1 for n in sizes) or any(p % P for p in plens):
+        raise ValueError("one prefix length (a multiple of P) per non-empty group")
+    group_of = np.repeat(np.arange(len(sizes)), sizes)
+    B = len(group_of)
+    suffix = rng.integers(suffix_lo, suffix_hi + 1, size=B)
+    need = sum(p // P for p in plens) + int(sum((int(n) + P - 1) // P for n in suffix))
+    NP = need + extra_pages
+    perm = rng.permutation(NP)
+    cursor = 0
+    prefix_pages = []
+    for p in plens:
+        prefix_pages.append(list(perm[cursor:cursor + p // P]))
+        cursor += p // P
+    rows = []
+    for b in range(B):
+        k = (int(suffix[b]) + P - 1) // P
+        rows.append(prefix_pages[group_of[b]] + list(perm[cursor:cursor + k]))
+        cursor += k
+    order = rng.permutation(B) if shuffled else np.arange(B)
+    rows = [rows[i] for i in order]
+    group_of = group_of[order]
+    seq = np.array([plens[group_of[b]] + int(suffix[order[b]]) for b in range(B)], np.int64)
+    filler = perm[cursor:]
+    stride = max((int(n) + P - 1) // P for n in seq)
+    token_slots = [_slots_of_row(rows[b], P, int(seq[b])) for b in range(B)]
+    pt = _pad_rows(rows, stride + 1, filler)
+    out_loc = np.array([token_slots[b][-1] for b in range(B)], np.int64)
+    return Case(name=name or f"cascade-{seed}", kind="decode", seed=seed, B=B, Hq=Hq, Hkv=Hkv,
+                D=D, P=P, L=1, NP=NP, layer=0, scale=1.0 / math.sqrt(D),
+                seq_lens=seq.astype(np.int32), page_table=pt, out_loc=out_loc.astype(np.int32),
+                token_slots=token_slots,
+                notes={"group_of_request": group_of.tolist(), "group_prefix": plens})
+
+
+def cascade_tables(case: Case) -> dict:
+    """The tables of a cascade decode call for a case whose requests share
+    per-group prefixes (cascade_case, radix_shared_decode): per group the
+    prefix's page row and length, the member lists, and per request the page
+    row and length of its private suffix. Host numpy int32 arrays; the
+    suffix pages follow from the same slots as the request's full row."""
+    group_of = np.asarray(case.notes["group_of_request"], np.int64)
+    G = int(group_of.max()) + 1 if case.B else 0
+    plens = case.notes.get("group_prefix")
+    if plens is None:
+        plens = [int(case.notes["prefix"])] * G
+    plens = np.asarray(plens, np.int64)
+    P = case.P
+    members = np.argsort(group_of, kind="stable").astype(np.int32)
+    counts = np.bincount(group_of, minlength=G)
+    member_indptr = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    prefix_rows, suffix_rows = [], []
+    for k in range(G):
+        first = int(members[member_indptr[k]])
+        slots = np.asarray(case.token_slots[first][:plens[k]], np.int64)
+        prefix_rows.append(list(slots[::P] // P))
+    suffix_lens = np.zeros(case.B, np.int64)
+    for b in range(case.B):
+        slots = np.asarray(case.token_slots[b][plens[group_of[b]]:], np.int64)
+        suffix_lens[b] = len(slots)
+        suffix_rows.append(list(slots[::P] // P))
+    pstride = max(max((len(r) for r in prefix_rows), default=0), 1)
+    sstride = max(max((len(r) for r in suffix_rows), default=0), 1)
+    zero = np.zeros(1, np.int64)
+    return {"prefix_page_table": _pad_rows(prefix_rows, pstride, zero),
+            "prefix_lens": plens.astype(np.int32),
+            "member_indptr": member_indptr, "members": members,
+            "page_table": _pad_rows(suffix_rows, sstride, zero),
+            "seq_lens": suffix_lens.astype(np.int32)}
+
+
 # --------------------------------------------------------------------------
 # The five named workloads
 # --------------------------------------------------------------------------
@@ -517,6 +600,7 @@ def radix_shared_decode(seed: int = 0, shuffled: bool = False) -> Case:
                 NP=NP, layer=0, scale=1.0 / math.sqrt(128), seq_lens=seq, page_table=pt,
                 out_loc=out_loc, token_slots=token_slots,
                 notes={"groups": groups, "group_size": per, "prefix": prefix,
+                       "group_prefix": [prefix] * groups,
                        "group_of_request": (order // per).tolist()})
 
 

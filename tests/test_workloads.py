@@ -2,6 +2,7 @@
 from __future__ import annotations
 
 import numpy as np
+import pytest
 import torch
 
 from helpers import oracle_run
@@ -86,3 +87,27 @@ def test_compact_case_reproduces_the_full_case():
             rows = np.concatenate([np.arange(c.qo_indptr[b], c.qo_indptr[b + 1])
                                    for b in keep])
         assert np.array_equal(so, o[rows]) and np.array_equal(slse, lse[rows])
+
+
+@pytest.mark.parametrize("P", [1, 16])
+def test_cascade_tables_rebuild_every_key_list(P):
+    """Prefix row + suffix row of each request name exactly its keys, in order."""
+    case = W.cascade_case(5, group_sizes=[3, 70, 1], prefix_lens=[32, 64, 0], P=P, Hq=8, Hkv=2)
+    t = W.cascade_tables(case)
+    gof = np.asarray(case.notes["group_of_request"])
+    for k in range(len(t["prefix_lens"])):
+        mem = t["members"][t["member_indptr"][k]:t["member_indptr"][k + 1]]
+        assert np.all(gof[mem] == k)
+    assert sorted(t["members"].tolist()) == list(range(case.B))
+    for b in range(case.B):
+        g = gof[b]
+        pre = [int(t["prefix_page_table"][g][i // P]) * P + i % P for i in range(t["prefix_lens"][g])]
+        suf = [int(t["page_table"][b][i // P]) * P + i % P for i in range(t["seq_lens"][b])]
+        assert pre + suf == [int(x) for x in case.token_slots[b]]
+
+
+def test_cascade_tables_of_the_radix_workload():
+    case = W.radix_shared_decode(0, shuffled=True)
+    t = W.cascade_tables(case)
+    assert t["prefix_lens"].tolist() == [2048] * 8
+    assert np.all(t["seq_lens"] == case.seq_lens - 2048)
