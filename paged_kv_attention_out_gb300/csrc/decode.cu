@@ -83,8 +83,8 @@ struct DecodeArgs {
   int32_t warps_per_head;
   int32_t chunk;
   int32_t splits;
-  int32_t pstride;        // partial slots per (request, q head): splits, or splits + 1
-                          // when slot `splits` holds a shared-prefix state (cascade)
+  int32_t pstride;        // partial slots per (request, q head): splits, or more when
+                          // slots splits .. pstride - 1 hold shared-prefix states (cascade)
   int32_t force_partial;  // write partial states even for one split (cascade)
   float *part_o;    // [B, Hq, pstride, D]
   float *part_lse;  // [B, Hq, pstride] (natural log)
@@ -379,8 +379,8 @@ __global__ void __launch_bounds__(kThreads, (kStages <= 3 ? 2 : 1)) decode_kerne
 }
 
 // Cross-split merge: one warp per (request, q head) with more than one
-// split; with a cascade's shared-prefix state in slot `splits`, every
-// (request, q head) merges its suffix splits with that slot.
+// split; with a cascade's shared-prefix states in slots splits .. pstride - 1,
+// every (request, q head) merges its suffix splits with those.
 template <int D>
 __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs a, int32_t batch) {
   const int warp = threadIdx.x >> 5;
@@ -392,8 +392,8 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs a, i
   const RowInfo ri = row_info(a, b, false);
   const int n = ri.nsplit;
   if (n <= 1 && !a.force_partial) return;
-  const int total = n + (a.pstride > a.splits ? 1 : 0);  // + the shared-prefix slot
-  auto slot = [&](int s) { return s < n ? s : a.splits; };
+  const int total = n + (a.pstride - a.splits);  // + the shared-prefix slots
+  auto slot = [&](int s) { return s < n ? s : a.splits + (s - n); };
   const float *pl = a.part_lse + bh * a.pstride;
   float M = -INFINITY;
   for (int s = lane; s < total; s += 32) M = fmaxf(M, pl[slot(s)]);
@@ -537,8 +537,8 @@ cudaError_t launch_decode(const PoolGeom &g, int32_t layer, const void *q, void 
   return launch_decode_merge(a, g, batch, stream);
 }
 
-size_t cascade_partial_bytes(int32_t batch, int32_t hq, int32_t d, int32_t splits) {
-  const size_t rows = static_cast<size_t>(batch) * hq * (static_cast<size_t>(splits) + 1);
+size_t cascade_partial_bytes(int32_t batch, int32_t hq, int32_t d, int32_t slots) {
+  const size_t rows = static_cast<size_t>(batch) * hq * static_cast<size_t>(slots);
   return ((rows * d * sizeof(float) + 255) & ~size_t(255)) +
          ((rows * sizeof(float) + 255) & ~size_t(255));
 }
@@ -547,12 +547,13 @@ cudaError_t launch_cascade_suffix(const PoolGeom &g, int32_t layer, const void *
                                   float *lse, const int32_t *page_table, int64_t table_stride,
                                   const int32_t *table_idx, const int32_t *seq_lens,
                                   int32_t batch, int32_t hq, float scale, const DecodePlan &plan,
-                                  void *partials, unsigned *err, cudaStream_t stream,
-                                  float **part_o, float **part_lse) {
+                                  int32_t prefix_slots, void *partials, unsigned *err,
+                                  cudaStream_t stream, float **part_o, float **part_lse) {
   DecodeArgs a = decode_args(g, layer, q, o, lse, page_table, table_stride, table_idx, seq_lens,
                              hq, scale, plan, err);
-  const size_t rows = static_cast<size_t>(batch) * hq * (static_cast<size_t>(plan.splits) + 1);
-  a.pstride = plan.splits + 1;
+  const size_t rows =
+      static_cast<size_t>(batch) * hq * (static_cast<size_t>(plan.splits) + prefix_slots);
+  a.pstride = plan.splits + prefix_slots;
   a.force_partial = 1;
   a.part_o = static_cast<float *>(partials);
   a.part_lse = reinterpret_cast<float *>(static_cast<uint8_t *>(partials) +
@@ -565,11 +566,12 @@ cudaError_t launch_cascade_suffix(const PoolGeom &g, int32_t layer, const void *
 cudaError_t launch_cascade_merge(const PoolGeom &g, int32_t layer, const void *q, void *o,
                                  float *lse, const int32_t *page_table, int64_t table_stride,
                                  const int32_t *table_idx, const int32_t *seq_lens, int32_t batch,
-                                 int32_t hq, float scale, const DecodePlan &plan, float *part_o,
-                                 float *part_lse, unsigned *err, cudaStream_t stream) {
+                                 int32_t hq, float scale, const DecodePlan &plan,
+                                 int32_t prefix_slots, float *part_o, float *part_lse,
+                                 unsigned *err, cudaStream_t stream) {
   DecodeArgs a = decode_args(g, layer, q, o, lse, page_table, table_stride, table_idx, seq_lens,
                              hq, scale, plan, err);
-  a.pstride = plan.splits + 1;
+  a.pstride = plan.splits + prefix_slots;
   a.force_partial = 1;
   a.part_o = part_o;
   a.part_lse = part_lse;

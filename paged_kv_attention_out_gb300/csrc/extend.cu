@@ -143,6 +143,7 @@ struct ExtendArgs {
   float *part_lse;
   int32_t pstride;
   int32_t pslot;
+  int32_t key_splits;  // non-causal: blockIdx.z takes key tiles of range z of this many
 };
 
 // Query token (row of q / o, before the head index) of chunk token `tok` of
@@ -440,10 +441,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int tok1 = max(0, min(tpt, tokens - tpt));
   const int tok0 = min(tpt, tokens);
   // causal: p is the cached prefix, query tile X's last token sees
-  // p + j0 + X tpt + tok_X keys; otherwise every query sees the p keys.
-  const int n0 = a.causal ? (p + j0 + tok0 + kN - 1) / kN : (p + kN - 1) / kN;
-  const int n1 = tok1 == 0 ? 0 : a.causal ? (p + j0 + tpt + tok1 + kN - 1) / kN : (p + kN - 1) / kN;
+  // p + j0 + X tpt + tok_X keys; otherwise every query sees the p keys, and
+  // this CTA takes key tiles tile0 .. tile0 + n - 1 of them (its key range).
+  int tile0 = 0, n_nc = 0;
+  if (!a.causal) {
+    const int nk = (p + kN - 1) / kN;
+    const int per = (nk + a.key_splits - 1) / a.key_splits;
+    tile0 = static_cast<int>(blockIdx.z) * per;
+    n_nc = max(0, min(nk, tile0 + per) - tile0);
+  }
+  const int n0 = a.causal ? (p + j0 + tok0 + kN - 1) / kN : n_nc;
+  const int n1 = tok1 == 0 ? 0 : a.causal ? (p + j0 + tpt + tok1 + kN - 1) / kN : n_nc;
   const int n_tiles = max(n0, n1);
+  const int pslot = a.pslot + static_cast<int>(blockIdx.z);  // partial slot of this key range
   if (n_tiles == 0) {
     // No visible key (an empty shared prefix): o = 0, lse = -inf.
     if (warp < kSoftmaxWarps) {
@@ -453,7 +463,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (qt >= 0) {
         const int64_t bh = static_cast<int64_t>(qt) * a.hq + kvh * a.group + (r % a.group);
         if (a.part_o) {
-          const int64_t prow = bh * a.pstride + a.pslot;
+          const int64_t prow = bh * a.pstride + pslot;
           for (int d = 0; d < D; d += 4)
             *reinterpret_cast<float4 *>(a.part_o + prow * D + d) = make_float4(0.f, 0.f, 0.f, 0.f);
           a.part_lse[prow] = -INFINITY;
@@ -524,8 +534,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive_expect_tx(bar(kBarFull + s), 2 * S::kTileBytes);
 #pragma unroll
         for (int h = 0; h < kHalves; ++h) {
-          tma_load_2d(dst + h * (kN * 128), &kv_map, h * 64, k_run + j * kN, bar(kBarFull + s));
-          tma_load_2d(dst + S::kTileBytes + h * (kN * 128), &kv_map, h * 64, v_run + j * kN,
+          tma_load_2d(dst + h * (kN * 128), &kv_map, h * 64, k_run + (tile0 + j) * kN,
+                      bar(kBarFull + s));
+          tma_load_2d(dst + S::kTileBytes + h * (kN * 128), &kv_map, h * 64,
+                      v_run + (tile0 + j) * kN,
                       bar(kBarFull + s));
         }
       }
@@ -636,7 +648,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld32(srow + 64, *reinterpret_cast<float(*)[32]>(&v[64]));
       tmem_ld32(srow + 96, *reinterpret_cast<float(*)[32]>(&v[96]));
       tmem_ld_wait();
-      const int key0 = j * kN;
+      const int key0 = (tile0 + j) * kN;
       if (key0 + kN - 1 > min_limit) {  // tile crosses some row's last key (warp-uniform)
 #pragma unroll
         for (int cc = 0; cc < kN; ++cc) v[cc] = key0 + cc <= limit ? v[cc] : -INFINITY;
@@ -710,7 +722,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float inv = l > 0.f ? 1.f / l : 0.f;
       const int64_t orow =
           static_cast<int64_t>(valid ? qtok : 0) * a.hq + kvh * a.group + (r % a.group);
-      const int64_t prow = orow * a.pstride + a.pslot;  // cascade partial slot
+      const int64_t prow = orow * a.pstride + pslot;  // cascade partial slot
 #pragma unroll 1
       for (int cb = 0; cb < D / 32; ++cb) {
         float o[32];
@@ -805,6 +817,21 @@ size_t extend_workspace_bytes(int32_t batch, int32_t hkv, int32_t d, int32_t cap
   return kv + 4ull * static_cast<uint64_t>(plan_ints(batch, extend_s_pad(capacity)));
 }
 
+int32_t cascade_prefix_splits(int32_t batch, int32_t hq, int32_t hkv, int32_t num_groups,
+                              int32_t max_prefix, int32_t sm_count) {
+  // Enough (block, kv head, key range) CTAs for about two per SM, each range
+  // at least four key tiles long.
+  const int64_t per = static_cast<int64_t>(kQTiles) * (kM / (hq / hkv));
+  int64_t blocks = (static_cast<int64_t>(batch) + per - 1) / per;
+  if (blocks < num_groups) blocks = num_groups;
+  const int64_t ctas = static_cast<int64_t>(hkv) * (blocks > 0 ? blocks : 1);
+  const int64_t want = (2 * static_cast<int64_t>(sm_count > 0 ? sm_count : 1) + ctas - 1) / ctas;
+  const int64_t nk = (static_cast<int64_t>(max_prefix > 0 ? max_prefix : 0) + kN - 1) / kN;
+  int64_t ks = want < nk / 4 ? want : nk / 4;
+  if (ks > 64) ks = 64;
+  return static_cast<int32_t>(ks < 1 ? 1 : ks);
+}
+
 cudaError_t launch_extend(const PoolGeom &g, int32_t layer, const void *q,
                           const int32_t *qo_indptr, void *o, float *lse,
                           const int32_t *page_table, int64_t table_stride,
@@ -864,6 +891,7 @@ cudaError_t launch_extend(const PoolGeom &g, int32_t layer, const void *q,
   a.part_lse = mode.part_lse;
   a.pstride = mode.pstride;
   a.pslot = mode.pslot;
+  a.key_splits = mode.causal ? 1 : (mode.key_splits < 1 ? 1 : mode.key_splits);
   CUtensorMap kv_map, q_map;
   if (!bf16_map(&kv_map, workspace, ws_rows, static_cast<uint64_t>(g.d), kN) ||
       !bf16_map(&q_map, q, q_rows, static_cast<uint64_t>(g.d), 1))
@@ -874,7 +902,8 @@ cudaError_t launch_extend(const PoolGeom &g, int32_t layer, const void *q,
   // one row of gather CTAs per request, plus one row holding the planner
   const dim3 ggrid(static_cast<unsigned>((s_pad + kGatherKeys - 1) / kGatherKeys),
                    static_cast<unsigned>(batch + 1));
-  const dim3 grid(g.hkv, static_cast<unsigned>(tiles));
+  const dim3 grid(g.hkv, static_cast<unsigned>(tiles),
+                   static_cast<unsigned>(mode.causal ? 1 : mode.key_splits));
   cudaError_t e;
   if (g.d == 128) {
     e = launch_pdl(extend_gather_kernel<128>, ggrid, dim3(kGatherThreads), 0, stream, ga);

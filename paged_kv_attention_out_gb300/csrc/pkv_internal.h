@@ -45,18 +45,22 @@ cudaError_t launch_decode(const PoolGeom &g, int32_t layer, const void *q, void 
 // Cascade decode: suffix partial states for split slots 0 .. splits - 1 of
 // [B, Hq, splits + 1] (decode_kernel, always partial), then the merge of those
 // with slot `splits`, the shared-prefix state written by the extend kernel.
-size_t cascade_partial_bytes(int32_t batch, int32_t hq, int32_t d, int32_t splits);
+size_t cascade_partial_bytes(int32_t batch, int32_t hq, int32_t d, int32_t slots);
+// Key ranges the shared prefix of a cascade is cut into, from host sizes only.
+int32_t cascade_prefix_splits(int32_t batch, int32_t hq, int32_t hkv, int32_t num_groups,
+                              int32_t max_prefix, int32_t sm_count);
 cudaError_t launch_cascade_suffix(const PoolGeom &g, int32_t layer, const void *q, void *o,
                                   float *lse, const int32_t *page_table, int64_t table_stride,
                                   const int32_t *table_idx, const int32_t *seq_lens,
                                   int32_t batch, int32_t hq, float scale, const DecodePlan &plan,
-                                  void *partials, unsigned *err, cudaStream_t stream,
-                                  float **part_o, float **part_lse);
+                                  int32_t prefix_slots, void *partials, unsigned *err,
+                                  cudaStream_t stream, float **part_o, float **part_lse);
 cudaError_t launch_cascade_merge(const PoolGeom &g, int32_t layer, const void *q, void *o,
                                  float *lse, const int32_t *page_table, int64_t table_stride,
                                  const int32_t *table_idx, const int32_t *seq_lens, int32_t batch,
-                                 int32_t hq, float scale, const DecodePlan &plan, float *part_o,
-                                 float *part_lse, unsigned *err, cudaStream_t stream);
+                                 int32_t hq, float scale, const DecodePlan &plan,
+                                 int32_t prefix_slots, float *part_o, float *part_lse,
+                                 unsigned *err, cudaStream_t stream);
 
 // Where the extend kernel's queries come from and where its results go. The
 // defaults are the extend call: chunk token t of request r is q row
@@ -71,6 +75,7 @@ struct ExtendMode {
   float *part_lse = nullptr;
   int32_t pstride = 0;
   int32_t pslot = 0;
+  int32_t key_splits = 1;  // non-causal: key ranges per block (slots pslot .. + key_splits - 1)
 };
 
 // Gathered-K/V workspace of the extend call: [2][batch][hkv][s_pad][d] bf16,
