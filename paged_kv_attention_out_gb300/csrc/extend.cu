@@ -819,13 +819,13 @@ size_t extend_workspace_bytes(int32_t batch, int32_t hkv, int32_t d, int32_t cap
 
 int32_t cascade_prefix_splits(int32_t batch, int32_t hq, int32_t hkv, int32_t num_groups,
                               int32_t max_prefix, int32_t sm_count) {
-  // Enough (block, kv head, key range) CTAs for about two per SM, each range
-  // at least four key tiles long.
+  // As many key ranges as keep the (block, kv head, key range) CTAs within
+  // one wave (one CTA per SM), each range at least four key tiles long.
   const int64_t per = static_cast<int64_t>(kQTiles) * (kM / (hq / hkv));
   int64_t blocks = (static_cast<int64_t>(batch) + per - 1) / per;
   if (blocks < num_groups) blocks = num_groups;
   const int64_t ctas = static_cast<int64_t>(hkv) * (blocks > 0 ? blocks : 1);
-  const int64_t want = (2 * static_cast<int64_t>(sm_count > 0 ? sm_count : 1) + ctas - 1) / ctas;
+  const int64_t want = static_cast<int64_t>(sm_count > 0 ? sm_count : 1) / ctas;
   const int64_t nk = (static_cast<int64_t>(max_prefix > 0 ? max_prefix : 0) + kN - 1) / kN;
   int64_t ks = want < nk / 4 ? want : nk / 4;
   if (ks > 64) ks = 64;
