@@ -609,10 +609,38 @@ def _tiny_workload(args, dev, flush, steps, warm):
     wl = Workload(case, dev)
     st, at = _measure(wl, steps, warm, flush)
     out["tiny-decode"] = {"metric": "step latency", "value": round(st * 1e3, 2), "unit": "us",
-                          "attention_us": round(at * 1e3, 2)}
+                          "attention_us": round(at * 1e3, 2),
+                          "graph_replay_us": round(_graph_replay_us(wl, steps, warm), 2)}
     del wl
     torch.cuda.empty_cache()
     return out
+
+
+def _graph_replay_us(wl: Workload, steps: int, warm: int) -> float:
+    """Mean device time of one store_kv + attention step captured in a CUDA
+    graph and replayed back to back (the serving engine replays decode steps
+    from graphs): launch overhead out of the picture."""
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        wl.store()
+        wl.attention()
+        with torch.cuda.graph(g, stream=s):
+            wl.store()
+            wl.attention()
+    torch.cuda.current_stream().wait_stream(s)
+    for _ in range(warm):
+        g.replay()
+    torch.cuda.synchronize()
+    reps = max(steps, 20)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) * 1e3 / reps
 
 
 # ---------------------------------------------------------------------------
