@@ -50,12 +50,12 @@ CSRC = os.path.join(ROOT, "paged_kv_attention_out_gb300", "csrc")
 MEASURED_TRAFFIC = {
     # profiles/decode_kernel_llama3-8b-decode.md: decode_kernel + decode_merge_kernel
     "decode": {"sources": ["decode.cu", "pkv_common.cuh"],
-               "sha256": "a015a442f6f44e5aea7058cdc64bede1ebc910c50fabe05fbbc0f0d2a1f11b20",
-               "bytes": 628803840},
+               "sha256": "2cf005893bbbba2f5f0aa8f39532cc188f8e4d321b0b179c718e195bfa41f63e",
+               "bytes": 628541952},
     # profiles/extend_kernels_chunked-prefill-extend.md: extend_gather_kernel + extend_tc_kernel
     "extend": {"sources": ["extend.cu", "tc_common.cuh", "pkv_common.cuh"],
-               "sha256": "edfa342202ee7ebb1a80b0f4af7fca8d4a198a175b8ae58c72229c8c7cbabeed",
-               "bytes": 522022912},
+               "sha256": "f0f47d24aedf8eddc2c5e6f19f65c867787df5a88813101df53ca606bca703a6",
+               "bytes": 521340928},
 }
 
 
