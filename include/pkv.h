@@ -151,6 +151,30 @@ pkv_status pkv_paged_decode_attn(const pkv_pool *pool, int32_t layer, const void
                                  int32_t max_seq_len_hint, void *workspace,
                                  size_t workspace_bytes, cudaStream_t stream);
 
+/*
+ * One decode step with store_kv fused in ("Code Notes: mini-sglang", Engine
+ * Layer table, BaseKVCachePool row: the new token's K and V are written into
+ * the pool, then attention reads the pool; GraphRunner row: decode steps are
+ * launch-bound, so one launch fewer matters). For every request b the new
+ * rows k_new[b, :, :] and v_new[b, :, :] (device bf16, [batch, Hkv, D] with
+ * kv_row_stride elements between requests, 16-byte aligned, stride >= Hkv*D
+ * and a multiple of 8) are stored at key position seq_lens[b] - 1 of its
+ * page_table row (the slot P * row[(n-1)/P] + (n-1)%P, n = seq_lens[b]),
+ * then attention runs exactly as pkv_paged_decode_attn (same arguments,
+ * workspace from pkv_decode_workspace_size). Equivalent to pkv_kv_store with
+ * out_loc[b] = that slot followed by pkv_paged_decode_attn; requests with
+ * seq_lens[b] = 0 store nothing. A bad page id at that position is flagged
+ * (PKV_DEVERR_PAGE_RANGE) and nothing is stored for it.
+ */
+pkv_status pkv_paged_decode_attn_store(const pkv_pool *pool, int32_t layer, const void *q,
+                                       const void *k_new, const void *v_new,
+                                       int64_t kv_row_stride, void *o, float *lse,
+                                       const int32_t *page_table, int64_t table_stride,
+                                       const int32_t *table_idx, const int32_t *seq_lens,
+                                       int32_t batch, int32_t num_q_heads, float scale,
+                                       int32_t max_seq_len_hint, void *workspace,
+                                       size_t workspace_bytes, cudaStream_t stream);
+
 /* Size of the library-owned scratch used by pkv_paged_decode_attn_noalloc. */
 #define PKV_NOALLOC_SCRATCH_BYTES (32u << 20)
 

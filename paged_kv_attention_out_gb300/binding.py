@@ -66,6 +66,10 @@ def load() -> ctypes.CDLL:
     L.pkv_paged_decode_attn.argtypes = [pool_p, _c_int32, _p, _p, _p, _p, _c_int64, _p, _p,
                                         _c_int32, _c_int32, ctypes.c_float, _c_int32, _p,
                                         ctypes.c_size_t, _p]
+    L.pkv_paged_decode_attn_store.restype = ctypes.c_int
+    L.pkv_paged_decode_attn_store.argtypes = [pool_p, _c_int32, _p, _p, _p, _c_int64, _p, _p, _p,
+                                              _c_int64, _p, _p, _c_int32, _c_int32,
+                                              ctypes.c_float, _c_int32, _p, ctypes.c_size_t, _p]
     L.pkv_paged_decode_attn_noalloc.restype = ctypes.c_int
     L.pkv_paged_decode_attn_noalloc.argtypes = [pool_p, _c_int32, _p, _p, _p, _p, _c_int64, _p,
                                                 _p, _c_int32, _c_int32, ctypes.c_float,
@@ -184,6 +188,39 @@ def pkv_paged_decode_attn(pool, layer: int, q, o, lse, page_table, seq_lens, sca
         ctypes.byref(ps), int(layer), _ptr(q), _ptr(o), _ptr(lse), _ptr(page_table),
         page_table.shape[1], _ptr(table_idx), _ptr(seq_lens), B, Hq, float(scale),
         int(max_seq_len_hint), _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def pkv_paged_decode_attn_store(pool, layer: int, q, k_new, v_new, o, lse, page_table, seq_lens,
+                                scale: float, max_seq_len_hint: int, workspace=None,
+                                table_idx=None, stream=None) -> None:
+    """Decode step with store_kv fused: k_new, v_new [B, Hkv, D] bf16 go to key
+    seq_lens[b] - 1 of each row, then decode as pkv_paged_decode_attn."""
+    ps = pool_struct(pool)
+    _want(q, torch.bfloat16, "q", 3)
+    _want(o, torch.bfloat16, "o", 3)
+    _contig(q, "q")
+    _contig(o, "o")
+    for t, name in ((k_new, "k_new"), (v_new, "v_new")):
+        _want(t, torch.bfloat16, name, 3)
+    if k_new.stride(0) != v_new.stride(0) or k_new.stride(1) != k_new.shape[2] \
+            or k_new.stride(2) != 1 or v_new.stride(1) != v_new.shape[2] or v_new.stride(2) != 1:
+        raise ValueError("k_new and v_new rows must share a row stride with heads/dims contiguous")
+    _want(page_table, torch.int32, "page_table", 2)
+    _contig(page_table, "page_table")
+    _want(seq_lens, torch.int32, "seq_lens", 1)
+    B, Hq, D = q.shape
+    if o.shape != q.shape or seq_lens.shape[0] != B or k_new.shape[0] != B:
+        raise ValueError("o must match q; seq_lens and k_new must have batch entries")
+    if lse is not None:
+        _want(lse, torch.float32, "lse", 2)
+        _contig(lse, "lse")
+    if table_idx is not None:
+        _want(table_idx, torch.int32, "table_idx", 1)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load().pkv_paged_decode_attn_store(
+        ctypes.byref(ps), int(layer), _ptr(q), _ptr(k_new), _ptr(v_new), k_new.stride(0), _ptr(o),
+        _ptr(lse), _ptr(page_table), page_table.shape[1], _ptr(table_idx), _ptr(seq_lens), B, Hq,
+        float(scale), int(max_seq_len_hint), _ptr(workspace), ws_bytes, _stream(stream)))
 
 
 def pkv_paged_decode_attn_noalloc(pool, layer: int, q, o, lse, page_table, seq_lens,

@@ -89,6 +89,13 @@ struct DecodeArgs {
   float *part_o;    // [B, Hq, pstride, D]
   float *part_lse;  // [B, Hq, pstride] (natural log)
   unsigned *err;
+  // store_kv fused into the step (may be null): request b's new key and
+  // value rows k_new[b], v_new[b] (row stride kv_row_stride elements) go to
+  // key seq_len - 1 of its row before it is attended
+  const __nv_bfloat16 *k_new;
+  const __nv_bfloat16 *v_new;
+  int64_t kv_row_stride;
+  __nv_bfloat16 *pool_w;
 };
 
 __device__ __forceinline__ float fast_exp2(float x) {
@@ -142,6 +149,32 @@ __global__ void __launch_bounds__(kThreads, (kStages <= 3 ? 2 : 1)) decode_kerne
   grid_dependents_launch();  // the split merge may be scheduled as CTAs drain
   const RowInfo ri = row_info(a, b, split == 0 && blockIdx.x == 0 && threadIdx.x == 0);
   if (split >= ri.nsplit) return;
+  if (a.k_new) {
+    // Fused store: the split holding key seq - 1 writes the new token's K and
+    // V rows of its kv heads first; no other CTA reads that key of these heads.
+    if (split == ri.nsplit - 1 && ri.seq > 0) {
+      const int pos = ri.seq - 1;
+      const int pe = __ldg(ri.row + pos / a.page_size);
+      const int64_t slot = static_cast<int64_t>(pe) * a.page_size + pos % a.page_size;
+      if (pe < 0 || slot >= a.slots) {
+        if (threadIdx.x == 0) flag_error(a.err, kErrPage);
+      } else {
+        constexpr int kCh = D / 8;  // 16-byte chunks per head row
+        for (int i = threadIdx.x; i < a.heads_per_cta * 2 * kCh; i += kThreads) {
+          const int ch = i % kCh;
+          const int c = (i / kCh) & 1;
+          const int h = blockIdx.x * a.heads_per_cta + i / kCh / 2;
+          const __nv_bfloat16 *src =
+              (c ? a.v_new : a.k_new) + static_cast<int64_t>(b) * a.kv_row_stride + h * D + ch * 8;
+          __nv_bfloat16 *dst = a.pool_w + (static_cast<int64_t>(c) * a.num_layers + a.layer) * a.plane +
+                               slot * a.hkv * D + h * D + ch * 8;
+          *reinterpret_cast<uint4 *>(dst) = *reinterpret_cast<const uint4 *>(src);
+        }
+      }
+      __threadfence();  // visible to this CTA's copies (and the GPU) before they read it
+    }
+    __syncthreads();
+  }
   const int key_begin = split * a.chunk;
   const int key_end = (split == ri.nsplit - 1) ? ri.seq : key_begin + a.chunk;
 
@@ -523,9 +556,15 @@ cudaError_t launch_decode(const PoolGeom &g, int32_t layer, const void *q, void 
                           const int32_t *page_table, int64_t table_stride,
                           const int32_t *table_idx, const int32_t *seq_lens, int32_t batch,
                           int32_t hq, float scale, const DecodePlan &plan, void *workspace,
-                          unsigned *err, cudaStream_t stream) {
+                          unsigned *err, cudaStream_t stream, const void *k_new,
+                          const void *v_new, int64_t kv_row_stride) {
   DecodeArgs a = decode_args(g, layer, q, o, lse, page_table, table_stride, table_idx, seq_lens,
                              hq, scale, plan, err);
+  a.k_new = static_cast<const __nv_bfloat16 *>(k_new);
+  a.v_new = static_cast<const __nv_bfloat16 *>(v_new);
+  a.kv_row_stride = kv_row_stride;
+  // the pool is the caller's writable buffer (store_kv writes it too)
+  a.pool_w = const_cast<__nv_bfloat16 *>(static_cast<const __nv_bfloat16 *>(g.base));
   if (plan.splits > 1) {
     const size_t rows = static_cast<size_t>(batch) * hq * plan.splits;
     const size_t o_bytes = (rows * g.d * sizeof(float) + 255) & ~size_t(255);

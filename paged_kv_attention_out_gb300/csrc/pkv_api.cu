@@ -173,12 +173,15 @@ size_t pkv_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num
       .workspace_bytes;
 }
 
-pkv_status pkv_paged_decode_attn(const pkv_pool *pool, int32_t layer, const void *q, void *o,
-                                 float *lse, const int32_t *page_table, int64_t table_stride,
-                                 const int32_t *table_idx, const int32_t *seq_lens,
-                                 int32_t batch, int32_t num_q_heads, float scale,
-                                 int32_t max_seq_len_hint, void *workspace,
-                                 size_t workspace_bytes, cudaStream_t stream) {
+// Decode, optionally with the step's new key / value rows stored first
+// (k_new != NULL: the fused store of pkv_paged_decode_attn_store).
+static pkv_status decode_call(const pkv_pool *pool, int32_t layer, const void *q,
+                              const void *k_new, const void *v_new, int64_t kv_row_stride,
+                              void *o, float *lse, const int32_t *page_table,
+                              int64_t table_stride, const int32_t *table_idx,
+                              const int32_t *seq_lens, int32_t batch, int32_t num_q_heads,
+                              float scale, int32_t max_seq_len_hint, void *workspace,
+                              size_t workspace_bytes, cudaStream_t stream) {
   pkv::PoolGeom g;
   pkv_status s = check_pool(pool, layer, &g);
   if (s != PKV_OK) return s;
@@ -218,8 +221,41 @@ pkv_status pkv_paged_decode_attn(const pkv_pool *pool, int32_t layer, const void
   }
   cudaError_t e = pkv::launch_decode(g, layer, q, o, lse, page_table, table_stride, table_idx,
                                      seq_lens, batch, num_q_heads, scale, plan, workspace, d->err,
-                                     stream);
+                                     stream, k_new, v_new, kv_row_stride);
   return e == cudaSuccess ? PKV_OK : cuda_fail(e, "decode launch");
+}
+
+pkv_status pkv_paged_decode_attn(const pkv_pool *pool, int32_t layer, const void *q, void *o,
+                                 float *lse, const int32_t *page_table, int64_t table_stride,
+                                 const int32_t *table_idx, const int32_t *seq_lens,
+                                 int32_t batch, int32_t num_q_heads, float scale,
+                                 int32_t max_seq_len_hint, void *workspace,
+                                 size_t workspace_bytes, cudaStream_t stream) {
+  return decode_call(pool, layer, q, nullptr, nullptr, 0, o, lse, page_table, table_stride,
+                     table_idx, seq_lens, batch, num_q_heads, scale, max_seq_len_hint, workspace,
+                     workspace_bytes, stream);
+}
+
+pkv_status pkv_paged_decode_attn_store(const pkv_pool *pool, int32_t layer, const void *q,
+                                       const void *k_new, const void *v_new,
+                                       int64_t kv_row_stride, void *o, float *lse,
+                                       const int32_t *page_table, int64_t table_stride,
+                                       const int32_t *table_idx, const int32_t *seq_lens,
+                                       int32_t batch, int32_t num_q_heads, float scale,
+                                       int32_t max_seq_len_hint, void *workspace,
+                                       size_t workspace_bytes, cudaStream_t stream) {
+  if (batch > 0) {
+    if (!k_new || !v_new) return fail(PKV_ERR_INVALID_ARG, "k_new and v_new must be non-NULL");
+    if (!aligned(k_new, 16) || !aligned(v_new, 16))
+      return fail(PKV_ERR_INVALID_ARG, "k_new and v_new must be 16-byte aligned");
+    if (pool && (kv_row_stride < static_cast<int64_t>(pool->num_kv_heads) * pool->head_dim ||
+                 kv_row_stride % 8 != 0))
+      return fail(PKV_ERR_INVALID_ARG, "kv_row_stride %lld must be >= Hkv*D and a multiple of 8",
+                  static_cast<long long>(kv_row_stride));
+  }
+  return decode_call(pool, layer, q, batch > 0 ? k_new : nullptr, v_new, kv_row_stride, o, lse,
+                     page_table, table_stride, table_idx, seq_lens, batch, num_q_heads, scale,
+                     max_seq_len_hint, workspace, workspace_bytes, stream);
 }
 
 static size_t align256(size_t n) { return (n + 255) & ~size_t(255); }

@@ -40,7 +40,8 @@ cudaError_t launch_decode(const PoolGeom &g, int32_t layer, const void *q, void 
                           const int32_t *page_table, int64_t table_stride,
                           const int32_t *table_idx, const int32_t *seq_lens, int32_t batch,
                           int32_t hq, float scale, const DecodePlan &plan, void *workspace,
-                          unsigned *err, cudaStream_t stream);
+                          unsigned *err, cudaStream_t stream, const void *k_new = nullptr,
+                          const void *v_new = nullptr, int64_t kv_row_stride = 0);
 
 // Cascade decode: suffix partial states for split slots 0 .. splits - 1 of
 // [B, Hq, splits + 1] (decode_kernel, always partial), then the merge of those
