@@ -425,16 +425,20 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs a, i
   const RowInfo ri = row_info(a, b, false);
   const int n = ri.nsplit;
   if (n <= 1 && !a.force_partial) return;
-  const int total = n + (a.pstride - a.splits);  // + the shared-prefix slots
-  auto slot = [&](int s) { return s < n ? s : a.splits + (s - n); };
+  // suffix splits in slots 0 .. n - 1, shared-prefix states (cascade) in
+  // slots splits .. pstride - 1
+  const int extra = a.pstride - a.splits;
   const float *pl = a.part_lse + bh * a.pstride;
+  const float *pe = pl + a.splits;
   float M = -INFINITY;
-  for (int s = lane; s < total; s += 32) M = fmaxf(M, pl[slot(s)]);
+  for (int s = lane; s < n; s += 32) M = fmaxf(M, pl[s]);
+  for (int s = lane; s < extra; s += 32) M = fmaxf(M, pe[s]);
 #pragma unroll
   for (int x = 16; x > 0; x >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, x));
   const float ref = M == -INFINITY ? 0.f : M;
   float L = 0.f;
-  for (int s = lane; s < total; s += 32) L += expf(pl[slot(s)] - ref);
+  for (int s = lane; s < n; s += 32) L += expf(pl[s] - ref);
+  for (int s = lane; s < extra; s += 32) L += expf(pe[s] - ref);
 #pragma unroll
   for (int x = 16; x > 0; x >>= 1) L += __shfl_xor_sync(0xffffffffu, L, x);
   const float inv = L > 0.f ? 1.f / L : 0.f;
@@ -442,9 +446,18 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs a, i
     float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
     const float *po = a.part_o + bh * a.pstride * D + lane * 4;
 #pragma unroll 4
-    for (int s = 0; s < total; ++s) {
-      const float w = expf(pl[slot(s)] - ref) * inv;
-      const float4 v = *reinterpret_cast<const float4 *>(po + static_cast<int64_t>(slot(s)) * D);
+    for (int s = 0; s < n; ++s) {
+      const float w = expf(pl[s] - ref) * inv;
+      const float4 v = *reinterpret_cast<const float4 *>(po + static_cast<int64_t>(s) * D);
+      O.x += w * v.x;
+      O.y += w * v.y;
+      O.z += w * v.z;
+      O.w += w * v.w;
+    }
+    for (int s = 0; s < extra; ++s) {
+      const float w = expf(pe[s] - ref) * inv;
+      const float4 v =
+          *reinterpret_cast<const float4 *>(po + static_cast<int64_t>(a.splits + s) * D);
       O.x += w * v.x;
       O.y += w * v.y;
       O.z += w * v.z;
