@@ -87,6 +87,27 @@ def test_bad_host_arguments_are_rejected_before_any_gpu_work(lib):
     # the workspace query refuses nonsense instead of guessing
     assert lib.pkv_decode_workspace_size(0, 32, 8, 128, 4096) == 0
     assert lib.pkv_decode_workspace_size(4, 30, 8, 128, 4096) == 0
+    assert lib.pkv_extend_workspace_size(0, 8, 128, 4096) == 0
+    assert lib.pkv_cascade_workspace_size(4, 32, 8, 128, 0, 2048, 512) == 0
+    assert lib.pkv_cascade_workspace_size(4, 30, 8, 128, 2, 2048, 512) == 0
+    # fused store + decode: NULL or misaligned new rows, row stride below Hkv * D
+    f = ctypes.c_float(1.0)
+    assert lib.pkv_paged_decode_attn_store(ctypes.byref(pool), 0, 16, None, 16, 256, 16, None,
+                                           16, 4, None, 16, 1, 4, f, 4, None, 0, None) == 1
+    assert lib.pkv_paged_decode_attn_store(ctypes.byref(pool), 0, 16, 18, 16, 256, 16, None,
+                                           16, 4, None, 16, 1, 4, f, 4, None, 0, None) == 1
+    assert lib.pkv_paged_decode_attn_store(ctypes.byref(pool), 0, 16, 16, 16, 128, 16, None,
+                                           16, 4, None, 16, 1, 4, f, 4, None, 0, None) == 1
+    # cascade: group above 8; every request must be in a group; NULL member lists
+    assert lib.pkv_paged_cascade_decode_attn(
+        ctypes.byref(pool), 0, 16, 16, None, 16, 4, 16, 16, 16, 1, 16, 4, None, 16, 1, 32, f,
+        64, 64, None, 0, None) == 2
+    assert lib.pkv_paged_cascade_decode_attn(
+        ctypes.byref(pool), 0, 16, 16, None, 16, 4, 16, 16, 16, 0, 16, 4, None, 16, 1, 4, f,
+        64, 64, None, 0, None) == 1
+    assert lib.pkv_paged_cascade_decode_attn(
+        ctypes.byref(pool), 0, 16, 16, None, 16, 4, 16, None, None, 1, 16, 4, None, 16, 1, 4, f,
+        64, 64, None, 0, None) == 1
 
 
 @pytest.mark.gpu
