@@ -406,3 +406,28 @@ def test_oracle_rejects_bad_arguments():
         oracle.decode_attn(pool, 0, q, bad, case.seq_lens, case.scale)
     with pytest.raises(ValueError):
         oracle.kv_store(pool, 0, k, v, np.array([case.NP * case.P], np.int32))
+
+
+@pytest.mark.parametrize("P", [1, 8])
+def test_cascade_decomposition_of_shared_prefix_decode(P):
+    """Reading R11: a request of a shared-prefix group attends to its group's
+    prefix keys followed by its own suffix keys, so its attention is the
+    log-sum-exp merge of attention over the prefix row and attention over the
+    suffix row (the merge invariant, pinned above, applied to the cascade
+    tables); an empty prefix leaves the suffix state unchanged."""
+    case = W.cascade_case(4, group_sizes=[3, 5, 2], prefix_lens=[16, 40, 0], P=P, Hq=4, Hkv=2,
+                          D=32, suffix_lo=1, suffix_hi=30)
+    want_o, want_lse, pool = oracle_run(case)
+    q = W.bf16_bits(case.q())
+    t = W.cascade_tables(case)
+    gof = np.asarray(case.notes["group_of_request"])
+    # the prefix state of each request: its group's prefix row
+    pre_pt = t["prefix_page_table"][gof]
+    pre_len = t["prefix_lens"][gof]
+    o_p, l_p = oracle.decode_attn(pool, case.layer, q, pre_pt, pre_len, case.scale)
+    o_s, l_s = oracle.decode_attn(pool, case.layer, q, t["page_table"], t["seq_lens"], case.scale)
+    o, lse = oracle.merge_lse(o_p, l_p, o_s, l_s)
+    assert np.allclose(o, want_o, atol=1e-12, rtol=0) and np.allclose(lse, want_lse, atol=1e-12)
+    empty = pre_len == 0
+    assert empty.any()
+    assert np.array_equal(o[empty], o_s[empty]) and np.array_equal(lse[empty], l_s[empty])
