@@ -51,8 +51,8 @@ CSRC = os.path.join(ROOT, "paged_kv_attention_out_gb300", "csrc")
 MEASURED_TRAFFIC = {
     # profiles/decode_kernel_llama3-8b-decode.md: decode_kernel + decode_merge_kernel
     "decode": {"sources": ["decode.cu", "pkv_common.cuh"],
-               "sha256": "2cf005893bbbba2f5f0aa8f39532cc188f8e4d321b0b179c718e195bfa41f63e",
-               "bytes": 628541952},
+               "sha256": "6526d6a1e89fdc5f79beaebf48fcbafd2935aa21187edbb9e5ef219bb641c0b4",
+               "bytes": 628446208},
     # profiles/extend_kernels_chunked-prefill-extend.md: extend_gather_kernel + extend_tc_kernel
     "extend": {"sources": ["extend.cu", "tc_common.cuh", "pkv_common.cuh"],
                "sha256": "f0f47d24aedf8eddc2c5e6f19f65c867787df5a88813101df53ca606bca703a6",
