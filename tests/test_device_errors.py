@@ -1,0 +1,136 @@
+"""Device-side argument checks of the attention calls: values in device
+memory that would index outside the pool, the tables or the workspace are
+skipped on the device (never dereferenced) and reported in the device error
+word (pkv_read_device_errors); requests not involved are computed as usual."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+from helpers import compare, gpu_inputs, oracle_run
+from paged_kv_attention_out_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+PAGE, SEQ, INDPTR = 0x2, 0x4, 0x8
+
+
+def _errors():
+    import paged_kv_attention_out_gb300 as pkv
+    torch.cuda.synchronize()
+    return pkv.pkv_read_device_errors()
+
+
+def _decode(case, pool, q, t, fused=None):
+    import paged_kv_attention_out_gb300 as pkv
+    h = case.max_seq_len
+    ws = torch.empty(max(pkv.pkv_decode_workspace_size(case.B, case.Hq, case.Hkv, case.D, h), 256),
+                     dtype=torch.uint8, device="cuda")
+    o = torch.empty_like(q)
+    if fused is None:
+        pkv.pkv_paged_decode_attn(pool, case.layer, q, o, None, t["page_table"], t["seq_lens"],
+                                  case.scale, h, ws)
+    else:
+        k, v = fused
+        pkv.pkv_paged_decode_attn_store(pool, case.layer, q, k, v, o, None, t["page_table"],
+                                        t["seq_lens"], case.scale, h, ws)
+    return o
+
+
+@pytest.mark.parametrize("fused", [False, True])
+def test_decode_page_id_out_of_range_is_flagged(fused):
+    import paged_kv_attention_out_gb300 as pkv
+    case = W.random_case(31, seq_lens=[200, 90, 300], Hq=8, Hkv=2, D=128, P=16)
+    pool, k, v, q, t = gpu_inputs(case)
+    if not fused:
+        pkv.pkv_kv_store(pool, case.layer, k, v, t["out_loc"])
+    pt = t["page_table"].clone()
+    pt[1, 2] = case.NP + 1000  # a page id past the pool in request 1's row
+    pt[1, (90 - 1) // 16] = -7  # and its newest key's page (the fused store's target)
+    _errors()
+    o = _decode(case, pool, q, dict(t, page_table=pt), fused=(k, v) if fused else None)
+    assert _errors() & PAGE
+    want, _, _ = oracle_run(case)
+    got = o.float().cpu().double().numpy()
+    ok = [0, 2]
+    compare(got[ok], want[ok])
+
+
+def test_decode_seq_len_past_the_row_is_flagged():
+    import paged_kv_attention_out_gb300 as pkv
+    case = W.random_case(32, seq_lens=[64, 100, 33], Hq=4, Hkv=2, D=64, P=1)
+    pool, k, v, q, t = gpu_inputs(case)
+    pkv.pkv_kv_store(pool, case.layer, k, v, t["out_loc"])
+    sl = t["seq_lens"].clone()
+    sl[0] = case.page_table.shape[1] * case.P + 5
+    _errors()
+    o = _decode(case, pool, q, dict(t, seq_lens=sl))
+    assert _errors() & SEQ
+    want, _, _ = oracle_run(case)
+    compare(o.float().cpu().double().numpy()[1:], want[1:])
+
+
+def test_extend_request_longer_than_the_hint_is_flagged_and_skipped():
+    import paged_kv_attention_out_gb300 as pkv
+    case = W.random_case(33, kind="extend", seq_lens=[100, 700, 60], chunk_lens=[40, 100, 60],
+                         Hq=8, Hkv=2, D=128, P=1)
+    pool, k, v, q, t = gpu_inputs(case)
+    pkv.pkv_kv_store(pool, case.layer, k, v, t["out_loc"])
+    hint = 200  # request 1 (700 keys) is beyond it
+    ws = torch.empty(pkv.pkv_extend_workspace_size(case.B, case.Hkv, case.D, hint),
+                     dtype=torch.uint8, device="cuda")
+    o = torch.zeros_like(q)
+    _errors()
+    pkv.pkv_paged_extend_attn(pool, case.layer, q, t["qo_indptr"], o, None, t["page_table"],
+                              t["seq_lens"], case.scale, hint, ws)
+    assert _errors() & SEQ
+    want, _, _ = oracle_run(case)
+    got = o.float().cpu().double().numpy()
+    rows = np.r_[0:40, 140:200]  # requests 0 and 2
+    compare(got[rows], want[rows])
+
+
+def test_extend_malformed_qo_indptr_is_flagged():
+    import paged_kv_attention_out_gb300 as pkv
+    case = W.random_case(34, kind="extend", seq_lens=[100, 120, 60], chunk_lens=[40, 50, 60],
+                         Hq=8, Hkv=2, D=64, P=1)
+    pool, k, v, q, t = gpu_inputs(case)
+    pkv.pkv_kv_store(pool, case.layer, k, v, t["out_loc"])
+    qo = t["qo_indptr"].clone()
+    qo[2] = 10  # decreasing: request 1 would have a negative chunk
+    h = case.max_seq_len
+    ws = torch.empty(pkv.pkv_extend_workspace_size(case.B, case.Hkv, case.D, h),
+                     dtype=torch.uint8, device="cuda")
+    o = torch.zeros_like(q)
+    _errors()
+    pkv.pkv_paged_extend_attn(pool, case.layer, q, qo, o, None, t["page_table"], t["seq_lens"],
+                              case.scale, h, ws)
+    assert _errors() & INDPTR
+    want, _, _ = oracle_run(case)
+    compare(o.float().cpu().double().numpy()[:40], want[:40])  # request 0 still computed
+
+
+def test_cascade_member_out_of_range_is_flagged():
+    import paged_kv_attention_out_gb300 as pkv
+    case = W.cascade_case(35, group_sizes=[6, 3], prefix_lens=[64, 32], Hq=8, Hkv=2, D=64)
+    pool, k, v, q, t = gpu_inputs(case)
+    pkv.pkv_kv_store(pool, case.layer, k, v, t["out_loc"])
+    ct = {n: torch.as_tensor(a, dtype=torch.int32, device="cuda")
+          for n, a in W.cascade_tables(case).items()}
+    members = ct["members"].clone()
+    bad = int(members[0])
+    members[0] = case.B + 50
+    pmax, smax = 64, int(ct["seq_lens"].max())
+    ws = torch.empty(pkv.pkv_cascade_workspace_size(case.B, case.Hq, case.Hkv, case.D, 2, pmax,
+                                                    smax), dtype=torch.uint8, device="cuda")
+    o = torch.zeros_like(q)
+    _errors()
+    pkv.pkv_paged_cascade_decode_attn(pool, case.layer, q, o, None, ct["prefix_page_table"],
+                                      ct["prefix_lens"], ct["member_indptr"], members,
+                                      ct["page_table"], ct["seq_lens"], case.scale, pmax, smax,
+                                      ws)
+    assert _errors() & INDPTR
+    want, _, _ = oracle_run(case)
+    ok = [b for b in range(case.B) if b != bad]
+    compare(o.float().cpu().double().numpy()[ok], want[ok])
