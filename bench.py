@@ -293,6 +293,28 @@ class FusedDecodeWorkload(Workload):
         return super().kernels_per_step() - 1
 
 
+class FusedExtendWorkload(Workload):
+    """The extend step through pkv_paged_extend_attn_store: store_kv of the
+    chunk's tokens fused into the gather launch. Shares the device tensors of
+    an existing extend Workload."""
+
+    def __init__(self, base: Workload):  # noqa: super().__init__ would rebuild the inputs
+        self.__dict__.update(base.__dict__)
+
+    def store(self):
+        pass
+
+    def attention(self):
+        c, t = self.case, self.t
+        self.pkv.pkv_paged_extend_attn_store(self.pool, c.layer, self.q, self.k, self.v,
+                                             t["qo_indptr"], self.o, self.lse, t["page_table"],
+                                             t["seq_lens"], c.scale, self.hint, self.ws,
+                                             table_idx=t.get("table_idx"))
+
+    def kernels_per_step(self) -> int:
+        return 2  # gather (with the store), attention
+
+
 class CascadeWorkload(Workload):
     """The radix-shared case through pkv_paged_cascade_decode_attn: each
     group's prefix attended once (tensor cores), merged with every member's
@@ -572,11 +594,13 @@ def _extend_workload(args, dev, peaks, peak_src, flush, steps, warm):
     case = W.chunked_prefill_extend(args.seed)
     wl = Workload(case, dev)
     st, at = _measure(wl, steps, warm, flush)
+    _, ft = _measure(FusedExtendWorkload(wl), steps, warm, flush)
     fl = extend_flops(case)
     out["chunked-prefill-extend"] = {
         "metric": "extend attn TFLOP/s", "value": round(fl / (at * 1e-3) / 1e12, 2),
         "unit": "TFLOP/s", "ms_attention": round(at, 4), "ms_step_with_store": round(st, 4),
-        "flops": fl, "tokens_per_s": round(case.total_q / (st * 1e-3), 1),
+        "ms_step_fused_store": round(ft, 4),
+        "flops": fl, "tokens_per_s": round(case.total_q / (min(st, ft) * 1e-3), 1),
         "roofline": {**roofline("tensor", fl, at, peaks, peak_src),
                      "kernel": ("pkv_paged_extend_attn: extend_gather_kernel + extend_tc_kernel "
                                 "(both launches inside the timed duration)"),

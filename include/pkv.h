@@ -250,6 +250,33 @@ pkv_status pkv_paged_extend_attn(const pkv_pool *pool, int32_t layer, const void
                                  size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * One extend step with store_kv fused in ("Code Notes: mini-sglang", Engine
+ * Layer table, BaseKVCachePool row: the chunk's new K and V are written into
+ * the pool, then attention reads the pool). k_new, v_new: device bf16
+ * [total_q, Hkv, D], row t holding the new K / V of query token t
+ * (kv_row_stride elements between tokens, 16-byte aligned, stride >= Hkv*D
+ * and a multiple of 8). For each request r the rows qo_indptr[r] + j,
+ * j < c_r, are stored at key position p_r + j of its page_table row (the slot
+ * P * row[i/P] + i%P, i = p_r + j), and attention runs exactly as
+ * pkv_paged_extend_attn with the same arguments and workspace. Equivalent
+ * to pkv_kv_store with out_loc[qo_indptr[r] + j] = that slot followed by
+ * pkv_paged_extend_attn, provided no other request's row of the call holds
+ * those slots. A bad page id at a chunk position is flagged
+ * (PKV_DEVERR_PAGE_RANGE) and that token is not stored; a request whose
+ * qo_indptr pair is malformed (PKV_DEVERR_INDPTR) or whose seq_len is above
+ * the hint (PKV_DEVERR_SEQ_LEN_RANGE) stores nothing.
+ */
+pkv_status pkv_paged_extend_attn_store(const pkv_pool *pool, int32_t layer, const void *q,
+                                       const void *k_new, const void *v_new,
+                                       int64_t kv_row_stride, const int32_t *qo_indptr, void *o,
+                                       float *lse, const int32_t *page_table,
+                                       int64_t table_stride, const int32_t *table_idx,
+                                       const int32_t *seq_lens, int32_t batch, int32_t total_q,
+                                       int32_t num_q_heads, float scale,
+                                       int32_t max_seq_len_hint, void *workspace,
+                                       size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * Bytes of device workspace pkv_paged_cascade_decode_attn needs: the split
  * partial states of the suffix decode plus one slot per (request, q head)
  * for the shared-prefix state, then the gathered prefix K/V of num_groups

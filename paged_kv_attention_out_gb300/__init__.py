@@ -8,5 +8,5 @@ from .binding import (PkvError, pkv_cascade_workspace_size,  # noqa: F401
                       pkv_decode_workspace_size, pkv_extend_workspace_size, pkv_init,
                       pkv_kv_store, pkv_paged_cascade_decode_attn,
                       pkv_merge_lse, pkv_paged_decode_attn, pkv_paged_decode_attn_noalloc, pkv_paged_decode_attn_store,
-                      pkv_paged_extend_attn,
+                      pkv_paged_extend_attn, pkv_paged_extend_attn_store,
                       pkv_read_device_errors)

@@ -80,6 +80,11 @@ def load() -> ctypes.CDLL:
     L.pkv_paged_extend_attn.argtypes = [pool_p, _c_int32, _p, _p, _p, _p, _p, _c_int64, _p, _p,
                                         _c_int32, _c_int32, _c_int32, ctypes.c_float,
                                         _c_int32, _p, ctypes.c_size_t, _p]
+    L.pkv_paged_extend_attn_store.restype = ctypes.c_int
+    L.pkv_paged_extend_attn_store.argtypes = [pool_p, _c_int32, _p, _p, _p, _c_int64, _p, _p, _p,
+                                              _p, _c_int64, _p, _p, _c_int32, _c_int32,
+                                              _c_int32, ctypes.c_float, _c_int32, _p,
+                                              ctypes.c_size_t, _p]
     L.pkv_cascade_workspace_size.restype = ctypes.c_size_t
     L.pkv_cascade_workspace_size.argtypes = [_c_int32] * 7
     L.pkv_paged_cascade_decode_attn.restype = ctypes.c_int
@@ -289,6 +294,47 @@ def pkv_paged_extend_attn(pool, layer: int, q, qo_indptr, o, lse, page_table, se
         ctypes.byref(ps), int(layer), _ptr(q), _ptr(qo_indptr), _ptr(o), _ptr(lse),
         _ptr(page_table), page_table.shape[1], _ptr(table_idx), _ptr(seq_lens), B, T, Hq,
         float(scale), int(max_seq_len_hint), _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def pkv_paged_extend_attn_store(pool, layer: int, q, k_new, v_new, qo_indptr, o, lse,
+                                page_table, seq_lens, scale: float, max_seq_len_hint: int,
+                                workspace, table_idx=None, stream=None) -> None:
+    """Extend step with store_kv fused: k_new, v_new [T, Hkv, D] bf16 (row t = query
+    token t) go to the chunk's key positions of each row, then extend as
+    pkv_paged_extend_attn."""
+    ps = pool_struct(pool)
+    _want(q, torch.bfloat16, "q", 3)
+    _want(o, torch.bfloat16, "o", 3)
+    _contig(q, "q")
+    _contig(o, "o")
+    for t, name in ((k_new, "k_new"), (v_new, "v_new")):
+        _want(t, torch.bfloat16, name, 3)
+    if k_new.stride(0) != v_new.stride(0) or k_new.stride(1) != k_new.shape[2] \
+            or k_new.stride(2) != 1 or v_new.stride(1) != v_new.shape[2] or v_new.stride(2) != 1:
+        raise ValueError("k_new and v_new rows must share a row stride with heads/dims contiguous")
+    _want(qo_indptr, torch.int32, "qo_indptr", 1)
+    _want(page_table, torch.int32, "page_table", 2)
+    _contig(page_table, "page_table")
+    _want(seq_lens, torch.int32, "seq_lens", 1)
+    T, Hq, D = q.shape
+    B = seq_lens.shape[0]
+    if o.shape != q.shape or qo_indptr.shape[0] != B + 1:
+        raise ValueError("o must match q and qo_indptr must have batch+1 entries")
+    if k_new.shape[0] != T or v_new.shape[0] != T:
+        raise ValueError("k_new and v_new must have total_q rows")
+    if lse is not None:
+        _want(lse, torch.float32, "lse", 2)
+        _contig(lse, "lse")
+    if table_idx is not None:
+        _want(table_idx, torch.int32, "table_idx", 1)
+    if workspace is not None:
+        _contig(workspace, "workspace")
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load().pkv_paged_extend_attn_store(
+        ctypes.byref(ps), int(layer), _ptr(q), _ptr(k_new), _ptr(v_new), k_new.stride(0),
+        _ptr(qo_indptr), _ptr(o), _ptr(lse), _ptr(page_table), page_table.shape[1],
+        _ptr(table_idx), _ptr(seq_lens), B, T, Hq, float(scale), int(max_seq_len_hint),
+        _ptr(workspace), ws_bytes, _stream(stream)))
 
 
 def pkv_cascade_workspace_size(batch: int, num_q_heads: int, num_kv_heads: int, head_dim: int,

@@ -118,6 +118,13 @@ struct GatherArgs {
   int32_t tokens_per_tile;
   int32_t causal;  // 0: every query of request r sees all seq_lens[r] keys
   int32_t *plan;
+  // Fused store (k_new != nullptr): the chunk's keys p_r .. seq_r - 1 are
+  // taken from rows qo_indptr[r] .. of k_new / v_new and also written into
+  // the pool at their page-table slots.
+  const __nv_bfloat16 *k_new;
+  const __nv_bfloat16 *v_new;
+  int64_t kv_row_stride;
+  __nv_bfloat16 *pool_w;
 };
 
 struct ExtendArgs {
@@ -303,6 +310,18 @@ __global__ void __launch_bounds__(kGatherThreads)
     return;
   }
   const int32_t *row_pages = a.page_table + static_cast<int64_t>(row) * a.table_stride;
+  // Fused store: keys from new_key0 on are the chunk's, key k is row
+  // new_row0 + k of k_new / v_new. A malformed qo_indptr pair (flagged by the
+  // planner) stores nothing and reads the pool as the unfused call would.
+  int new_key0 = seq;
+  int64_t new_row0 = 0;
+  if (a.k_new) {
+    const int beg = a.qo_indptr[r], end = a.qo_indptr[r + 1];
+    if (beg >= 0 && end >= beg && end <= a.total_q && end - beg <= seq) {
+      new_key0 = seq - (end - beg);
+      new_row0 = static_cast<int64_t>(beg) - new_key0;
+    }
+  }
   // One warp per key: its K row and V row (Hkv * D contiguous elements each
   // in the pool); 16-byte chunk `ch` of a row goes to kv head ch / (D / 8)'s run.
   constexpr int kChunks = D / 8;  // 16-byte chunks per head row
@@ -317,15 +336,25 @@ __global__ void __launch_bounds__(kGatherThreads)
     const int key = key0 + kk;
     // the key's K row (c = 0) and V row (c = 1) are copied together
     const uint4 *src[2] = {nullptr, nullptr};
+    uint4 *store[2] = {nullptr, nullptr};  // fused store: the key's pool rows
     if (key < seq) {
       const int pidx = key / a.page_size;
       const int ent = __ldg(row_pages + pidx);
       const int64_t slot = static_cast<int64_t>(ent) * a.page_size + (key - pidx * a.page_size);
-      if (ent >= 0 && slot < a.slots) {
+      const bool slot_ok = ent >= 0 && slot < a.slots;
+      if (key >= new_key0) {
+        const int64_t nrow = (new_row0 + key) * a.kv_row_stride;
+        src[0] = reinterpret_cast<const uint4 *>(a.k_new + nrow);
+        src[1] = reinterpret_cast<const uint4 *>(a.v_new + nrow);
+      }
+      if (slot_ok) {
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           const int64_t prow = (static_cast<int64_t>(c) * a.num_layers + a.layer) * a.slots + slot;
-          src[c] = reinterpret_cast<const uint4 *>(a.pool + prow * row_elems);
+          if (key >= new_key0)
+            store[c] = reinterpret_cast<uint4 *>(a.pool_w + prow * row_elems);
+          else
+            src[c] = reinterpret_cast<const uint4 *>(a.pool + prow * row_elems);
         }
       } else if (lane == 0) {
         flag_error(a.err, kErrPage);
@@ -347,9 +376,11 @@ __global__ void __launch_bounds__(kGatherThreads)
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
           const int ch = ch0 + 32 * u;
-          if (ch < nch)
+          if (ch < nch) {
             *reinterpret_cast<uint4 *>(dst + (ch / kChunks) * run_elems + (ch % kChunks) * 8) =
                 v[c][u];
+            if (store[c] != nullptr) store[c][ch] = v[c][u];
+          }
         }
       }
     }
@@ -865,6 +896,10 @@ cudaError_t launch_extend(const PoolGeom &g, int32_t layer, const void *q,
   ga.total_q = total_q;
   ga.tokens_per_tile = kM / (hq / g.hkv);
   ga.causal = mode.causal;
+  ga.k_new = static_cast<const __nv_bfloat16 *>(mode.k_new);
+  ga.v_new = static_cast<const __nv_bfloat16 *>(mode.v_new);
+  ga.kv_row_stride = mode.kv_row_stride;
+  ga.pool_w = static_cast<__nv_bfloat16 *>(const_cast<void *>(g.base));
   ga.plan = reinterpret_cast<int32_t *>(
       static_cast<uint8_t *>(workspace) +
       ((extend_kv_bytes(batch, g.hkv, g.d, capacity) + 255) & ~uint64_t(255)));

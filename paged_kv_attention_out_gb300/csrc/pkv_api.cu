@@ -401,13 +401,15 @@ size_t pkv_extend_workspace_size(int32_t batch, int32_t num_kv_heads, int32_t he
   return pkv::extend_workspace_bytes(batch, num_kv_heads, head_dim, max_seq_len_hint);
 }
 
-pkv_status pkv_paged_extend_attn(const pkv_pool *pool, int32_t layer, const void *q,
-                                 const int32_t *qo_indptr, void *o, float *lse,
-                                 const int32_t *page_table, int64_t table_stride,
-                                 const int32_t *table_idx, const int32_t *seq_lens,
-                                 int32_t batch, int32_t total_q, int32_t num_q_heads,
-                                 float scale, int32_t max_seq_len_hint, void *workspace,
-                                 size_t workspace_bytes, cudaStream_t stream) {
+// Extend with (k_new != NULL) or without the fused store of the chunk's K/V.
+static pkv_status extend_call(const pkv_pool *pool, int32_t layer, const void *q,
+                              const void *k_new, const void *v_new, int64_t kv_row_stride,
+                              const int32_t *qo_indptr, void *o, float *lse,
+                              const int32_t *page_table, int64_t table_stride,
+                              const int32_t *table_idx, const int32_t *seq_lens, int32_t batch,
+                              int32_t total_q, int32_t num_q_heads, float scale,
+                              int32_t max_seq_len_hint, void *workspace, size_t workspace_bytes,
+                              cudaStream_t stream) {
   pkv::PoolGeom g;
   pkv_status s = check_pool(pool, layer, &g);
   if (s != PKV_OK) return s;
@@ -448,11 +450,51 @@ pkv_status pkv_paged_extend_attn(const pkv_pool *pool, int32_t layer, const void
     return fail(PKV_ERR_UNSUPPORTED, "extend: too many query tiles in one call");
   DevInfo *d = nullptr;
   if ((s = device_info(&d)) != PKV_OK) return s;
+  pkv::ExtendMode mode;
+  mode.k_new = k_new;
+  mode.v_new = v_new;
+  mode.kv_row_stride = kv_row_stride;
   cudaError_t e = pkv::launch_extend(g, layer, q, qo_indptr, o, lse, page_table, table_stride,
                                      table_idx, seq_lens, batch, total_q, num_q_heads, scale,
                                      static_cast<int32_t>(cap), workspace, d->sm_count, d->err,
-                                     stream);
+                                     stream, mode);
   return e == cudaSuccess ? PKV_OK : cuda_fail(e, "extend launch");
+}
+
+pkv_status pkv_paged_extend_attn(const pkv_pool *pool, int32_t layer, const void *q,
+                                 const int32_t *qo_indptr, void *o, float *lse,
+                                 const int32_t *page_table, int64_t table_stride,
+                                 const int32_t *table_idx, const int32_t *seq_lens,
+                                 int32_t batch, int32_t total_q, int32_t num_q_heads,
+                                 float scale, int32_t max_seq_len_hint, void *workspace,
+                                 size_t workspace_bytes, cudaStream_t stream) {
+  return extend_call(pool, layer, q, nullptr, nullptr, 0, qo_indptr, o, lse, page_table,
+                     table_stride, table_idx, seq_lens, batch, total_q, num_q_heads, scale,
+                     max_seq_len_hint, workspace, workspace_bytes, stream);
+}
+
+pkv_status pkv_paged_extend_attn_store(const pkv_pool *pool, int32_t layer, const void *q,
+                                       const void *k_new, const void *v_new,
+                                       int64_t kv_row_stride, const int32_t *qo_indptr, void *o,
+                                       float *lse, const int32_t *page_table,
+                                       int64_t table_stride, const int32_t *table_idx,
+                                       const int32_t *seq_lens, int32_t batch, int32_t total_q,
+                                       int32_t num_q_heads, float scale,
+                                       int32_t max_seq_len_hint, void *workspace,
+                                       size_t workspace_bytes, cudaStream_t stream) {
+  if (batch > 0 && total_q > 0) {
+    if (!k_new || !v_new) return fail(PKV_ERR_INVALID_ARG, "k_new and v_new must be non-NULL");
+    if (!aligned(k_new, 16) || !aligned(v_new, 16))
+      return fail(PKV_ERR_INVALID_ARG, "k_new and v_new must be 16-byte aligned");
+    if (pool && (kv_row_stride < static_cast<int64_t>(pool->num_kv_heads) * pool->head_dim ||
+                 kv_row_stride % 8 != 0))
+      return fail(PKV_ERR_INVALID_ARG, "kv_row_stride %lld must be >= Hkv*D and a multiple of 8",
+                  static_cast<long long>(kv_row_stride));
+  }
+  return extend_call(pool, layer, q, batch > 0 && total_q > 0 ? k_new : nullptr, v_new,
+                     kv_row_stride, qo_indptr, o, lse, page_table, table_stride, table_idx,
+                     seq_lens, batch, total_q, num_q_heads, scale, max_seq_len_hint, workspace,
+                     workspace_bytes, stream);
 }
 
 pkv_status pkv_merge_lse(const float *o_a, const float *lse_a, const float *o_b,

@@ -77,6 +77,11 @@ struct ExtendMode {
   int32_t pstride = 0;
   int32_t pslot = 0;
   int32_t key_splits = 1;  // non-causal: key ranges per block (slots pslot .. + key_splits - 1)
+  // causal only: store_kv fused into the gather (chunk rows of k_new / v_new,
+  // kv_row_stride elements apart, written into the pool at their slots)
+  const void *k_new = nullptr;
+  const void *v_new = nullptr;
+  int64_t kv_row_stride = 0;
 };
 
 // Gathered-K/V workspace of the extend call: [2][batch][hkv][s_pad][d] bf16,

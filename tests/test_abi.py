@@ -98,6 +98,16 @@ def test_bad_host_arguments_are_rejected_before_any_gpu_work(lib):
                                            16, 4, None, 16, 1, 4, f, 4, None, 0, None) == 1
     assert lib.pkv_paged_decode_attn_store(ctypes.byref(pool), 0, 16, 16, 16, 128, 16, None,
                                            16, 4, None, 16, 1, 4, f, 4, None, 0, None) == 1
+    # fused store + extend: the same refusals
+    assert lib.pkv_paged_extend_attn_store(ctypes.byref(pool), 0, 16, None, 16, 256, 16, 16,
+                                           None, 16, 4, None, 16, 1, 8, 4, f, 8, None, 0,
+                                           None) == 1
+    assert lib.pkv_paged_extend_attn_store(ctypes.byref(pool), 0, 16, 16, 34, 256, 16, 16,
+                                           None, 16, 4, None, 16, 1, 8, 4, f, 8, None, 0,
+                                           None) == 1
+    assert lib.pkv_paged_extend_attn_store(ctypes.byref(pool), 0, 16, 16, 16, 100, 16, 16,
+                                           None, 16, 4, None, 16, 1, 8, 4, f, 8, None, 0,
+                                           None) == 1
     # cascade: group above 8; every request must be in a group; NULL member lists
     assert lib.pkv_paged_cascade_decode_attn(
         ctypes.byref(pool), 0, 16, 16, None, 16, 4, 16, 16, 16, 1, 16, 4, None, 16, 1, 32, f,

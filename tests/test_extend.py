@@ -48,6 +48,15 @@ def test_extend_shared_prefix():
     check_against_oracle(case)
 
 
+def test_mixed_prefill_and_decode_batch():
+    """One extend call over a batch mixing prefill chunks with decode requests
+    (chunk of one token after a long cached prefix): a decode row of an extend
+    call is the decode of that request."""
+    case = W.random_case(55, kind="extend", seq_lens=[513, 1, 2000, 37, 900, 4096, 2, 130],
+                         chunk_lens=[1, 1, 300, 1, 128, 1, 2, 129], Hq=32, Hkv=8, D=128, P=16)
+    check_against_oracle(case)
+
+
 def test_chunked_prefill_full_size_sampled():
     case = W.chunked_prefill_extend(0)
     o, lse, _ = gpu_run(case)
