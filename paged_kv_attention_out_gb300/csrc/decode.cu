@@ -413,7 +413,12 @@ __global__ void __launch_bounds__(kThreads, (kStages <= 3 ? 2 : 1)) decode_kerne
 
 // Cross-split merge: one warp per (request, q head) with more than one
 // split; with a cascade's shared-prefix states in slots splits .. pstride - 1,
-// every (request, q head) merges its suffix splits with those.
+// every (request, q head) merges its suffix splits with those. Lane s holds
+// the lse of state s; the partial rows of up to kMergeBatch states are
+// loaded together with the lse values, so the common case costs one
+// round trip to L2 after the decode grid completes.
+constexpr int kMergeBatch = 16;
+
 template <int D>
 __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs a, int32_t batch) {
   const int warp = threadIdx.x >> 5;
@@ -421,48 +426,74 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs a, i
   const int64_t bh = static_cast<int64_t>(blockIdx.x) * 4 + warp;
   if (bh >= static_cast<int64_t>(batch) * a.hq) return;
   const int b = static_cast<int>(bh / a.hq);
-  grid_dependency_wait();  // the partial states come from decode_kernel
+  // seq_lens and table_idx are inputs of the call (complete before any
+  // decode CTA passed its own dependency wait), so they are read before ours.
   const RowInfo ri = row_info(a, b, false);
   const int n = ri.nsplit;
   if (n <= 1 && !a.force_partial) return;
   // suffix splits in slots 0 .. n - 1, shared-prefix states (cascade) in
-  // slots splits .. pstride - 1
-  const int extra = a.pstride - a.splits;
+  // slots splits .. pstride - 1: state s < n is slot s, state n + e is slot
+  // splits + e
+  const int total = n + (a.pstride - a.splits);
   const float *pl = a.part_lse + bh * a.pstride;
-  const float *pe = pl + a.splits;
-  float M = -INFINITY;
-  for (int s = lane; s < n; s += 32) M = fmaxf(M, pl[s]);
-  for (int s = lane; s < extra; s += 32) M = fmaxf(M, pe[s]);
+  const float *po = a.part_o + bh * a.pstride * D + lane * 4;
+  auto slot = [&](int st) { return st < n ? st : a.splits + (st - n); };
+  grid_dependency_wait();  // the partial states come from decode_kernel
+  const bool row_lane = lane < D / 4;
+  float4 v[kMergeBatch];
+#pragma unroll
+  for (int u = 0; u < kMergeBatch; ++u)
+    v[u] = (row_lane && u < total)
+               ? *reinterpret_cast<const float4 *>(po + static_cast<int64_t>(slot(u)) * D)
+               : make_float4(0.f, 0.f, 0.f, 0.f);
+  float lse_l = lane < total ? pl[slot(lane)] : -INFINITY;
+  float M = lse_l;
+  for (int s = lane + 32; s < total; s += 32) M = fmaxf(M, pl[slot(s)]);
 #pragma unroll
   for (int x = 16; x > 0; x >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, x));
   const float ref = M == -INFINITY ? 0.f : M;
-  float L = 0.f;
-  for (int s = lane; s < n; s += 32) L += expf(pl[s] - ref);
-  for (int s = lane; s < extra; s += 32) L += expf(pe[s] - ref);
+  const float e_l = lane < total ? expf(lse_l - ref) : 0.f;
+  float L = e_l;
+  for (int s = lane + 32; s < total; s += 32) L += expf(pl[slot(s)] - ref);
 #pragma unroll
   for (int x = 16; x > 0; x >>= 1) L += __shfl_xor_sync(0xffffffffu, L, x);
   const float inv = L > 0.f ? 1.f / L : 0.f;
-  if (lane < D / 4) {
-    float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
-    const float *po = a.part_o + bh * a.pstride * D + lane * 4;
-#pragma unroll 4
-    for (int s = 0; s < n; ++s) {
-      const float w = expf(pl[s] - ref) * inv;
-      const float4 v = *reinterpret_cast<const float4 *>(po + static_cast<int64_t>(s) * D);
-      O.x += w * v.x;
-      O.y += w * v.y;
-      O.z += w * v.z;
-      O.w += w * v.w;
+  float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+  for (int u = 0; u < kMergeBatch; ++u) {
+    const float w = __shfl_sync(0xffffffffu, e_l, u) * inv;
+    O.x += w * v[u].x;
+    O.y += w * v[u].y;
+    O.z += w * v[u].z;
+    O.w += w * v[u].w;
+  }
+  // Beyond the first batch (long rows, cascade prefix states): batches of
+  // eight rows, all loads of a batch issued before their weights are used.
+  for (int s0 = kMergeBatch; s0 < total; s0 += 8) {
+    float4 x[8];
+    float w[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int st = s0 + u;
+      const bool in = st < total;
+      x[u] = (row_lane && in)
+                 ? *reinterpret_cast<const float4 *>(po + static_cast<int64_t>(slot(st)) * D)
+                 : make_float4(0.f, 0.f, 0.f, 0.f);
+      w[u] = in && st >= 32 ? pl[slot(st)] : 0.f;
     }
-    for (int s = 0; s < extra; ++s) {
-      const float w = expf(pe[s] - ref) * inv;
-      const float4 v =
-          *reinterpret_cast<const float4 *>(po + static_cast<int64_t>(a.splits + s) * D);
-      O.x += w * v.x;
-      O.y += w * v.y;
-      O.z += w * v.z;
-      O.w += w * v.w;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int st = s0 + u;
+      const float e = st < 32 ? __shfl_sync(0xffffffffu, e_l, st & 31)
+                              : (st < total ? expf(w[u] - ref) : 0.f);
+      const float wt = e * inv;
+      O.x += wt * x[u].x;
+      O.y += wt * x[u].y;
+      O.z += wt * x[u].z;
+      O.w += wt * x[u].w;
     }
+  }
+  if (row_lane) {
     uint2 packed;
     packed.x = pack_bf16(O.x, O.y);
     packed.y = pack_bf16(O.z, O.w);
