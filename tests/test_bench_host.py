@@ -80,3 +80,20 @@ def test_reference_arm_other_ranks_exit_quietly():
                         "--warmup", "3"], cwd=ROOT, capture_output=True, text=True,
                        timeout=300, env=env)
     assert r.returncode == 0 and r.stdout.strip() == ""
+
+
+def test_e2e_staging_buffer_round_trips_every_tensor(monkeypatch):
+    """The e2e step moves its inputs in one copy: every tensor's view of the
+    staging buffer holds exactly its bytes, at a 256-byte aligned offset."""
+    import torch
+    import bench
+    monkeypatch.setattr(torch.Tensor, "pin_memory", lambda self: self)  # no CUDA here
+    x = {"q": torch.randn(3, 4, 8).to(torch.bfloat16), "t": torch.arange(11, dtype=torch.int32),
+         "l": torch.randn(5, 3)}
+    host, dev, views = bench._staging(x, "cpu")
+    assert host.numel() == 256 * 3
+    dev.copy_(host)
+    for name, t in x.items():
+        assert views[name].dtype == t.dtype and views[name].shape == t.shape
+        assert torch.equal(views[name], t)
+        assert (views[name].data_ptr() - dev.data_ptr()) % 256 == 0
