@@ -56,8 +56,8 @@ MEASURED_TRAFFIC = {
                "bytes": 628162048},
     # profiles/extend_kernels_chunked-prefill-extend.md: extend_gather_kernel + extend_tc_kernel
     "extend": {"sources": ["extend.cu", "tc_common.cuh", "pkv_common.cuh"],
-               "sha256": "f0f47d24aedf8eddc2c5e6f19f65c867787df5a88813101df53ca606bca703a6",
-               "bytes": 521340928},
+               "sha256": "dbb711343cbffa5bad87e73ecf90b32cdd63fe411c57ea4454f68b4fc3953887",
+               "bytes": 528233728},
 }
 
 

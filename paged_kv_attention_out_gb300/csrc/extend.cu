@@ -286,7 +286,9 @@ __device__ void plan_blocks(const GatherArgs &a) {
   if (tid == 0) a.plan[0] = nblk;
 }
 
-template <int D>
+// kStore: the fused store (a.k_new != nullptr), a separate instantiation so
+// the plain gather keeps its lean inner loop.
+template <int D, bool kStore>
 __global__ void __launch_bounds__(kGatherThreads)
     extend_gather_kernel(const GatherArgs a) {
   grid_dependency_wait();  // the chunk's K/V may come from the previous kernel (store_kv)
@@ -315,7 +317,7 @@ __global__ void __launch_bounds__(kGatherThreads)
   // planner) stores nothing and reads the pool as the unfused call would.
   int new_key0 = seq;
   int64_t new_row0 = 0;
-  if (a.k_new) {
+  if (kStore) {
     const int beg = a.qo_indptr[r], end = a.qo_indptr[r + 1];
     if (beg >= 0 && end >= beg && end <= a.total_q && end - beg <= seq) {
       new_key0 = seq - (end - beg);
@@ -342,7 +344,7 @@ __global__ void __launch_bounds__(kGatherThreads)
       const int ent = __ldg(row_pages + pidx);
       const int64_t slot = static_cast<int64_t>(ent) * a.page_size + (key - pidx * a.page_size);
       const bool slot_ok = ent >= 0 && slot < a.slots;
-      if (key >= new_key0) {
+      if (kStore && key >= new_key0) {
         const int64_t nrow = (new_row0 + key) * a.kv_row_stride;
         src[0] = reinterpret_cast<const uint4 *>(a.k_new + nrow);
         src[1] = reinterpret_cast<const uint4 *>(a.v_new + nrow);
@@ -351,7 +353,7 @@ __global__ void __launch_bounds__(kGatherThreads)
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           const int64_t prow = (static_cast<int64_t>(c) * a.num_layers + a.layer) * a.slots + slot;
-          if (key >= new_key0)
+          if (kStore && key >= new_key0)
             store[c] = reinterpret_cast<uint4 *>(a.pool_w + prow * row_elems);
           else
             src[c] = reinterpret_cast<const uint4 *>(a.pool + prow * row_elems);
@@ -379,7 +381,7 @@ __global__ void __launch_bounds__(kGatherThreads)
           if (ch < nch) {
             *reinterpret_cast<uint4 *>(dst + (ch / kChunks) * run_elems + (ch % kChunks) * 8) =
                 v[c][u];
-            if (store[c] != nullptr) store[c][ch] = v[c][u];
+            if (kStore && store[c] != nullptr) store[c][ch] = v[c][u];
           }
         }
       }
@@ -941,7 +943,10 @@ cudaError_t launch_extend(const PoolGeom &g, int32_t layer, const void *q,
                    static_cast<unsigned>(mode.causal ? 1 : mode.key_splits));
   cudaError_t e;
   if (g.d == 128) {
-    e = launch_pdl(extend_gather_kernel<128>, ggrid, dim3(kGatherThreads), 0, stream, ga);
+    e = ga.k_new ? launch_pdl(extend_gather_kernel<128, true>, ggrid, dim3(kGatherThreads), 0,
+                              stream, ga)
+                 : launch_pdl(extend_gather_kernel<128, false>, ggrid, dim3(kGatherThreads), 0,
+                              stream, ga);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(extend_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              Smem<128>::kTotal);
@@ -949,7 +954,10 @@ cudaError_t launch_extend(const PoolGeom &g, int32_t layer, const void *q,
     e = launch_pdl(extend_tc_kernel<128>, grid, dim3(kThreads), Smem<128>::kTotal, stream,
                    kv_map, q_map, a);
   } else {
-    e = launch_pdl(extend_gather_kernel<64>, ggrid, dim3(kGatherThreads), 0, stream, ga);
+    e = ga.k_new ? launch_pdl(extend_gather_kernel<64, true>, ggrid, dim3(kGatherThreads), 0,
+                              stream, ga)
+                 : launch_pdl(extend_gather_kernel<64, false>, ggrid, dim3(kGatherThreads), 0,
+                              stream, ga);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(extend_tc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              Smem<64>::kTotal);
