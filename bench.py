@@ -9,7 +9,9 @@ split-KV decode attention through the page table, and the cross-split
 log-sum-exp merge. `value` is decode
 attention KV throughput in GB/s (algorithmic bytes: every K/V byte of every
 key, the page-table entries, q and o) over whole-step device time, inputs
-resident in HBM, L2 flushed between steps. The other named workloads
+resident in HBM, L2 flushed between steps (a 320 MB write, then a 256 MB
+read, so no input line is in L2 and the flush's own dirty lines are not
+written back inside the timed region). The other named workloads
 (chunked-prefill extend in TFLOP/s, long-context and radix-shared decode in
 GB/s, the tiny decode in microseconds) are measured in the same run and
 reported under "workloads".
@@ -43,6 +45,7 @@ sys.path.insert(0, ROOT)
 from paged_kv_attention_out_gb300 import workloads as W  # noqa: E402
 
 L2_FLUSH_BYTES = 320 << 20  # > 2x the 129 MB L2
+L2_CLEAN_BYTES = 256 << 20  # read after the flush write (see L2Flush)
 CSRC = os.path.join(ROOT, "paged_kv_attention_out_gb300", "csrc")
 
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per call, summed
@@ -343,17 +346,37 @@ class CascadeWorkload(Workload):
         return 5  # store, suffix decode, prefix gather, prefix attention, merge
 
 
-def time_steps(wl: Workload, steps: int, warmup: int, flush: torch.Tensor):
+class L2Flush:
+    """Between timed steps: write a buffer larger than L2 (no input line
+    survives), then read another buffer larger than L2, so the write's own
+    dirty lines are written back before the timed region instead of inside
+    it; a step then starts with L2 holding clean, unrelated lines (as after
+    the weight-reading GEMMs of a model layer). write_only=True keeps the
+    plain write flush, reported beside it for comparison."""
+
+    def __init__(self, dev, write_only: bool = False):
+        self.w = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+        self.r = None if write_only else torch.ones(L2_CLEAN_BYTES // 4, dtype=torch.float32,
+                                                    device=dev)
+        self.acc = torch.zeros((), dtype=torch.float32, device=dev)
+
+    def __call__(self):
+        self.w.zero_()
+        if self.r is not None:
+            torch.sum(self.r, dim=(0,), out=self.acc)
+
+
+def time_steps(wl: Workload, steps: int, warmup: int, flush: L2Flush):
     """Per-step CUDA-event times (ms) of store + attention, and of attention alone."""
     stream = torch.cuda.current_stream()
     for _ in range(warmup):
-        flush.zero_()
+        flush()
         wl.store()
         wl.attention()
     torch.cuda.synchronize()
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
     for i in range(steps):
-        flush.zero_()
+        flush()
         ev[i][0].record(stream)
         wl.store()
         ev[i][1].record(stream)
@@ -384,7 +407,7 @@ def _staging(tensors: dict, device):
     return host, devb, views
 
 
-def time_e2e(wl: Workload, steps: int, warmup: int, flush: torch.Tensor):
+def time_e2e(wl: Workload, steps: int, warmup: int, flush: L2Flush):
     """Same step through the public API from pinned host memory: H2D of the
     step's inputs (q, new k/v, out_loc, page_table, seq_lens), the calls, and
     D2H of the result (o, lse), all inside the timed region. The inputs sit
@@ -409,12 +432,12 @@ def time_e2e(wl: Workload, steps: int, warmup: int, flush: torch.Tensor):
         out_h.copy_(out_d, non_blocking=True)
 
     for _ in range(warmup):
-        flush.zero_()
+        flush()
         one()
     torch.cuda.synchronize()
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
     for i in range(steps):
-        flush.zero_()
+        flush()
         ev[i][0].record(stream)
         one()
         ev[i][1].record(stream)
@@ -477,7 +500,7 @@ def run_pkv(args):
     import paged_kv_attention_out_gb300 as pkv
     pkv.pkv_init()
     peaks, peak_src = load_peaks()
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flush = L2Flush(dev)
     if args.only not in (None, "llama3-8b-decode"):
         # one named workload alone (used for profiling): prints its JSON object
         if rank == 0:
@@ -512,6 +535,10 @@ def run_pkv(args):
     max_ms, all_units = aggregate_ranks(total_ms, units * args.steps, world)
     value = all_units / (max_ms * 1e-3) / 1e9
     e2e_ms, h2d, d2h = time_e2e(wl, max(3, min(args.steps, 200)), args.warmup, flush)
+    # the same step after the plain write flush (its dirty lines written back
+    # inside the timed region), for comparison
+    wo_ms, _ = time_steps(wl, max(3, min(args.steps, 200)), args.warmup,
+                          L2Flush(dev, write_only=True))
     e2e_value = units / (statistics.mean(e2e_ms) * 1e-3) / 1e9
     kernels = wl.kernels_per_step()
     sep_attn = statistics.mean(sep_attn_ms)
@@ -565,7 +592,9 @@ def run_pkv(args):
                    "pool": f"{case.NP} slots x {case.L} layers", "seed": args.seed,
                    "step": ("kv_store fused into split-KV decode (pkv_paged_decode_attn_store) "
                             "+ split merge"),
-                   "algorithmic_bytes_per_step": units, "l2": "flushed between steps",
+                   "algorithmic_bytes_per_step": units,
+                   "l2": ("flushed between steps: a 320 MB write, then a 256 MB read so the "
+                          "write's dirty lines are written back before the timed region"),
                    "parallelism": f"replicas x{world}"},
         "roofline": main["roofline"],
         "cpu_baseline": cpu,
@@ -577,7 +606,10 @@ def run_pkv(args):
         "detail": {"fused_step_ms": main["fused_step_ms"],
                    "unfused_step_ms": main["unfused_step_ms"],
                    "decode_call_ms": main["attn_ms"], "kv_store_ms": main["store_ms"],
-                   "kernels_per_step": kernels},
+                   "kernels_per_step": kernels,
+                   "fused_step_ms_write_only_flush": round(statistics.mean(wo_ms), 5),
+                   "value_write_only_flush": round(units / (statistics.mean(wo_ms) * 1e-3) / 1e9,
+                                                   2)},
         "workloads": workloads,
     }
     print(json.dumps(line), flush=True)
