@@ -313,11 +313,9 @@ size_t pkv_cascade_workspace_size(int32_t batch, int32_t num_q_heads, int32_t nu
  * computed and PKV_DEVERR_SEQ_LEN_RANGE is flagged. max_suffix_len_hint
  * sizes the suffix split plan as max_seq_len_hint does for decode. workspace:
  * device, 256-byte aligned, at least pkv_cascade_workspace_size(...) bytes
- * (with the same effective prefix bound). The shared-prefix kernels run on
- * a library-owned second stream forked from `stream` (event record / wait)
- * and joined back before the merge, so they overlap the suffix decode; the
- * first cascade call on a device creates that stream and its two events
- * (make it before any stream capture). Still asynchronous on `stream`.
+ * (with the same effective prefix bound). Every kernel runs on `stream`
+ * (the shared-prefix gather is launched so that it can run beside the
+ * suffix decode's last CTAs).
  */
 pkv_status pkv_paged_cascade_decode_attn(
     const pkv_pool *pool, int32_t layer, const void *q, void *o, float *lse,

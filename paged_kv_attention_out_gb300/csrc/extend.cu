@@ -125,6 +125,10 @@ struct GatherArgs {
   const __nv_bfloat16 *v_new;
   int64_t kv_row_stride;
   __nv_bfloat16 *pool_w;
+  // Nothing read here comes from the previous kernel on the stream (the
+  // cascade's suffix decode): wait for it only at exit, so this grid runs
+  // beside its tail and still completes after it.
+  int32_t defer_wait;
 };
 
 struct ExtendArgs {
@@ -289,10 +293,20 @@ __device__ void plan_blocks(const GatherArgs &a) {
 // kStore: the fused store (a.k_new != nullptr), a separate instantiation so
 // the plain gather keeps its lean inner loop.
 template <int D, bool kStore>
+__device__ __forceinline__ void gather_body(const GatherArgs &a);
+
+template <int D, bool kStore>
 __global__ void __launch_bounds__(kGatherThreads)
     extend_gather_kernel(const GatherArgs a) {
-  grid_dependency_wait();  // the chunk's K/V may come from the previous kernel (store_kv)
+  // the chunk's K/V may come from the previous kernel (store_kv)
+  if (!a.defer_wait) grid_dependency_wait();
   grid_dependents_launch();
+  gather_body<D, kStore>(a);
+  if (a.defer_wait) grid_dependency_wait();
+}
+
+template <int D, bool kStore>
+__device__ __forceinline__ void gather_body(const GatherArgs &a) {
   if (static_cast<int>(blockIdx.y) == a.batch) {  // the extra row: one planner CTA
     if (blockIdx.x == 0) plan_blocks(a);
     return;
@@ -901,6 +915,7 @@ cudaError_t launch_extend(const PoolGeom &g, int32_t layer, const void *q,
   ga.k_new = static_cast<const __nv_bfloat16 *>(mode.k_new);
   ga.v_new = static_cast<const __nv_bfloat16 *>(mode.v_new);
   ga.kv_row_stride = mode.kv_row_stride;
+  ga.defer_wait = mode.overlap_previous;
   ga.pool_w = static_cast<__nv_bfloat16 *>(const_cast<void *>(g.base));
   ga.plan = reinterpret_cast<int32_t *>(
       static_cast<uint8_t *>(workspace) +

@@ -24,11 +24,6 @@ struct DevInfo {
   pkv_status status = PKV_OK;
   int sm_count = 0;
   unsigned *err = nullptr;
-  // cascade decode: a second stream for the shared-prefix kernels and the
-  // fork / join events (created by the first cascade call on the device)
-  cudaStream_t aux = nullptr;
-  cudaEvent_t fork = nullptr, join = nullptr;
-  std::mutex cascade_mu;  // one fork / join sequence at a time on these
 };
 
 constexpr int kMaxDevices = 64;
@@ -276,20 +271,6 @@ size_t pkv_cascade_workspace_size(int32_t batch, int32_t num_q_heads, int32_t nu
          pkv::extend_workspace_bytes(num_groups, num_kv_heads, head_dim, max_prefix_len_hint);
 }
 
-// The cascade's second stream and events for the current device (DevInfo d).
-pkv_status cascade_streams(DevInfo *d) {
-  std::lock_guard<std::mutex> lock(g_mu);
-  if (d->aux) return PKV_OK;
-  cudaError_t e = cudaStreamCreateWithFlags(&d->aux, cudaStreamNonBlocking);
-  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&d->fork, cudaEventDisableTiming);
-  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&d->join, cudaEventDisableTiming);
-  if (e != cudaSuccess) {
-    d->aux = nullptr;
-    return cuda_fail(e, "cascade stream / event creation");
-  }
-  return PKV_OK;
-}
-
 pkv_status pkv_paged_cascade_decode_attn(
     const pkv_pool *pool, int32_t layer, const void *q, void *o, float *lse,
     const int32_t *prefix_page_table, int64_t prefix_table_stride, const int32_t *prefix_lens,
@@ -354,23 +335,18 @@ pkv_status pkv_paged_cascade_decode_attn(
     return fail(PKV_ERR_WORKSPACE_TOO_SMALL, "workspace %zu bytes, %zu needed", workspace_bytes,
                 need);
   if (!aligned(workspace, 256)) return fail(PKV_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
-  if ((s = cascade_streams(d)) != PKV_OK) return s;
-  // The shared-prefix attention (gather + tensor-core kernel) runs on a
-  // second stream, forked from and joined back into `stream`, concurrently
-  // with the suffix decode: one is compute-bound, the other HBM-bound.
-  std::lock_guard<std::mutex> lock(d->cascade_mu);
-  cudaError_t e = cudaEventRecord(d->fork, stream);
-  if (e == cudaSuccess) e = cudaStreamWaitEvent(d->aux, d->fork, 0);
-  if (e != cudaSuccess) return cuda_fail(e, "cascade fork");
-  // 1. suffix partial states (slots 0 .. splits - 1), on `stream`
+  // All on `stream`: the suffix decode, then the shared-prefix gather (it
+  // reads nothing the suffix decode writes, so it runs beside the suffix's
+  // tail and only its exit waits for it), the prefix attention, the merge.
+  // 1. suffix partial states (slots 0 .. splits - 1)
   float *part_o = nullptr, *part_lse = nullptr;
-  e = pkv::launch_cascade_suffix(g, layer, q, o, lse, page_table, table_stride, table_idx,
-                                 seq_lens, batch, num_q_heads, scale, plan, ks, workspace, d->err,
-                                 stream, &part_o, &part_lse);
+  cudaError_t e = pkv::launch_cascade_suffix(g, layer, q, o, lse, page_table, table_stride,
+                                             table_idx, seq_lens, batch, num_q_heads, scale, plan,
+                                             ks, workspace, d->err, stream, &part_o, &part_lse);
   if (e != cudaSuccess) return cuda_fail(e, "cascade suffix launch");
-  // 2. shared-prefix states of every member (slots splits .. splits + ks - 1),
-  //    on the second stream: the extend kernels, non-causal, one block of
-  //    queries per group's members, ks key ranges
+  // 2. shared-prefix states of every member (slots splits .. splits + ks - 1):
+  //    the extend kernels, non-causal, one block of queries per group's
+  //    members, ks key ranges
   pkv::ExtendMode mode;
   mode.causal = 0;
   mode.members = members;
@@ -379,16 +355,14 @@ pkv_status pkv_paged_cascade_decode_attn(
   mode.pstride = plan.splits + ks;
   mode.pslot = plan.splits;
   mode.key_splits = ks;
+  mode.overlap_previous = 1;
   e = pkv::launch_extend(g, layer, q, member_indptr, o, nullptr, prefix_page_table,
                          prefix_table_stride, nullptr, prefix_lens, num_groups, batch,
                          num_q_heads, scale, static_cast<int32_t>(pcap),
                          static_cast<uint8_t *>(workspace) + part_bytes, d->sm_count, d->err,
-                         d->aux, mode);
+                         stream, mode);
   if (e != cudaSuccess) return cuda_fail(e, "cascade prefix launch");
-  e = cudaEventRecord(d->join, d->aux);
-  if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, d->join, 0);
-  if (e != cudaSuccess) return cuda_fail(e, "cascade join");
-  // 3. merge, on `stream`
+  // 3. merge of every request's suffix splits and prefix states
   e = pkv::launch_cascade_merge(g, layer, q, o, lse, page_table, table_stride, table_idx,
                                 seq_lens, batch, num_q_heads, scale, plan, ks, part_o, part_lse,
                                 d->err, stream);

@@ -82,6 +82,9 @@ struct ExtendMode {
   const void *k_new = nullptr;
   const void *v_new = nullptr;
   int64_t kv_row_stride = 0;
+  // the gather reads nothing the previous kernel on the stream writes: it
+  // may run beside that kernel (its dependency wait moves to its exit)
+  int32_t overlap_previous = 0;
 };
 
 // Gathered-K/V workspace of the extend call: [2][batch][hkv][s_pad][d] bf16,
