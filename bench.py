@@ -59,8 +59,8 @@ MEASURED_TRAFFIC = {
                "bytes": 628162048},
     # profiles/extend_kernels_chunked-prefill-extend.md: extend_gather_kernel + extend_tc_kernel
     "extend": {"sources": ["extend.cu", "tc_common.cuh", "pkv_common.cuh"],
-               "sha256": "dbb711343cbffa5bad87e73ecf90b32cdd63fe411c57ea4454f68b4fc3953887",
-               "bytes": 528233728},
+               "sha256": "1346caf7eceeadf58410b7173be9f334d568cfb8d81e05685d2ce96fd612239b",
+               "bytes": 523301120},
 }
 
 
