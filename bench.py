@@ -49,15 +49,15 @@ L2_CLEAN_BYTES = 256 << 20  # read after the flush write (see L2Flush)
 CSRC = os.path.join(ROOT, "paged_kv_attention_out_gb300", "csrc")
 
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per call, summed
-# over the call's launches, from the ncu captures summarised under profiles/.
-# Each entry holds the SHA-256 of the kernel sources it was taken on; the
-# bench reports it only while those sources are unchanged (else null).
+# over the call's launches, from one ncu capture of each call. Each entry
+# holds the SHA-256 of the kernel sources it was taken on; the bench reports
+# it only while those sources are unchanged (else null).
 MEASURED_TRAFFIC = {
-    # profiles/decode_kernel_llama3-8b-decode.md: decode_kernel + decode_merge_kernel
+    # decode_kernel + decode_merge_kernel, Llama-3-8B-shaped decode
     "decode": {"sources": ["decode.cu", "pkv_common.cuh"],
                "sha256": "26163185fe6caad9331194f293495c329b9ec4affdb61e921c9b561df33c954d",
                "bytes": 628162048},
-    # profiles/extend_kernels_chunked-prefill-extend.md: extend_gather_kernel + extend_tc_kernel
+    # extend_gather_kernel + extend_tc_kernel, chunked-prefill extend
     "extend": {"sources": ["extend.cu", "tc_common.cuh", "pkv_common.cuh"],
                "sha256": "1346caf7eceeadf58410b7173be9f334d568cfb8d81e05685d2ce96fd612239b",
                "bytes": 523301120},
@@ -837,8 +837,19 @@ def parse_args(argv=None):
     return a
 
 
+def check_gpus(args, world: int):
+    """--gpus must match the number of ranks actually running: one rank per
+    GPU is launched by torchrun, so `--gpus N` without it (or with another
+    count) would measure a different number of GPUs than it reports."""
+    if args.gpus != world:
+        raise SystemExit(f"bench.py: --gpus {args.gpus} but {world} rank(s) are running "
+                         f"(WORLD_SIZE={world}); launch N > 1 with torchrun "
+                         f"--nproc-per-node N ... bench.py --gpus N")
+
+
 def main(argv=None):
     args = parse_args(argv)
+    check_gpus(args, dist_env()[1])
     if args.impl == "reference":
         run_reference(args)
     else:

@@ -43,6 +43,7 @@
 #include <math.h>
 
 #include <mutex>
+#include <type_traits>
 
 #include "pkv_common.cuh"
 #include "pkv_internal.h"
@@ -415,6 +416,12 @@ __device__ __forceinline__ float max3f(float x, float y, float z) {
   return r;
 }
 
+__device__ __forceinline__ float min3f(float x, float y, float z) {
+  float r;
+  asm("min.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(x), "f"(y), "f"(z));
+  return r;
+}
+
 // (y0, y1) = (x0, x1) * s + c, one packed fp32 instruction.
 __device__ __forceinline__ void fma2(float &y0, float &y1, float x0, float x1, float s, float c) {
   asm("{\n .reg .b64 x, m, a, y;\n mov.b64 x, {%2, %3};\n mov.b64 m, {%4, %4};\n"
@@ -686,6 +693,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t orow_t = tmem + lane_base + kTmemO + x * D;
     float m_used = -INFINITY, l = 0.f;
     bool ok = true;
+    // Sign of the softmax scale (any finite value is allowed): the largest
+    // scaled score scale * s comes from the largest raw score s when scale
+    // >= 0 and from the smallest when scale < 0. Grid-uniform.
+    const bool neg = a.scale_log2 < 0.f;
     for (int j = 0; j < n_x; ++j) {
       if (!(ok = mbar_wait_warp(bar(kBarSFull + x), j & 1, abort))) break;
       tc_fence_after_sync();
@@ -696,21 +707,43 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld32(srow + 96, *reinterpret_cast<float(*)[32]>(&v[96]));
       tmem_ld_wait();
       const int key0 = (tile0 + j) * kN;
-      if (key0 + kN - 1 > min_limit) {  // tile crosses some row's last key (warp-uniform)
+      // The tile crosses some row's last visible key (warp-uniform). Keys past
+      // a row's last one take the raw value that is never its extreme.
+      const bool crosses = key0 + kN - 1 > min_limit;
+      if (crosses) {
+        const float fill = neg ? INFINITY : -INFINITY;
 #pragma unroll
-        for (int cc = 0; cc < kN; ++cc) v[cc] = key0 + cc <= limit ? v[cc] : -INFINITY;
+        for (int cc = 0; cc < kN; ++cc) v[cc] = key0 + cc <= limit ? v[cc] : fill;
       }
-      // Row max of the raw scores (scale > 0 commutes with max).
-      float mx0 = fmaxf(v[0], v[1]), mx1 = fmaxf(v[2], v[3]);
-      float mx2 = fmaxf(v[4], v[5]), mx3 = fmaxf(v[6], v[7]);
+      // Row max of the scaled scores from the raw scores' max (scale >= 0)
+      // or min (scale < 0), four independent chains.
+      float ext;
+      if (!neg) {
+        float mx0 = fmaxf(v[0], v[1]), mx1 = fmaxf(v[2], v[3]);
+        float mx2 = fmaxf(v[4], v[5]), mx3 = fmaxf(v[6], v[7]);
 #pragma unroll
-      for (int cc = 8; cc < kN; cc += 8) {
-        mx0 = max3f(mx0, v[cc], v[cc + 1]);
-        mx1 = max3f(mx1, v[cc + 2], v[cc + 3]);
-        mx2 = max3f(mx2, v[cc + 4], v[cc + 5]);
-        mx3 = max3f(mx3, v[cc + 6], v[cc + 7]);
+        for (int cc = 8; cc < kN; cc += 8) {
+          mx0 = max3f(mx0, v[cc], v[cc + 1]);
+          mx1 = max3f(mx1, v[cc + 2], v[cc + 3]);
+          mx2 = max3f(mx2, v[cc + 4], v[cc + 5]);
+          mx3 = max3f(mx3, v[cc + 6], v[cc + 7]);
+        }
+        ext = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
+      } else {
+        float mn0 = fminf(v[0], v[1]), mn1 = fminf(v[2], v[3]);
+        float mn2 = fminf(v[4], v[5]), mn3 = fminf(v[6], v[7]);
+#pragma unroll
+        for (int cc = 8; cc < kN; cc += 8) {
+          mn0 = min3f(mn0, v[cc], v[cc + 1]);
+          mn1 = min3f(mn1, v[cc + 2], v[cc + 3]);
+          mn2 = min3f(mn2, v[cc + 4], v[cc + 5]);
+          mn3 = min3f(mn3, v[cc + 6], v[cc + 7]);
+        }
+        ext = fminf(fminf(mn0, mn1), fminf(mn2, mn3));
       }
-      const float mt = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * a.scale_log2;
+      // A row with no visible key in this tile has ext = +-inf and no
+      // maximum (for scale 0 the product would be NaN).
+      const float mt = (crosses && isinf(ext)) ? -INFINITY : ext * a.scale_log2;
       // Lazy rescale: move the reference max only when a row's max grew by
       // more than 2^kRescaleThreshold (warp-uniform: tcgen05.ld/st are
       // .sync.aligned, so every lane takes part, with factor 1 where its
@@ -726,23 +759,37 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const float nm = m_used == -INFINITY ? 0.f : -m_used;
       float sa0 = 0.f, sa1 = 0.f, sb0 = 0.f, sb1 = 0.f;
+      // P = exp2(scale * s - m) as bf16 pairs into TMEM. On a crossing tile
+      // a masked key's exponent is forced to -inf after the FMA (its fill
+      // times scale is -inf, except for scale 0, where it is NaN).
+      auto exp_to_p = [&](auto masked) {
+        constexpr bool kMasked = decltype(masked)::value;
 #pragma unroll
-      for (int cc = 0; cc < kN; cc += 32) {
-        uint32_t w[16];
+        for (int cc = 0; cc < kN; cc += 32) {
+          uint32_t w[16];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          float y0, y1;
-          fma2(y0, y1, v[cc + 2 * e], v[cc + 2 * e + 1], a.scale_log2, nm);
-          y0 = fast_exp2(y0);
-          y1 = fast_exp2(y1);
-          if (e & 1)
-            add2(sb0, sb1, y0, y1);
-          else
-            add2(sa0, sa1, y0, y1);
-          w[e] = pack_bf16(y0, y1);
+          for (int e = 0; e < 16; ++e) {
+            float y0, y1;
+            fma2(y0, y1, v[cc + 2 * e], v[cc + 2 * e + 1], a.scale_log2, nm);
+            if (kMasked) {
+              y0 = key0 + cc + 2 * e <= limit ? y0 : -INFINITY;
+              y1 = key0 + cc + 2 * e + 1 <= limit ? y1 : -INFINITY;
+            }
+            y0 = fast_exp2(y0);
+            y1 = fast_exp2(y1);
+            if (e & 1)
+              add2(sb0, sb1, y0, y1);
+            else
+              add2(sa0, sa1, y0, y1);
+            w[e] = pack_bf16(y0, y1);
+          }
+          tmem_st16u(srow + cc / 2, w);  // P_x: keys cc .. cc + 31 -> columns cc/2 ..
         }
-        tmem_st16u(srow + cc / 2, w);  // P_x: keys cc .. cc + 31 -> columns cc/2 ..
-      }
+      };
+      if (crosses)
+        exp_to_p(std::true_type{});
+      else
+        exp_to_p(std::false_type{});
       l = l * f + ((sa0 + sa1) + (sb0 + sb1));
       if (rescale) {
         // O_x is stable: S_x(j) completed, so did PV_x(j - 1) before it.

@@ -442,7 +442,7 @@ def random_case(seed: int, *, kind: str = "decode", seq_lens, chunk_lens=None,
 def cascade_case(seed: int, *, group_sizes, prefix_lens, suffix_lo: int = 1,
                  suffix_hi: int = 64, Hq: int = 4, Hkv: int = 2, D: int = 64, P: int = 1,
                  shuffled: bool = True, extra_pages: int = 16,
-                 name: str | None = None) -> Case:
+                 scale: float | None = None, name: str | None = None) -> Case:
     """Decode case whose requests come in groups sharing a prefix, as a radix
     cache hit gives: group k has group_sizes[k] members that share its first
     prefix_lens[k] keys (a multiple of P, possibly 0); each member then has a
@@ -480,7 +480,8 @@ def cascade_case(seed: int, *, group_sizes, prefix_lens, suffix_lo: int = 1,
     pt = _pad_rows(rows, stride + 1, filler)
     out_loc = np.array([token_slots[b][-1] for b in range(B)], np.int64)
     return Case(name=name or f"cascade-{seed}", kind="decode", seed=seed, B=B, Hq=Hq, Hkv=Hkv,
-                D=D, P=P, L=1, NP=NP, layer=0, scale=1.0 / math.sqrt(D),
+                D=D, P=P, L=1, NP=NP, layer=0,
+                scale=scale if scale is not None else 1.0 / math.sqrt(D),
                 seq_lens=seq.astype(np.int32), page_table=pt, out_loc=out_loc.astype(np.int32),
                 token_slots=token_slots,
                 notes={"group_of_request": group_of.tolist(), "group_prefix": plens})

@@ -76,10 +76,54 @@ def test_reference_arm_prints_one_json_line():
 
 def test_reference_arm_other_ranks_exit_quietly():
     env = dict(os.environ, RANK="1", WORLD_SIZE="2")
-    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--steps", "1",
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--gpus", "2",
+                        "--steps", "1",
                         "--warmup", "3"], cwd=ROOT, capture_output=True, text=True,
                        timeout=300, env=env)
     assert r.returncode == 0 and r.stdout.strip() == ""
+
+
+def test_gpus_must_match_the_running_ranks():
+    """`--gpus 2` without a second rank exits non-zero instead of measuring one
+    GPU under an n_gpus of 1."""
+    env = {k: v for k, v in os.environ.items() if k not in ("RANK", "WORLD_SIZE", "LOCAL_RANK")}
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--gpus", "2",
+                        "--steps", "1", "--warmup", "3"], cwd=ROOT, capture_output=True,
+                       text=True, timeout=300, env=env)
+    assert r.returncode != 0 and "--gpus 2" in r.stderr and r.stdout.strip() == ""
+
+
+def _bench_rank(rank, world, port, q):
+    """One rank of `bench.py --impl reference --gpus 2` under a gloo world."""
+    import contextlib
+    import io
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    out = io.StringIO()
+    with contextlib.redirect_stdout(out):
+        bench.main(["--impl", "reference", "--gpus", str(world), "--steps", "1",
+                    "--warmup", "3"])
+    dist.barrier()
+    dist.destroy_process_group()
+    q.put((rank, out.getvalue()))
+
+
+def test_world_of_two_reports_n_gpus_equal_to_the_world_size():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = 30000 + os.getpid() % 1000
+    procs = [ctx.Process(target=_bench_rank, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    out = dict(q.get(timeout=600) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert out[1].strip() == ""  # only rank 0 prints
+    lines = [x for x in out[0].splitlines() if x.strip()]
+    assert len(lines) == 1 and json.loads(lines[0])["n_gpus"] == 2
 
 
 def test_e2e_staging_buffer_round_trips_every_tensor(monkeypatch):

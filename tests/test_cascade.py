@@ -11,7 +11,8 @@ import numpy as np
 import pytest
 import torch
 
-from helpers import compare, gpu_inputs, lse_compare, oracle_run
+from helpers import (assert_every_row_written, compare, gpu_inputs, lse_compare, nan_outputs,
+                     oracle_run)
 from paged_kv_attention_out_gb300 import workloads as W
 
 pytestmark = pytest.mark.gpu
@@ -30,8 +31,7 @@ def cascade_run(case: W.Case, poison: bool = True, repeat: int = 1):
     ws = torch.full((n,), 0x7F, dtype=torch.uint8, device="cuda")  # stale contents
     outs = []
     for _ in range(repeat):
-        o = torch.empty_like(q)
-        lse = torch.empty(q.shape[:2], dtype=torch.float32, device="cuda")
+        o, lse = nan_outputs(q)
         pkv.pkv_paged_cascade_decode_attn(
             pool, case.layer, q, o, lse, ct["prefix_page_table"], ct["prefix_lens"],
             ct["member_indptr"], ct["members"], ct["page_table"], ct["seq_lens"], case.scale,
@@ -52,6 +52,20 @@ def test_cascade_matches_oracle(P, Hq, Hkv, D, sizes, prefixes):
     case = W.cascade_case(7, group_sizes=sizes, prefix_lens=prefixes, P=P, Hq=Hq, Hkv=Hkv,
                           D=D, suffix_lo=1, suffix_hi=150)
     (o, lse), = cascade_run(case)
+    assert_every_row_written(o, lse)
+    want_o, want_lse, _ = oracle_run(case)
+    compare(o, want_o)
+    lse_compare(lse, want_lse)
+
+
+@pytest.mark.parametrize("scale", [-0.0884, -1.0, 0.0, 2.0])
+def test_cascade_any_finite_scale(scale):
+    """The shared-prefix attention runs on the extend kernel (non-causal, its
+    last prefix tile masked): any finite scale, as for decode."""
+    case = W.cascade_case(9, group_sizes=[40, 3], prefix_lens=[300, 129], P=1, Hq=32, Hkv=8,
+                          D=128, suffix_lo=1, suffix_hi=200, scale=scale)
+    (o, lse), = cascade_run(case)
+    assert_every_row_written(o, lse)
     want_o, want_lse, _ = oracle_run(case)
     compare(o, want_o)
     lse_compare(lse, want_lse)
@@ -64,17 +78,14 @@ def test_cascade_repeat_is_bitwise_stable():
 
 
 @pytest.mark.parametrize("shuffled", [False, True])
-def test_radix_shared_cascade_full_size_sampled(shuffled):
+def test_radix_shared_cascade_full_size_every_request(shuffled):
     case = W.radix_shared_decode(0, shuffled=shuffled)
     (o, lse), = cascade_run(case)
     torch.cuda.empty_cache()
-    assert np.isfinite(o).all()
-    groups = np.array(case.notes["group_of_request"])
-    req = sorted(np.flatnonzero(groups == groups[0])[:3].tolist() +
-                 np.flatnonzero(groups != groups[0])[:3].tolist())
-    want_o, want_lse, _ = oracle_run(case.compact(req))
-    compare(o[req], want_o)
-    lse_compare(lse[req], want_lse)
+    assert_every_row_written(o, lse)
+    want_o, want_lse, _ = oracle_run(case.compact(list(range(case.B))))
+    compare(o, want_o)
+    lse_compare(lse, want_lse)
 
 
 def test_cascade_workspace_too_small_is_refused():

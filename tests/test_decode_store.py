@@ -8,7 +8,8 @@ import numpy as np
 import pytest
 import torch
 
-from helpers import compare, gpu_inputs, lse_compare, oracle_run, to_bits
+from helpers import (assert_every_row_written, compare, gpu_inputs, lse_compare, nan_outputs,
+                     oracle_run, to_bits)
 from paged_kv_attention_out_gb300 import workloads as W
 
 pytestmark = pytest.mark.gpu
@@ -20,8 +21,7 @@ def fused_run(case, poison=True, hint=None, with_lse=True):
     h = case.max_seq_len if hint is None else hint
     ws = torch.empty(max(pkv.pkv_decode_workspace_size(case.B, case.Hq, case.Hkv, case.D, h), 256),
                      dtype=torch.uint8, device="cuda")
-    o = torch.empty_like(q)
-    lse = torch.empty(q.shape[:2], dtype=torch.float32, device="cuda") if with_lse else None
+    o, lse = nan_outputs(q, with_lse)
     pkv.pkv_paged_decode_attn_store(pool, case.layer, q, k, v, o, lse, t["page_table"],
                                     t["seq_lens"], case.scale, h, ws, table_idx=t.get("table_idx"))
     torch.cuda.synchronize()
@@ -37,6 +37,7 @@ def fused_run(case, poison=True, hint=None, with_lse=True):
 def test_fused_store_decode_matches_oracle_and_pool_bits(kw):
     case = W.random_case(21, **kw)
     o, lse, pool = fused_run(case)
+    assert_every_row_written(o, lse)
     want_o, want_lse, want_pool = oracle_run(case)
     compare(o.float().cpu().double().numpy(), want_o)
     lse_compare(lse.cpu().double().numpy(), want_lse)
@@ -52,8 +53,7 @@ def test_fused_equals_separate_store_then_decode_bitwise():
     h = case.max_seq_len
     ws = torch.empty(max(pkv.pkv_decode_workspace_size(case.B, case.Hq, case.Hkv, case.D, h), 256),
                      dtype=torch.uint8, device="cuda")
-    o2 = torch.empty_like(q)
-    l2 = torch.empty(q.shape[:2], dtype=torch.float32, device="cuda")
+    o2, l2 = nan_outputs(q)
     pkv.pkv_kv_store(pool, case.layer, k, v, t["out_loc"])
     pkv.pkv_paged_decode_attn(pool, case.layer, q, o2, l2, t["page_table"], t["seq_lens"],
                               case.scale, h, ws)
@@ -62,13 +62,12 @@ def test_fused_equals_separate_store_then_decode_bitwise():
     assert torch.equal(p1.view(torch.int16), pool.view(torch.int16))
 
 
-def test_llama8b_fused_full_size_sampled():
+def test_llama8b_fused_full_size_every_request():
     case = W.llama8b_decode(0)
     o, lse, pool = fused_run(case)
     del pool
     torch.cuda.empty_cache()
-    rng = np.random.default_rng(1)
-    req = sorted({int(np.argmax(case.seq_lens)), *rng.choice(case.B, 3, replace=False).tolist()})
-    want_o, want_lse, _ = oracle_run(case.compact(req))
-    compare(o.float().cpu().double().numpy()[req], want_o)
-    lse_compare(lse.cpu().double().numpy()[req], want_lse)
+    assert_every_row_written(o, lse)
+    want_o, want_lse, _ = oracle_run(case.compact(list(range(case.B))))
+    compare(o.float().cpu().double().numpy(), want_o)
+    lse_compare(lse.cpu().double().numpy(), want_lse)

@@ -27,7 +27,7 @@ def _decode(case, pool, q, t, fused=None):
     h = case.max_seq_len
     ws = torch.empty(max(pkv.pkv_decode_workspace_size(case.B, case.Hq, case.Hkv, case.D, h), 256),
                      dtype=torch.uint8, device="cuda")
-    o = torch.empty_like(q)
+    o = torch.full_like(q, float("nan"))
     if fused is None:
         pkv.pkv_paged_decode_attn(pool, case.layer, q, o, None, t["page_table"], t["seq_lens"],
                                   case.scale, h, ws)
@@ -80,7 +80,7 @@ def test_extend_request_longer_than_the_hint_is_flagged_and_skipped():
     hint = 200  # request 1 (700 keys) is beyond it
     ws = torch.empty(pkv.pkv_extend_workspace_size(case.B, case.Hkv, case.D, hint),
                      dtype=torch.uint8, device="cuda")
-    o = torch.zeros_like(q)
+    o = torch.full_like(q, float("nan"))
     _errors()
     pkv.pkv_paged_extend_attn(pool, case.layer, q, t["qo_indptr"], o, None, t["page_table"],
                               t["seq_lens"], case.scale, hint, ws)
@@ -102,7 +102,7 @@ def test_extend_malformed_qo_indptr_is_flagged():
     h = case.max_seq_len
     ws = torch.empty(pkv.pkv_extend_workspace_size(case.B, case.Hkv, case.D, h),
                      dtype=torch.uint8, device="cuda")
-    o = torch.zeros_like(q)
+    o = torch.full_like(q, float("nan"))
     _errors()
     pkv.pkv_paged_extend_attn(pool, case.layer, q, qo, o, None, t["page_table"], t["seq_lens"],
                               case.scale, h, ws)
@@ -124,7 +124,7 @@ def test_cascade_member_out_of_range_is_flagged():
     pmax, smax = 64, int(ct["seq_lens"].max())
     ws = torch.empty(pkv.pkv_cascade_workspace_size(case.B, case.Hq, case.Hkv, case.D, 2, pmax,
                                                     smax), dtype=torch.uint8, device="cuda")
-    o = torch.zeros_like(q)
+    o = torch.full_like(q, float("nan"))
     _errors()
     pkv.pkv_paged_cascade_decode_attn(pool, case.layer, q, o, None, ct["prefix_page_table"],
                                       ct["prefix_lens"], ct["member_indptr"], members,

@@ -1,9 +1,12 @@
 """Paged extend (chunked-prefill) attention on the GPU against the oracle.
 
-Small cases run the whole oracle. The full-size chunked-prefill workload is
-checked on sampled chunk queries: query j of request r equals a decode over
-the first p_r + j + 1 keys of its row (a pin of the oracle), computed on a
-compact cut of that request.
+Small cases run the whole oracle. The full-size chunked-prefill workload
+(outputs NaN-filled before the call) must write every row, and two whole
+requests, the one with the longest cached prefix and the one with the
+longest chunk, are compared query by query and head by head against the
+oracle on a compact cut of each request; the others on sampled queries
+(query j of request r equals a decode over the first p_r + j + 1 keys of
+its row, a pin of the oracle).
 """
 from __future__ import annotations
 
@@ -12,7 +15,8 @@ import pytest
 import torch
 
 import oracle
-from helpers import (check_against_oracle, compare, gpu_run, lse_compare, oracle_inputs)
+from helpers import (assert_every_row_written, check_against_oracle, compare, gpu_run,
+                     lse_compare, oracle_inputs, oracle_run)
 from paged_kv_attention_out_gb300 import workloads as W
 
 pytestmark = pytest.mark.gpu
@@ -57,13 +61,35 @@ def test_mixed_prefill_and_decode_batch():
     check_against_oracle(case)
 
 
-def test_chunked_prefill_full_size_sampled():
+# The softmax scale is any finite number: negative (the largest scaled score
+# comes from the smallest raw score), zero (every visible key weighs the
+# same: o = mean(V), lse = log n) and large (scores spread over hundreds of
+# log2 units, so the lazy rescale of O runs on most tiles).
+@pytest.mark.parametrize("scale", [-0.0884, -1.0, 0.0, 1.0, 3.0])
+@pytest.mark.parametrize("D", [64, 128])
+def test_extend_any_finite_scale(scale, D):
+    case = W.random_case(56, kind="extend", seq_lens=[300, 129, 700, 64],
+                         chunk_lens=[170, 129, 256, 1], Hq=8, Hkv=2, D=D, P=16,
+                         scale=scale)
+    check_against_oracle(case)
+
+
+def test_chunked_prefill_full_size():
     case = W.chunked_prefill_extend(0)
     o, lse, _ = gpu_run(case)
-    assert np.isfinite(o).all()
+    torch.cuda.empty_cache()
+    assert_every_row_written(o, lse)
+    chunks = np.diff(case.qo_indptr)
+    prefixes = case.seq_lens - chunks
+    whole = sorted({int(np.argmax(prefixes)), int(np.argmax(chunks))})
+    for r in whole:  # every chunk token, every head: every block and diagonal tile
+        s, e = int(case.qo_indptr[r]), int(case.qo_indptr[r + 1])
+        want_o, want_lse, _ = oracle_run(case.compact([r]))
+        compare(o[s:e], want_o)
+        lse_compare(lse[s:e], want_lse)
     rng = np.random.default_rng(0)
     q_all = W.bf16_bits(case.q())
-    for r in range(case.B):
+    for r in sorted(set(range(case.B)) - set(whole)):
         sub = case.compact([r])
         pool, k, v, _ = oracle_inputs(sub)
         oracle.kv_store(pool, 0, k, v, sub.out_loc)

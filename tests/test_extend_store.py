@@ -10,7 +10,8 @@ import pytest
 import torch
 
 import oracle
-from helpers import compare, gpu_inputs, lse_compare, oracle_inputs, oracle_run, to_bits
+from helpers import (assert_every_row_written, compare, gpu_inputs, lse_compare, nan_outputs,
+                     oracle_inputs, oracle_run, to_bits)
 from paged_kv_attention_out_gb300 import workloads as W
 
 pytestmark = pytest.mark.gpu
@@ -22,8 +23,7 @@ def fused_run(case, poison=True):
     h = case.max_seq_len
     ws = torch.empty(pkv.pkv_extend_workspace_size(case.B, case.Hkv, case.D, h),
                      dtype=torch.uint8, device="cuda")
-    o = torch.empty_like(q)
-    lse = torch.empty(q.shape[:2], dtype=torch.float32, device="cuda")
+    o, lse = nan_outputs(q)
     pkv.pkv_paged_extend_attn_store(pool, case.layer, q, k, v, t["qo_indptr"], o, lse,
                                     t["page_table"], t["seq_lens"], case.scale, h, ws,
                                     table_idx=t.get("table_idx"))
@@ -37,8 +37,7 @@ def separate_run(case, poison=True):
     h = case.max_seq_len
     ws = torch.empty(pkv.pkv_extend_workspace_size(case.B, case.Hkv, case.D, h),
                      dtype=torch.uint8, device="cuda")
-    o = torch.empty_like(q)
-    lse = torch.empty(q.shape[:2], dtype=torch.float32, device="cuda")
+    o, lse = nan_outputs(q)
     pkv.pkv_kv_store(pool, case.layer, k, v, t["out_loc"])
     pkv.pkv_paged_extend_attn(pool, case.layer, q, t["qo_indptr"], o, lse, t["page_table"],
                               t["seq_lens"], case.scale, h, ws, table_idx=t.get("table_idx"))
@@ -58,6 +57,7 @@ def separate_run(case, poison=True):
 def test_fused_store_extend_matches_oracle_and_pool_bits(kw):
     case = W.random_case(61, kind="extend", **kw)
     o, lse, pool = fused_run(case)
+    assert_every_row_written(o, lse)
     want_o, want_lse, want_pool = oracle_run(case)
     compare(o.float().cpu().double().numpy(), want_o)
     lse_compare(lse.cpu().double().numpy(), want_lse)
@@ -83,6 +83,7 @@ def test_chunked_prefill_fused_full_size():
     o2, l2, p2 = separate_run(case)
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
     assert torch.equal(p1.view(torch.int16), p2.view(torch.int16))
+    assert_every_row_written(o1, l1)
     del p1, p2
     torch.cuda.empty_cache()
     o = o1.float().cpu().double().numpy()
@@ -114,7 +115,7 @@ def test_fused_bad_chunk_page_is_flagged_and_not_stored():
     h = case.max_seq_len
     ws = torch.empty(pkv.pkv_extend_workspace_size(case.B, case.Hkv, case.D, h),
                      dtype=torch.uint8, device="cuda")
-    o = torch.empty_like(q)
+    o, _ = nan_outputs(q, with_lse=False)
     pkv.pkv_read_device_errors()
     pkv.pkv_paged_extend_attn_store(pool, case.layer, q, k, v, t["qo_indptr"], o, None, pt,
                                     t["seq_lens"], case.scale, h, ws)

@@ -63,8 +63,8 @@ def test_decode_step_in_a_graph():
                      dtype=torch.uint8, device="cuda")
 
     def call(pool, k, v, q):
-        o = torch.empty_like(q)
-        lse = torch.empty(q.shape[:2], dtype=torch.float32, device="cuda")
+        o = torch.full_like(q, float("nan"))
+        lse = torch.full(q.shape[:2], float("nan"), dtype=torch.float32, device="cuda")
         pkv.pkv_kv_store(pool, case.layer, k, v, t["out_loc"])
         pkv.pkv_paged_decode_attn(pool, case.layer, q, o, lse, t["page_table"], t["seq_lens"],
                                   case.scale, h, ws)
@@ -85,8 +85,8 @@ def test_extend_step_in_a_graph():
                      dtype=torch.uint8, device="cuda")
 
     def call(pool, k, v, q):
-        o = torch.empty_like(q)
-        lse = torch.empty(q.shape[:2], dtype=torch.float32, device="cuda")
+        o = torch.full_like(q, float("nan"))
+        lse = torch.full(q.shape[:2], float("nan"), dtype=torch.float32, device="cuda")
         pkv.pkv_kv_store(pool, case.layer, k, v, t["out_loc"])
         pkv.pkv_paged_extend_attn(pool, case.layer, q, t["qo_indptr"], o, lse, t["page_table"],
                                   t["seq_lens"], case.scale, h, ws)
@@ -108,8 +108,8 @@ def test_cascade_step_in_a_graph():
                                                     smax), dtype=torch.uint8, device="cuda")
 
     def call(pool, k, v, q):
-        o = torch.empty_like(q)
-        lse = torch.empty(q.shape[:2], dtype=torch.float32, device="cuda")
+        o = torch.full_like(q, float("nan"))
+        lse = torch.full(q.shape[:2], float("nan"), dtype=torch.float32, device="cuda")
         pkv.pkv_kv_store(pool, case.layer, k, v, t["out_loc"])
         pkv.pkv_paged_cascade_decode_attn(
             pool, case.layer, q, o, lse, ct["prefix_page_table"], ct["prefix_lens"],

@@ -6,7 +6,8 @@ import numpy as np
 import pytest
 import torch
 
-from helpers import check_against_oracle, compare, gpu_inputs, lse_compare, oracle_run
+from helpers import (assert_every_row_written, check_against_oracle, compare, gpu_inputs,
+                     lse_compare, nan_outputs, oracle_run)
 from paged_kv_attention_out_gb300 import workloads as W
 
 pytestmark = pytest.mark.gpu
@@ -44,14 +45,14 @@ def test_cascade_300_groups():
     smax = int(ct["seq_lens"].max())
     ws = torch.empty(pkv.pkv_cascade_workspace_size(case.B, case.Hq, case.Hkv, case.D, G, pmax,
                                                     smax), dtype=torch.uint8, device="cuda")
-    o = torch.empty_like(q)
-    lse = torch.empty(q.shape[:2], dtype=torch.float32, device="cuda")
+    o, lse = nan_outputs(q)
     pkv.pkv_read_device_errors()
     pkv.pkv_paged_cascade_decode_attn(pool, case.layer, q, o, lse, ct["prefix_page_table"],
                                       ct["prefix_lens"], ct["member_indptr"], ct["members"],
                                       ct["page_table"], ct["seq_lens"], case.scale, pmax, smax,
                                       ws)
     assert pkv.pkv_read_device_errors() == 0
+    assert_every_row_written(o, lse)
     want_o, want_lse, _ = oracle_run(case)
     compare(o.float().cpu().double().numpy(), want_o)
     lse_compare(lse.cpu().double().numpy(), want_lse)

@@ -33,8 +33,8 @@ def test_merge_matches_oracle(out_dtype, rows, H, D):
     want_o, want_l = oracle.merge_lse(o_a.double().numpy(), l_a.double().numpy(),
                                       o_b.double().numpy(), l_b.double().numpy())
     d = [x.cuda() for x in (o_a, l_a, o_b, l_b)]
-    out = torch.empty(rows, H, D, dtype=out_dtype, device="cuda")
-    lse = torch.empty(rows, H, device="cuda")
+    out = torch.full((rows, H, D), float("nan"), dtype=out_dtype, device="cuda")
+    lse = torch.full((rows, H), float("nan"), device="cuda")
     pkv.pkv_merge_lse(*d, out, lse)
     torch.cuda.synchronize()
     got = out.double().cpu().numpy()

@@ -6,16 +6,18 @@ offers no allocation hook, or a serving loop that must never call cudaMalloc
 because it can synchronise the device and fail with out-of-memory mid-step.
 For them the library keeps the split-KV scratch in a fixed device array of
 its own. These tests call that entry point through the C ABI and check it
-against pkv_paged_decode_attn with a caller workspace, on two calls in a row
-(the second call finds the first call's leftovers in the shared scratch),
-and check that a plan larger than the array is refused.
+bit for bit against pkv_paged_decode_attn with a caller workspace (the
+same plan and kernels), and the first call also against the oracle, on two
+calls in a row (the second call finds the first call's leftovers in the
+shared scratch), and check that a plan larger than the array is refused.
 """
 from __future__ import annotations
 
 import pytest
 import torch
 
-from helpers import (compare, ensure_built, gpu_attention, gpu_inputs, lse_compare)
+from helpers import (assert_every_row_written, compare, ensure_built, gpu_attention, gpu_inputs,
+                     lse_compare, nan_outputs, oracle_run)
 from paged_kv_attention_out_gb300 import workloads as W
 
 pytestmark = pytest.mark.gpu
@@ -23,21 +25,27 @@ pytestmark = pytest.mark.gpu
 SCRATCH_BYTES = 32 << 20  # PKV_NOALLOC_SCRATCH_BYTES in include/pkv.h
 
 
-def _noalloc_vs_workspace(case):
+def _noalloc_vs_workspace(case, against_oracle=False):
+    """Both calls run the same split plan and kernels, so the scratch variant
+    must give the workspace variant's bits exactly: a wrong scratch offset or
+    a leftover of the previous call would change them."""
     import paged_kv_attention_out_gb300 as pkv
     pool, k, v, q, t = gpu_inputs(case)
     pkv.pkv_kv_store(pool, case.layer, k, v, t["out_loc"])
     need = pkv.pkv_decode_workspace_size(case.B, case.Hq, case.Hkv, case.D, case.max_seq_len)
     assert 0 < need <= SCRATCH_BYTES, "the case must exercise the split scratch"
     want_o, want_lse = gpu_attention(case, pool, q, t)  # caller-provided workspace
-    o = torch.full_like(q, float("nan"))
-    lse = torch.full(q.shape[:2], float("nan"), dtype=torch.float32, device=q.device)
+    o, lse = nan_outputs(q)
     pkv.pkv_paged_decode_attn_noalloc(pool, case.layer, q, o, lse, t["page_table"],
                                       t["seq_lens"], case.scale, case.max_seq_len,
                                       table_idx=t.get("table_idx"))
     torch.cuda.synchronize()
-    compare(o.double().cpu().numpy(), want_o.double().cpu().numpy())
-    lse_compare(lse.double().cpu().numpy(), want_lse.double().cpu().numpy())
+    assert_every_row_written(o, lse)
+    assert torch.equal(o, want_o) and torch.equal(lse, want_lse)
+    if against_oracle:
+        oo, ol, _ = oracle_run(case)
+        compare(o.double().cpu().numpy(), oo)
+        lse_compare(lse.double().cpu().numpy(), ol)
 
 
 def test_noalloc_matches_workspace_decode_on_two_calls_in_a_row():
@@ -46,7 +54,7 @@ def test_noalloc_matches_workspace_decode_on_two_calls_in_a_row():
                           P=1)
     second = W.random_case(72, seq_lens=[9000, 33, 2500], Hq=32, Hkv=4, D=128, P=16,
                            use_table_idx=True)
-    _noalloc_vs_workspace(first)
+    _noalloc_vs_workspace(first, against_oracle=True)
     _noalloc_vs_workspace(second)
 
 
