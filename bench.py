@@ -636,6 +636,8 @@ def other_workloads(args, dev, peaks, peak_src, flush, only=None):
         out.update(_radix_workload(args, dev, peaks, peak_src, flush, steps, warm))
     if want("tiny-decode"):
         out.update(_tiny_workload(args, dev, flush, steps, warm))
+    if want("decode-graph-batches"):
+        out.update(_graph_batches_workload(args, dev, flush, steps, warm))
     return out
 
 
@@ -728,6 +730,71 @@ def _tiny_workload(args, dev, flush, steps, warm):
     return out
 
 
+def _graph_batches_workload(args, dev, flush, steps, warm):
+    """Small-batch decode latency through the graph harness: the fused
+    store_kv + decode step of the Llama-3-8B-shaped workload captured at
+    batch sizes 1, 2, 4, ..., 64 (DecodeGraphRunner) and replayed at each
+    size on that many of its requests; per size the replay time (L2 flushed
+    before each replay, CUDA events around the replay alone) and the same
+    step as an eager call. The pool holds one layer (the attended data are
+    the same as in the 32-layer pool)."""
+    from paged_kv_attention_out_gb300.graph_runner import DecodeGraphRunner
+    import paged_kv_attention_out_gb300 as pkv
+    case = W.llama8b_decode(args.seed)
+    case.L, case.layer = 1, 0
+    pool = case.make_pool(dev, poison=False)
+    k, v = case.new_kv(dev)
+    q = case.q(dev)
+    t = case.device_tables(dev)
+    runner = DecodeGraphRunner(pool, 0, case.Hq, case.B, t["page_table"].shape[1],
+                               case.max_seq_len, case.scale)
+    stream = torch.cuda.current_stream()
+    reps = max(10, min(steps, 50))
+    rows = {"batch": [], "replay_us": [], "eager_us": [], "replay_gbs": []}
+    for n in runner.sizes:
+        runner.stage(q[:n], k[:n], v[:n], t["page_table"][:n], t["seq_lens"][:n])
+        ws = torch.empty(max(pkv.pkv_decode_workspace_size(n, case.Hq, case.Hkv, case.D,
+                                                           case.max_seq_len), 256),
+                         dtype=torch.uint8, device=dev)
+        o = torch.empty_like(q[:n])
+        lse = torch.empty(n, case.Hq, dtype=torch.float32, device=dev)
+
+        def eager():
+            pkv.pkv_paged_decode_attn_store(pool, 0, q[:n], k[:n], v[:n], o, lse,
+                                            t["page_table"][:n], t["seq_lens"][:n],
+                                            case.scale, case.max_seq_len, ws)
+
+        def replay():
+            runner.replay(n)
+
+        times = {}
+        for name, fn in (("replay", replay), ("eager", eager)):
+            for _ in range(warm):
+                flush()
+                fn()
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(reps)]
+            for e0, e1 in ev:
+                flush()
+                e0.record(stream)
+                fn()
+                e1.record(stream)
+            torch.cuda.synchronize()
+            times[name] = statistics.mean(e0.elapsed_time(e1) for e0, e1 in ev) * 1e3
+        by = decode_bytes(case.compact(list(range(n))))
+        rows["batch"].append(n)
+        rows["replay_us"].append(round(times["replay"], 2))
+        rows["eager_us"].append(round(times["eager"], 2))
+        rows["replay_gbs"].append(round(by / (times["replay"] * 1e-6) / 1e9, 1))
+    del runner, pool
+    torch.cuda.empty_cache()
+    return {"decode-graph-batches": {
+        "metric": "decode step latency (graph replay)", "unit": "us",
+        "step": "store_kv fused into decode + split merge, Llama-3-8B-shaped requests "
+                "(first n of the 64), replayed from the graph captured at n",
+        **rows}}
+
+
 def _graph_replay_us(wl: Workload, steps: int, warm: int) -> float:
     """Mean device time of one store_kv + attention step captured in a CUDA
     graph and replayed back to back (the serving engine replays decode steps
@@ -817,7 +884,7 @@ def parse_args(argv=None):
                     help="skip the other named workloads")
     ap.add_argument("--only", choices=["llama3-8b-decode", "chunked-prefill-extend",
                                        "long-context-decode", "radix-shared-decode",
-                                       "tiny-decode"], default=None,
+                                       "tiny-decode", "decode-graph-batches"], default=None,
                     help="run one named workload alone and print its JSON object "
                          "(for profiling); llama3-8b-decode = the main line")
     ap.add_argument("--no-cpu-baseline", action="store_true")

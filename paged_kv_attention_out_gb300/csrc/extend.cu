@@ -43,7 +43,6 @@
 #include <math.h>
 
 #include <mutex>
-#include <type_traits>
 
 #include "pkv_common.cuh"
 #include "pkv_internal.h"
@@ -94,7 +93,8 @@ enum : int {
   kBarOFull = 8,      // MMA: every MMA done, O final
   kBarTeardown = 9,   // MMA: everything issued has finished (abort path)
   kBarQFull = 10,     // producer: both Q tiles landed (TMA bytes)
-  kBarCount = 11,
+  kBarQReady = 11,    // softmax warps: Q negated / zeroed in place (q_mode != 0)
+  kBarCount = 12,
 };
 
 struct GatherArgs {
@@ -145,7 +145,12 @@ struct ExtendArgs {
   int32_t tokens_per_tile;  // floor(128 / group) chunk tokens per query tile
   int32_t capacity;
   int32_t s_pad;
-  float scale_log2;
+  float scale_log2;  // |scale| * log2(e) (log2(e) when scale is 0), always > 0
+  // How the softmax scale's sign reaches the scores: the row max is taken
+  // on raw scores, which needs scale_log2 > 0, so a negative scale negates
+  // Q in shared memory (scale * q.k = |scale| * (-q).k, exactly) and a zero
+  // scale zeroes it (every score 0, as for q = 0). 0: Q as given.
+  int32_t q_mode;
   unsigned *err;
   const int32_t *plan;
   // query source and result sink (see ExtendMode)
@@ -404,40 +409,6 @@ __device__ __forceinline__ void gather_body(const GatherArgs &a) {
   }
 }
 
-__device__ __forceinline__ float fast_exp2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
-__device__ __forceinline__ float max3f(float x, float y, float z) {
-  float r;
-  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(x), "f"(y), "f"(z));
-  return r;
-}
-
-__device__ __forceinline__ float min3f(float x, float y, float z) {
-  float r;
-  asm("min.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(x), "f"(y), "f"(z));
-  return r;
-}
-
-// (y0, y1) = (x0, x1) * s + c, one packed fp32 instruction.
-__device__ __forceinline__ void fma2(float &y0, float &y1, float x0, float x1, float s, float c) {
-  asm("{\n .reg .b64 x, m, a, y;\n mov.b64 x, {%2, %3};\n mov.b64 m, {%4, %4};\n"
-      " mov.b64 a, {%5, %5};\n fma.rn.f32x2 y, x, m, a;\n mov.b64 {%0, %1}, y;\n}"
-      : "=f"(y0), "=f"(y1)
-      : "f"(x0), "f"(x1), "f"(s), "f"(c));
-}
-
-// (s0, s1) += (x0, x1), one packed fp32 instruction.
-__device__ __forceinline__ void add2(float &s0, float &s1, float x0, float x1) {
-  asm("{\n .reg .b64 s, x;\n mov.b64 s, {%0, %1};\n mov.b64 x, {%2, %3};\n"
-      " add.rn.f32x2 s, s, x;\n mov.b64 {%0, %1}, s;\n}"
-      : "+f"(s0), "+f"(s1)
-      : "f"(x0), "f"(x1));
-}
-
 // kv_map: the workspace as a 2-D bf16 tensor [2 * batch * Hkv * s_pad rows][D],
 // box {64, 128}; q_map: q as [total_q * Hq rows][D], box {64, 1}. Both with
 // 128-byte swizzle.
@@ -541,6 +512,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(kBarOFull), 1);
     mbar_init(bar(kBarTeardown), 1);
     mbar_init(bar(kBarQFull), 1);
+    mbar_init(bar(kBarQReady), kSoftmaxWarps * 32);
     mbar_init_fence();
   }
   if (warp == kMmaWarp) tmem_alloc(smem_addr(&s_tmem), kTmemCols);
@@ -647,7 +619,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                        dv + ks * (2048 >> 4), idesc_pv, (j > 0 || ks > 0) ? 1u : 0u);
         return true;
       };
-      bool ok = mbar_wait_fast(bar(kBarQFull), 0, abort) && mbar_wait_fast(bar(kBarFull), 0, abort);
+      bool ok = mbar_wait_fast(bar(a.q_mode ? kBarQReady : kBarQFull), 0, abort) &&
+                mbar_wait_fast(bar(kBarFull), 0, abort);
       if (ok) {
         tc_fence_after_sync();
         qk(0, 0);
@@ -693,11 +666,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t orow_t = tmem + lane_base + kTmemO + x * D;
     float m_used = -INFINITY, l = 0.f;
     bool ok = true;
-    // Sign of the softmax scale (any finite value is allowed): the largest
-    // scaled score scale * s comes from the largest raw score s when scale
-    // >= 0 and from the smallest when scale < 0. Grid-uniform.
-    const bool neg = a.scale_log2 < 0.f;
-    for (int j = 0; j < n_x; ++j) {
+    if (a.q_mode != 0) {
+      // Fold the softmax scale's sign into Q once (both query tiles, all
+      // eight softmax warps), before the first S = Q K^T is issued.
+      ok = mbar_wait_warp(bar(kBarQFull), 0, abort);
+      if (ok) {
+        uint4 *qs = reinterpret_cast<uint4 *>(smem + S::kQ);
+        const uint32_t flip = 0x80008000u;  // the sign bits of a bf16 pair
+        for (int i = tid; i < kQTiles * S::kQBytes / 16; i += kSoftmaxWarps * 32) {
+          uint4 w = qs[i];
+          if (a.q_mode == 1) {
+            w.x ^= flip;
+            w.y ^= flip;
+            w.z ^= flip;
+            w.w ^= flip;
+          } else {
+            w = make_uint4(0u, 0u, 0u, 0u);
+          }
+          qs[i] = w;
+        }
+        fence_async_shared();  // generic-proxy writes, read next by tcgen05.mma
+      }
+      mbar_arrive(bar(kBarQReady));
+    }
+    for (int j = 0; ok && j < n_x; ++j) {
       if (!(ok = mbar_wait_warp(bar(kBarSFull + x), j & 1, abort))) break;
       tc_fence_after_sync();
       float v[kN];
@@ -707,43 +699,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld32(srow + 96, *reinterpret_cast<float(*)[32]>(&v[96]));
       tmem_ld_wait();
       const int key0 = (tile0 + j) * kN;
-      // The tile crosses some row's last visible key (warp-uniform). Keys past
-      // a row's last one take the raw value that is never its extreme.
-      const bool crosses = key0 + kN - 1 > min_limit;
-      if (crosses) {
-        const float fill = neg ? INFINITY : -INFINITY;
+      if (key0 + kN - 1 > min_limit) {  // tile crosses some row's last key (warp-uniform)
 #pragma unroll
-        for (int cc = 0; cc < kN; ++cc) v[cc] = key0 + cc <= limit ? v[cc] : fill;
+        for (int cc = 0; cc < kN; ++cc) v[cc] = key0 + cc <= limit ? v[cc] : -INFINITY;
       }
-      // Row max of the scaled scores from the raw scores' max (scale >= 0)
-      // or min (scale < 0), four independent chains.
-      float ext;
-      if (!neg) {
-        float mx0 = fmaxf(v[0], v[1]), mx1 = fmaxf(v[2], v[3]);
-        float mx2 = fmaxf(v[4], v[5]), mx3 = fmaxf(v[6], v[7]);
+      // Row max of the raw scores; scale_log2 > 0 commutes with max (a
+      // negative or zero softmax scale was folded into Q, see QMode).
+      float mx0 = fmaxf(v[0], v[1]), mx1 = fmaxf(v[2], v[3]);
+      float mx2 = fmaxf(v[4], v[5]), mx3 = fmaxf(v[6], v[7]);
 #pragma unroll
-        for (int cc = 8; cc < kN; cc += 8) {
-          mx0 = max3f(mx0, v[cc], v[cc + 1]);
-          mx1 = max3f(mx1, v[cc + 2], v[cc + 3]);
-          mx2 = max3f(mx2, v[cc + 4], v[cc + 5]);
-          mx3 = max3f(mx3, v[cc + 6], v[cc + 7]);
-        }
-        ext = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
-      } else {
-        float mn0 = fminf(v[0], v[1]), mn1 = fminf(v[2], v[3]);
-        float mn2 = fminf(v[4], v[5]), mn3 = fminf(v[6], v[7]);
-#pragma unroll
-        for (int cc = 8; cc < kN; cc += 8) {
-          mn0 = min3f(mn0, v[cc], v[cc + 1]);
-          mn1 = min3f(mn1, v[cc + 2], v[cc + 3]);
-          mn2 = min3f(mn2, v[cc + 4], v[cc + 5]);
-          mn3 = min3f(mn3, v[cc + 6], v[cc + 7]);
-        }
-        ext = fminf(fminf(mn0, mn1), fminf(mn2, mn3));
+      for (int cc = 8; cc < kN; cc += 8) {
+        mx0 = max3f(mx0, v[cc], v[cc + 1]);
+        mx1 = max3f(mx1, v[cc + 2], v[cc + 3]);
+        mx2 = max3f(mx2, v[cc + 4], v[cc + 5]);
+        mx3 = max3f(mx3, v[cc + 6], v[cc + 7]);
       }
-      // A row with no visible key in this tile has ext = +-inf and no
-      // maximum (for scale 0 the product would be NaN).
-      const float mt = (crosses && isinf(ext)) ? -INFINITY : ext * a.scale_log2;
+      const float mt = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * a.scale_log2;
       // Lazy rescale: move the reference max only when a row's max grew by
       // more than 2^kRescaleThreshold (warp-uniform: tcgen05.ld/st are
       // .sync.aligned, so every lane takes part, with factor 1 where its
@@ -759,37 +730,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const float nm = m_used == -INFINITY ? 0.f : -m_used;
       float sa0 = 0.f, sa1 = 0.f, sb0 = 0.f, sb1 = 0.f;
-      // P = exp2(scale * s - m) as bf16 pairs into TMEM. On a crossing tile
-      // a masked key's exponent is forced to -inf after the FMA (its fill
-      // times scale is -inf, except for scale 0, where it is NaN).
-      auto exp_to_p = [&](auto masked) {
-        constexpr bool kMasked = decltype(masked)::value;
 #pragma unroll
-        for (int cc = 0; cc < kN; cc += 32) {
-          uint32_t w[16];
+      for (int cc = 0; cc < kN; cc += 32) {
+        uint32_t w[16];
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            float y0, y1;
-            fma2(y0, y1, v[cc + 2 * e], v[cc + 2 * e + 1], a.scale_log2, nm);
-            if (kMasked) {
-              y0 = key0 + cc + 2 * e <= limit ? y0 : -INFINITY;
-              y1 = key0 + cc + 2 * e + 1 <= limit ? y1 : -INFINITY;
-            }
-            y0 = fast_exp2(y0);
-            y1 = fast_exp2(y1);
-            if (e & 1)
-              add2(sb0, sb1, y0, y1);
-            else
-              add2(sa0, sa1, y0, y1);
-            w[e] = pack_bf16(y0, y1);
-          }
-          tmem_st16u(srow + cc / 2, w);  // P_x: keys cc .. cc + 31 -> columns cc/2 ..
+        for (int e = 0; e < 16; ++e) {
+          float y0, y1;
+          fma2(y0, y1, v[cc + 2 * e], v[cc + 2 * e + 1], a.scale_log2, nm);
+          y0 = fast_exp2(y0);
+          y1 = fast_exp2(y1);
+          if (e & 1)
+            add2(sb0, sb1, y0, y1);
+          else
+            add2(sa0, sa1, y0, y1);
+          w[e] = pack_bf16(y0, y1);
         }
-      };
-      if (crosses)
-        exp_to_p(std::true_type{});
-      else
-        exp_to_p(std::false_type{});
+        tmem_st16u(srow + cc / 2, w);  // P_x: keys cc .. cc + 31 -> columns cc/2 ..
+      }
       l = l * f + ((sa0 + sa1) + (sb0 + sb1));
       if (rescale) {
         // O_x is stable: S_x(j) completed, so did PV_x(j - 1) before it.
@@ -981,7 +938,8 @@ cudaError_t launch_extend(const PoolGeom &g, int32_t layer, const void *q,
   a.tokens_per_tile = kM / a.group;
   a.capacity = capacity;
   a.s_pad = static_cast<int32_t>(s_pad);
-  a.scale_log2 = scale * kLog2e;
+  a.q_mode = scale > 0.f ? 0 : (scale < 0.f ? 1 : 2);
+  a.scale_log2 = scale > 0.f ? scale * kLog2e : (scale < 0.f ? -scale * kLog2e : kLog2e);
   a.err = err;
   a.plan = ga.plan;
   a.causal = mode.causal;

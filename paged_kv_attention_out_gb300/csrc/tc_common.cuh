@@ -315,4 +315,34 @@ __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, vo
   return __all_sync(0xffffffffu, ok);
 }
 
+// Softmax arithmetic of the tcgen05 attention kernels (one query row per
+// thread, log2 domain).
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ float max3f(float x, float y, float z) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(x), "f"(y), "f"(z));
+  return r;
+}
+
+// (y0, y1) = (x0, x1) * s + c, one packed fp32 instruction.
+__device__ __forceinline__ void fma2(float &y0, float &y1, float x0, float x1, float s, float c) {
+  asm("{\n .reg .b64 x, m, a, y;\n mov.b64 x, {%2, %3};\n mov.b64 m, {%4, %4};\n"
+      " mov.b64 a, {%5, %5};\n fma.rn.f32x2 y, x, m, a;\n mov.b64 {%0, %1}, y;\n}"
+      : "=f"(y0), "=f"(y1)
+      : "f"(x0), "f"(x1), "f"(s), "f"(c));
+}
+
+// (s0, s1) += (x0, x1), one packed fp32 instruction.
+__device__ __forceinline__ void add2(float &s0, float &s1, float x0, float x1) {
+  asm("{\n .reg .b64 s, x;\n mov.b64 s, {%0, %1};\n mov.b64 x, {%2, %3};\n"
+      " add.rn.f32x2 s, s, x;\n mov.b64 {%0, %1}, s;\n}"
+      : "+f"(s0), "+f"(s1)
+      : "f"(x0), "f"(x1));
+}
+
 }  // namespace pkv
