@@ -17,7 +17,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libpkv.so")
-SOURCES = ["pkv_api.cu", "kv_store.cu", "decode.cu", "extend.cu", "merge.cu",
+SOURCES = ["pkv_api.cu", "kv_store.cu", "decode.cu", "extend.cu", "cascade.cu", "merge.cu",
            "decode_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -43,17 +43,28 @@ namespace {
 
 constexpr int kM = 128;  // query rows per CTA (= TMEM lanes)
 constexpr int kN = 128;  // keys per K/V tile
-constexpr int kStages = 3;
+#ifndef PKV_PREFIX_STAGES
+#define PKV_PREFIX_STAGES 3
+#endif
+constexpr int kStages = PKV_PREFIX_STAGES;
 constexpr int kSoftmaxWarps = 4;
 constexpr int kMmaWarp = kSoftmaxWarps;
 constexpr int kProducerWarp0 = kSoftmaxWarps + 1;
-constexpr int kProducerWarps = 4;
+#ifndef PKV_PREFIX_PRODUCER_WARPS
+#define PKV_PREFIX_PRODUCER_WARPS 4
+#endif
+constexpr int kProducerWarps = PKV_PREFIX_PRODUCER_WARPS;
+constexpr int kKeysPerWarp = kN / kProducerWarps;  // keys of a tile one producer warp copies
+static_assert(kKeysPerWarp * kProducerWarps == kN && kKeysPerWarp <= 32, "producer split");
 constexpr int kProducerThreads = kProducerWarps * 32;
 constexpr int kThreads = (kSoftmaxWarps + 1 + kProducerWarps) * 32;
 constexpr uint32_t kTmemCols = 256;  // S / P at columns 0 .. 127, O at 128 .. 128 + D - 1
 constexpr uint32_t kTmemS = 0;
 constexpr uint32_t kTmemO = 128;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
+#ifndef PKV_PREFIX_MAX_SPLITS
+#define PKV_PREFIX_MAX_SPLITS 64  // key ranges per group at most
+#endif
 
 template <int D>
 struct PrefixSmem {
@@ -103,19 +114,27 @@ struct PrefixArgs {
   unsigned *err;
 };
 
-// The (group, first member) of block `rank`: groups in order, each cut into
-// blocks of members_per_tile members. One warp; writes *group = -1 past the
-// last block. A group whose member_indptr pair is malformed has no block.
-__device__ void locate_block(const PrefixArgs &a, int rank, bool report, int *group, int *m0) {
+// Block `rank` of the grid's y dimension: groups in order, each cut into
+// blocks of members_per_tile members. One warp; returns the group (-1 past
+// the last block), the block's first member index into `members`, the
+// group's member end and its prefix length, all from one round of loads. A
+// group whose member_indptr pair is malformed has no block.
+struct BlockInfo {
+  int group, first, end, plen;
+};
+
+__device__ BlockInfo locate_block(const PrefixArgs &a, int rank, bool report) {
   const int lane = threadIdx.x & 31;
   const int mpt = a.members_per_tile;
   int base = 0;
-  int found = -1, first = 0;
+  BlockInfo out{-1, 0, 0, 0};
   for (int k0 = 0; k0 < a.num_groups; k0 += 32) {
     const int k = k0 + lane;
-    int nb = 0;
+    int nb = 0, beg = 0, end = 0, plen = 0;
     if (k < a.num_groups) {
-      const int beg = a.member_indptr[k], end = a.member_indptr[k + 1];
+      beg = a.member_indptr[k];
+      end = a.member_indptr[k + 1];
+      plen = a.prefix_lens[k];
       if (beg < 0 || end < beg || end > a.batch) {
         if (report) flag_error(a.err, kErrIndptr);
       } else {
@@ -133,14 +152,15 @@ __device__ void locate_block(const PrefixArgs &a, int rank, bool report, int *gr
       const unsigned who = __ballot_sync(0xffffffffu, rank >= base + inc - nb && rank < base + inc);
       const int src = __ffs(who) - 1;
       const int start = __shfl_sync(0xffffffffu, base + inc - nb, src);
-      found = k0 + src;
-      first = (rank - start) * mpt;
+      out.group = k0 + src;
+      out.first = __shfl_sync(0xffffffffu, beg, src) + (rank - start) * mpt;
+      out.end = __shfl_sync(0xffffffffu, end, src);
+      out.plen = __shfl_sync(0xffffffffu, plen, src);
       break;
     }
     base += total;
   }
-  *group = found;
-  *m0 = first;
+  return out;
 }
 
 template <int D>
@@ -148,7 +168,8 @@ __global__ void __launch_bounds__(kThreads, 1) cascade_prefix_kernel(const Prefi
   using S = PrefixSmem<D>;
   constexpr int kChunks = D / 8;  // 16-byte chunks per row
   extern __shared__ uint8_t smem_raw[];
-  __shared__ int s_group, s_m0;
+  __shared__ BlockInfo s_blk;
+  __shared__ int64_t s_qrow[kM];  // q_row() of every query row (producers)
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
   const int tid = threadIdx.x;
@@ -162,20 +183,18 @@ __global__ void __launch_bounds__(kThreads, 1) cascade_prefix_kernel(const Prefi
   grid_dependency_wait();
   grid_dependents_launch();
   if (warp == 0) {
-    int k, m0;
-    locate_block(a, blockIdx.y, blockIdx.x == 0 && blockIdx.z == 0, &k, &m0);
+    const BlockInfo bi = locate_block(a, blockIdx.y, blockIdx.x == 0 && blockIdx.z == 0);
     if (lane == 0) {
-      s_group = k;
-      s_m0 = m0;
+      s_blk = bi;
       s_abort = 0;
     }
   }
   __syncthreads();
-  const int k = s_group;
+  const int k = s_blk.group;
   if (k < 0) return;
-  const int beg = a.member_indptr[k] + s_m0;
-  const int nm = min(a.members_per_tile, a.member_indptr[k + 1] - beg);  // members in the tile
-  int plen = a.prefix_lens[k];
+  const int beg = s_blk.first;                             // first member of the tile
+  const int nm = min(a.members_per_tile, s_blk.end - beg);  // members in the tile
+  int plen = s_blk.plen;
   const bool report = kvh == 0 && z == 0 && tid == 0;
   if (plen < 0 || plen > a.prefix_stride * a.page_size) {
     if (report) flag_error(a.err, kErrSeqLen);
@@ -189,14 +208,16 @@ __global__ void __launch_bounds__(kThreads, 1) cascade_prefix_kernel(const Prefi
   const int32_t *prow = a.prefix_table + static_cast<int64_t>(k) * a.prefix_stride;
 
   // Query row r of the tile: member r / g, q head kvh * g + r % g; the row of
-  // q and of the partial state, or -1 for a padding row.
+  // q and of the partial state, -1 for a padding row, -2 for a member index
+  // outside the batch (skipped and flagged).
   auto q_row = [&](int r) -> int64_t {
     const int m = r / a.group;
     if (m >= a.members_per_tile || m >= nm) return -1;
     const int b = a.members[beg + m];
-    if (b < 0 || b >= a.batch) return -1;
+    if (b < 0 || b >= a.batch) return -2;
     return static_cast<int64_t>(b) * a.hq + kvh * a.group + r % a.group;
   };
+  if (warp < kSoftmaxWarps && z == 0 && q_row(tid) == -2) flag_error(a.err, kErrIndptr);
 
   if (n_tiles == 0) {  // no key in this range: o = 0, lse = -inf
     if (warp < kSoftmaxWarps) {
@@ -238,27 +259,19 @@ __global__ void __launch_bounds__(kThreads, 1) cascade_prefix_kernel(const Prefi
 
   if (warp >= kProducerWarp0) {
     // ------------------------------------------------------------ producers
-    const int pt = tid - kProducerWarp0 * 32;  // 0 .. 127
-    const int pw = pt >> 5;                    // producer warp: keys 32 pw .. 32 pw + 31 of a tile
+    const int pt = tid - kProducerWarp0 * 32;
+    const int pw = pt >> 5;  // producer warp: keys kKeysPerWarp pw .. + kKeysPerWarp - 1 of a tile
     bool ok = true;
-    // Q: 128 rows x kChunks chunks; consecutive threads take consecutive
-    // chunks of a row (coalesced 16-byte pieces).
-    for (int c = pt; c < kM * kChunks; c += kProducerThreads) {
-      const int r = c / kChunks, ch = c % kChunks;
-      const int64_t qr = q_row(r);
-      cp_async_16(sbase + S::kQ + sw128_offset(kM, r, ch * 8),
-                  qr >= 0 ? a.q + qr * D + ch * 8 : a.q, qr >= 0 ? 16 : 0);
-    }
-    cp_async_commit();
-    // The slot of this thread's key of tile j (thread pt holds key pt), -1
-    // past the prefix or for a bad page id.
     const int64_t row_elems = static_cast<int64_t>(a.hkv) * D;
     const __nv_bfloat16 *kbase =
         a.pool + static_cast<int64_t>(a.layer) * a.slots * row_elems + kvh * D;
     const __nv_bfloat16 *vbase =
         a.pool + (static_cast<int64_t>(a.num_layers) + a.layer) * a.slots * row_elems + kvh * D;
-    auto key_slot = [&](int j) -> long long {
-      const int key = (tile0 + j) * kN + pt;
+    // The slot of this lane's key of tile j (lane l of warp pw holds key
+    // kKeysPerWarp pw + l % kKeysPerWarp), -1 past the prefix or for a bad
+    // page id.
+    auto key_slot_of = [&](int j) -> long long {
+      const int key = (tile0 + j) * kN + pw * kKeysPerWarp + lane % kKeysPerWarp;
       if (key >= plen) return -1;
       const int pidx = key / a.page_size;
       const int ent = __ldg(prow + pidx);
@@ -269,9 +282,23 @@ __global__ void __launch_bounds__(kThreads, 1) cascade_prefix_kernel(const Prefi
       }
       return s;
     };
+    // The first tile's page entries and the rows' member ids are loaded
+    // together, before any copy is issued (each copy's asm is a compiler
+    // barrier, so loads placed between copies would run one after another).
+    long long slot = key_slot_of(0);
+    for (int r = pt; r < kM; r += kProducerThreads) s_qrow[r] = q_row(r);
+    named_barrier_sync(1, kProducerThreads);
+    // Q: 128 rows x kChunks chunks; consecutive threads take consecutive
+    // chunks of a row (coalesced 16-byte pieces).
+    for (int c = pt; c < kM * kChunks; c += kProducerThreads) {
+      const int r = c / kChunks, ch = c % kChunks;
+      const int64_t qr = s_qrow[r];
+      cp_async_16(sbase + S::kQ + sw128_offset(kM, r, ch * 8),
+                  qr >= 0 ? a.q + qr * D + ch * 8 : a.q, qr >= 0 ? 16 : 0);
+    }
+    cp_async_commit();
     constexpr int kKeysPerInstr = 32 / kChunks;  // keys one warp instruction covers
     const int ch = lane % kChunks;
-    long long slot = key_slot(0);
     int issued = 0;
     for (int j = 0; j < n_tiles; ++j) {
       const int s = j % kStages;
@@ -280,10 +307,10 @@ __global__ void __launch_bounds__(kThreads, 1) cascade_prefix_kernel(const Prefi
         break;
       const uint32_t kst = sbase + S::kKV + s * 2 * S::kTileBytes;
 #pragma unroll
-      for (int it = 0; it < 32 / kKeysPerInstr; ++it) {
-        const int kl = it * kKeysPerInstr + lane / kChunks;  // key within this warp's 32
+      for (int it = 0; it < kKeysPerWarp / kKeysPerInstr; ++it) {
+        const int kl = it * kKeysPerInstr + lane / kChunks;  // key within this warp's share
         const long long sl = __shfl_sync(0xffffffffu, slot, kl);
-        const int kk = pw * 32 + kl;  // key within the tile
+        const int kk = pw * kKeysPerWarp + kl;  // key within the tile
         const bool kv_ok = sl >= 0;
         const int64_t off = kv_ok ? sl * row_elems + ch * 8 : 0;
         const uint32_t dst = kst + sw128_offset(kN, kk, ch * 8);
@@ -292,7 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1) cascade_prefix_kernel(const Prefi
       }
       cp_async_commit();
       ++issued;
-      if (j + 1 < n_tiles) slot = key_slot(j + 1);  // next tile's page entry, off the copy path
+      if (j + 1 < n_tiles) slot = key_slot_of(j + 1);  // next tile's page entry, off the copy path
       // The previous group (Q, or tile j - 1) has landed: hand it over.
       cp_async_wait<1>();
       fence_async_shared();
@@ -468,23 +495,39 @@ __global__ void __launch_bounds__(kThreads, 1) cascade_prefix_kernel(const Prefi
       *abort = 1;
       flag_error(a.err, kErrTimeout);
     } else {
+      // O / l through shared memory (the K/V stages are free: every MMA is
+      // done), so that each store instruction writes whole rows of the
+      // partial state instead of 16 bytes of 32 different rows.
       tc_fence_after_sync();
       const float inv = l > 0.f ? 1.f / l : 0.f;
-      const int64_t prow_o = (bh >= 0 ? bh : 0) * a.pstride + a.pslot + z;
+      constexpr int kStride = D + 4;  // floats per staged row (16-byte skew: no bank conflicts)
+      float *stage = reinterpret_cast<float *>(smem + S::kKV) + warp * 32 * kStride;
 #pragma unroll 1
       for (int cb = 0; cb < D / 32; ++cb) {
         float o[32];
         tmem_ld32(orow_t + cb * 32, o);
         tmem_ld_wait();
-        if (bh >= 0) {
-          float4 *dst = reinterpret_cast<float4 *>(a.part_o + prow_o * D + cb * 32);
 #pragma unroll
-          for (int q4 = 0; q4 < 8; ++q4)
-            dst[q4] = make_float4(o[q4 * 4] * inv, o[q4 * 4 + 1] * inv, o[q4 * 4 + 2] * inv,
-                                  o[q4 * 4 + 3] * inv);
+        for (int q4 = 0; q4 < 8; ++q4)
+          *reinterpret_cast<float4 *>(stage + lane * kStride + cb * 32 + q4 * 4) =
+              make_float4(o[q4 * 4] * inv, o[q4 * 4 + 1] * inv, o[q4 * 4 + 2] * inv,
+                          o[q4 * 4 + 3] * inv);
+      }
+      __syncwarp();
+      constexpr int kLanesPerRow = D / 4;  // one float4 per lane
+      constexpr int kRowsPerStore = 32 / kLanesPerRow;
+      for (int rr0 = 0; rr0 < 32; rr0 += kRowsPerStore) {
+        const int rr = rr0 + lane / kLanesPerRow;  // row of this warp
+        const int64_t rbh = __shfl_sync(0xffffffffu, bh, rr);
+        if (rbh >= 0) {
+          const int c4 = (lane % kLanesPerRow) * 4;
+          *reinterpret_cast<float4 *>(a.part_o + (rbh * a.pstride + a.pslot + z) * D + c4) =
+              *reinterpret_cast<const float4 *>(stage + rr * kStride + c4);
         }
       }
-      if (bh >= 0) a.part_lse[prow_o] = l > 0.f ? (m_used + __log2f(l)) * kLn2 : -INFINITY;
+      if (bh >= 0)
+        a.part_lse[bh * a.pstride + a.pslot + z] =
+            l > 0.f ? (m_used + __log2f(l)) * kLn2 : -INFINITY;
     }
   }
 
@@ -516,17 +559,26 @@ cudaError_t launch_prefix(const PrefixArgs &a, dim3 grid, cudaStream_t stream) {
 }  // namespace
 
 int32_t cascade_prefix_splits(int32_t batch, int32_t hq, int32_t hkv, int32_t num_groups,
-                              int32_t max_prefix, int32_t sm_count) {
-  // As many key ranges as keep the (block, kv head, key range) CTAs within
-  // one wave (one CTA per SM), each range at least two key tiles long.
+                              int32_t max_prefix, int32_t max_suffix, int32_t sm_count) {
+  // The prefix CTAs (one per SM) and the suffix decode's CTAs share the GPU
+  // and both are bound by the bytes they gather, so the prefix gets about its
+  // share of the bytes in SMs: key ranges per (member block, kv head) =
+  // SMs x prefix / (prefix + suffix) / CTAs, from the host bounds, at least
+  // one, at most one wave, each range at least two key tiles long.
   const int64_t mpt = kM / (hq / hkv);
   int64_t blocks = (static_cast<int64_t>(batch) + mpt - 1) / mpt;
   if (blocks < num_groups) blocks = num_groups;
   const int64_t ctas = static_cast<int64_t>(hkv) * (blocks > 0 ? blocks : 1);
-  const int64_t want = static_cast<int64_t>(sm_count > 0 ? sm_count : 1) / ctas;
+  const int64_t sms = sm_count > 0 ? sm_count : 1;
+  const double pre = static_cast<double>(num_groups) * (max_prefix > 0 ? max_prefix : 0);
+  const double suf = static_cast<double>(batch) * (max_suffix > 1 ? max_suffix : 1);
+  int64_t ks = static_cast<int64_t>(static_cast<double>(sms) * pre / (pre + suf) /
+                                    static_cast<double>(ctas) + 0.5);
+  const int64_t wave = sms / ctas;
   const int64_t nk = (static_cast<int64_t>(max_prefix > 0 ? max_prefix : 0) + kN - 1) / kN;
-  int64_t ks = want < nk / 2 ? want : nk / 2;
-  if (ks > 64) ks = 64;
+  if (ks > wave) ks = wave;
+  if (ks > nk / 2) ks = nk / 2;
+  if (ks > PKV_PREFIX_MAX_SPLITS) ks = PKV_PREFIX_MAX_SPLITS;
   return static_cast<int32_t>(ks < 1 ? 1 : ks);
 }
 

@@ -45,6 +45,9 @@ namespace {
 #ifndef PKV_DECODE_MIN_SPLIT_TILES
 #define PKV_DECODE_MIN_SPLIT_TILES 8  // smallest split, in 16-key tiles
 #endif
+#ifndef PKV_MERGE_BATCH
+#define PKV_MERGE_BATCH 16  // partial rows the merge loads in its first round trip
+#endif
 
 constexpr int kWarps = PKV_DECODE_WARPS;
 constexpr int kThreads = kWarps * 32;
@@ -96,6 +99,11 @@ struct DecodeArgs {
   const __nv_bfloat16 *v_new;
   int64_t kv_row_stride;
   __nv_bfloat16 *pool_w;
+  // Cascade suffix: the previous kernel on the stream (the shared-prefix
+  // attention) writes nothing this kernel reads, so the CTAs do not wait for
+  // it at entry; the split-0 CTAs of the last request wait for it at exit,
+  // so this grid still completes after it (and the merge after both).
+  int32_t defer_wait;
 };
 
 __device__ __forceinline__ float fast_exp2(float x) {
@@ -145,7 +153,7 @@ __global__ void __launch_bounds__(kThreads, (kStages <= 3 ? 2 : 1)) decode_kerne
   const int split = blockIdx.y;
   const int b = blockIdx.z;
 
-  grid_dependency_wait();    // inputs may come from the previous kernel (store_kv)
+  if (!a.defer_wait) grid_dependency_wait();  // inputs may come from the previous kernel (store_kv)
   grid_dependents_launch();  // the split merge may be scheduled as CTAs drain
   const RowInfo ri = row_info(a, b, split == 0 && blockIdx.x == 0 && threadIdx.x == 0);
   if (split >= ri.nsplit) return;
@@ -409,6 +417,7 @@ __global__ void __launch_bounds__(kThreads, (kStages <= 3 ? 2 : 1)) decode_kerne
       if (d4 == 0) a.part_lse[bh * a.pstride + split] = lse_nat;
     }
   }
+  if (a.defer_wait && split == 0 && b == static_cast<int>(gridDim.z) - 1) grid_dependency_wait();
 }
 
 // Cross-split merge: one warp per (request, q head) with more than one
@@ -416,18 +425,36 @@ __global__ void __launch_bounds__(kThreads, (kStages <= 3 ? 2 : 1)) decode_kerne
 // every (request, q head) merges its suffix splits with those. Lane s holds
 // the lse of state s; the partial rows of up to kMergeBatch states are
 // loaded together with the lse values, so the common case costs one
-// round trip to L2 after the decode grid completes.
-constexpr int kMergeBatch = 16;
+// round trip to L2 after the decode grid completes. The grid holds at most
+// one wave of CTAs; a warp takes (request, q head) pairs warp-stride.
+constexpr int kMergeBatch = PKV_MERGE_BATCH;
+constexpr int kMergeThreads = 128;
+#ifndef PKV_MERGE_CTAS_PER_SM
+#define PKV_MERGE_CTAS_PER_SM 16  // resident merge CTAs per SM the grid is sized for
+#endif
+
 
 template <int D>
-__global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs a, int32_t batch) {
+__device__ __forceinline__ void merge_pair(const DecodeArgs &a, int64_t bh, int lane);
+
+template <int D>
+__global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const DecodeArgs a, int32_t batch) {
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int64_t bh = static_cast<int64_t>(blockIdx.x) * 4 + warp;
-  if (bh >= static_cast<int64_t>(batch) * a.hq) return;
-  const int b = static_cast<int>(bh / a.hq);
+  const int64_t pairs = static_cast<int64_t>(batch) * a.hq;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * (kMergeThreads / 32);
+  int64_t bh = static_cast<int64_t>(blockIdx.x) * (kMergeThreads / 32) + warp;
   // seq_lens and table_idx are inputs of the call (complete before any
-  // decode CTA passed its own dependency wait), so they are read before ours.
+  // decode CTA passed its own dependency wait): the first pair's are read
+  // before the wait.
+  if (bh < pairs) (void)row_info(a, static_cast<int>(bh / a.hq), false);
+  grid_dependency_wait();  // the partial states come from decode_kernel
+  for (; bh < pairs; bh += stride) merge_pair<D>(a, bh, lane);
+}
+
+template <int D>
+__device__ __forceinline__ void merge_pair(const DecodeArgs &a, int64_t bh, int lane) {
+  const int b = static_cast<int>(bh / a.hq);
   const RowInfo ri = row_info(a, b, false);
   const int n = ri.nsplit;
   if (n <= 1 && !a.force_partial) return;
@@ -438,7 +465,6 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs a, i
   const float *pl = a.part_lse + bh * a.pstride;
   const float *po = a.part_o + bh * a.pstride * D + lane * 4;
   auto slot = [&](int st) { return st < n ? st : a.splits + (st - n); };
-  grid_dependency_wait();  // the partial states come from decode_kernel
   const bool row_lane = lane < D / 4;
   float4 v[kMergeBatch];
 #pragma unroll
@@ -504,10 +530,28 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs a, i
 
 }  // namespace
 
+static DecodePlan plan_splits(int32_t batch, int32_t hq, int32_t hkv, int32_t d,
+                              int32_t max_seq_len, int32_t sm_count, int32_t units_per_sm);
+
 DecodePlan plan_decode(int32_t batch, int32_t hq, int32_t hkv, int32_t d, int32_t max_seq_len,
                        int32_t sm_count) {
+  return plan_splits(batch, hq, hkv, d, max_seq_len, sm_count, PKV_DECODE_UNITS_PER_SM);
+}
+
+#ifndef PKV_CASCADE_UNITS_PER_SM
+#define PKV_CASCADE_UNITS_PER_SM PKV_DECODE_UNITS_PER_SM
+#endif
+
+DecodePlan plan_cascade_suffix(int32_t batch, int32_t hq, int32_t hkv, int32_t d,
+                               int32_t max_seq_len, int32_t sm_count) {
+  return plan_splits(batch, hq, hkv, d, max_seq_len, sm_count, PKV_CASCADE_UNITS_PER_SM);
+}
+
+static DecodePlan plan_splits(int32_t batch, int32_t hq, int32_t hkv, int32_t d,
+                              int32_t max_seq_len, int32_t sm_count, int32_t units_per_sm) {
   (void)hq;
   DecodePlan p{};
+  p.sm_count = sm_count;
   p.heads_per_cta = hkv >= kWarps ? kWarps : hkv;
   p.warps_per_head = kWarps / p.heads_per_cta;
   p.head_groups = hkv / p.heads_per_cta;
@@ -517,7 +561,7 @@ DecodePlan plan_decode(int32_t batch, int32_t hq, int32_t hkv, int32_t d, int32_
   // request were max_seq long, with at least PKV_DECODE_MIN_SPLIT_TILES tiles
   // per split so partial states stay a few percent of the KV bytes.
   const int64_t units = static_cast<int64_t>(batch) * p.head_groups * tiles;
-  const int64_t target = static_cast<int64_t>(sm_count > 0 ? sm_count : 1) * PKV_DECODE_UNITS_PER_SM;
+  const int64_t target = static_cast<int64_t>(sm_count > 0 ? sm_count : 1) * units_per_sm;
   int64_t chunk_tiles = (units + target - 1) / target;
   if (chunk_tiles < PKV_DECODE_MIN_SPLIT_TILES) chunk_tiles = PKV_DECODE_MIN_SPLIT_TILES;
   int64_t splits = (tiles + chunk_tiles - 1) / chunk_tiles;
@@ -589,9 +633,12 @@ static cudaError_t launch_decode_main(const DecodeArgs &a, const PoolGeom &g,
 }
 
 static cudaError_t launch_decode_merge(const DecodeArgs &a, const PoolGeom &g, int32_t batch,
-                                       cudaStream_t stream) {
+                                       int32_t sm_count, cudaStream_t stream) {
   const int64_t pairs = static_cast<int64_t>(batch) * a.hq;
-  const dim3 mgrid(static_cast<unsigned>((pairs + 3) / 4));
+  int64_t ctas = (pairs + 3) / 4;
+  const int64_t wave = static_cast<int64_t>(sm_count > 0 ? sm_count : 1) * PKV_MERGE_CTAS_PER_SM;
+  if (ctas > wave) ctas = wave;
+  const dim3 mgrid(static_cast<unsigned>(ctas));
   if (g.d == 128) return launch_pdl(decode_merge_kernel<128>, mgrid, dim3(128), 0, stream, a, batch);
   return launch_pdl(decode_merge_kernel<64>, mgrid, dim3(128), 0, stream, a, batch);
 }
@@ -617,13 +664,21 @@ cudaError_t launch_decode(const PoolGeom &g, int32_t layer, const void *q, void 
   }
   cudaError_t e = launch_decode_main(a, g, plan, batch, stream);
   if (e != cudaSuccess || plan.splits <= 1) return e;
-  return launch_decode_merge(a, g, batch, stream);
+  return launch_decode_merge(a, g, batch, plan.sm_count, stream);
 }
 
 size_t cascade_partial_bytes(int32_t batch, int32_t hq, int32_t d, int32_t slots) {
   const size_t rows = static_cast<size_t>(batch) * hq * static_cast<size_t>(slots);
   return ((rows * d * sizeof(float) + 255) & ~size_t(255)) +
          ((rows * sizeof(float) + 255) & ~size_t(255));
+}
+
+void cascade_partial_ptrs(void *partials, int32_t batch, int32_t hq, int32_t d, int32_t slots,
+                          float **part_o, float **part_lse) {
+  const size_t rows = static_cast<size_t>(batch) * hq * static_cast<size_t>(slots);
+  *part_o = static_cast<float *>(partials);
+  *part_lse = reinterpret_cast<float *>(static_cast<uint8_t *>(partials) +
+                                        ((rows * d * sizeof(float) + 255) & ~size_t(255)));
 }
 
 cudaError_t launch_cascade_suffix(const PoolGeom &g, int32_t layer, const void *q, void *o,
@@ -634,13 +689,10 @@ cudaError_t launch_cascade_suffix(const PoolGeom &g, int32_t layer, const void *
                                   cudaStream_t stream, float **part_o, float **part_lse) {
   DecodeArgs a = decode_args(g, layer, q, o, lse, page_table, table_stride, table_idx, seq_lens,
                              hq, scale, plan, err);
-  const size_t rows =
-      static_cast<size_t>(batch) * hq * (static_cast<size_t>(plan.splits) + prefix_slots);
   a.pstride = plan.splits + prefix_slots;
   a.force_partial = 1;
-  a.part_o = static_cast<float *>(partials);
-  a.part_lse = reinterpret_cast<float *>(static_cast<uint8_t *>(partials) +
-                                         ((rows * g.d * sizeof(float) + 255) & ~size_t(255)));
+  a.defer_wait = 1;
+  cascade_partial_ptrs(partials, batch, hq, g.d, a.pstride, &a.part_o, &a.part_lse);
   *part_o = a.part_o;
   *part_lse = a.part_lse;
   return launch_decode_main(a, g, plan, batch, stream);
@@ -658,7 +710,7 @@ cudaError_t launch_cascade_merge(const PoolGeom &g, int32_t layer, const void *q
   a.force_partial = 1;
   a.part_o = part_o;
   a.part_lse = part_lse;
-  return launch_decode_merge(a, g, batch, stream);
+  return launch_decode_merge(a, g, batch, plan.sm_count, stream);
 }
 
 }  // namespace pkv

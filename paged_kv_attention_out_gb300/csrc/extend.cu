@@ -117,7 +117,6 @@ struct GatherArgs {
   const int32_t *qo_indptr;
   int32_t total_q;
   int32_t tokens_per_tile;
-  int32_t causal;  // 0: every query of request r sees all seq_lens[r] keys
   int32_t *plan;
   // Fused store (k_new != nullptr): the chunk's keys p_r .. seq_r - 1 are
   // taken from rows qo_indptr[r] .. of k_new / v_new and also written into
@@ -126,10 +125,6 @@ struct GatherArgs {
   const __nv_bfloat16 *v_new;
   int64_t kv_row_stride;
   __nv_bfloat16 *pool_w;
-  // Nothing read here comes from the previous kernel on the stream (the
-  // cascade's suffix decode): wait for it only at exit, so this grid runs
-  // beside its tail and still completes after it.
-  int32_t defer_wait;
 };
 
 struct ExtendArgs {
@@ -153,24 +148,7 @@ struct ExtendArgs {
   int32_t q_mode;
   unsigned *err;
   const int32_t *plan;
-  // query source and result sink (see ExtendMode)
-  int32_t causal;
-  const int32_t *members;
-  float *part_o;
-  float *part_lse;
-  int32_t pstride;
-  int32_t pslot;
-  int32_t key_splits;  // non-causal: blockIdx.z takes key tiles of range z of this many
 };
-
-// Query token (row of q / o, before the head index) of chunk token `tok` of
-// the CTA's block: the next rows of q for extend, the member request for the
-// shared-prefix attention of a cascade (-1 if that index is out of range).
-__device__ __forceinline__ int query_token(const ExtendArgs &a, int t_base, int j0, int tok) {
-  if (!a.members) return t_base + j0 + tok;
-  const int b = a.members[t_base + j0 + tok];
-  return (b >= 0 && b < a.total_q) ? b : -1;
-}
 
 constexpr int kGatherKeys = 16;     // keys per gather CTA (two per warp)
 constexpr int kGatherThreads = 256;
@@ -226,7 +204,7 @@ __device__ void plan_blocks(const GatherArgs &a) {
     if (r < nreq) {
       c = a.qo_indptr[r + 1] - a.qo_indptr[r];
       const int seq = a.seq_lens[r];
-      p = a.causal ? seq - c : seq;  // causal: the cached prefix; else the keys every query sees
+      p = seq - c;  // the cached prefix
       if (p < 0) {
         flag_error(a.err, kErrIndptr);
       } else if (seq <= a.capacity) {  // above capacity: flagged by the gather
@@ -247,10 +225,8 @@ __device__ void plan_blocks(const GatherArgs &a) {
       const int tokens = min(per, c - j0);
       const int tok0 = min(a.tokens_per_tile, tokens);
       const int tok1 = max(0, tokens - a.tokens_per_tile);
-      const int n0 = a.causal ? (p + j0 + tok0 + 127) / 128 : (p + 127) / 128;
-      const int n1 = tok1 == 0 ? 0
-                     : a.causal ? (p + j0 + a.tokens_per_tile + tok1 + 127) / 128
-                                : (p + 127) / 128;
+      const int n0 = (p + j0 + tok0 + 127) / 128;
+      const int n1 = tok1 == 0 ? 0 : (p + j0 + a.tokens_per_tile + tok1 + 127) / 128;
       const int cost = min(n0 + n1 + 2, nbuck - 1);
       const int b = first + i;
       ent[3 * b] = r;
@@ -304,11 +280,9 @@ __device__ __forceinline__ void gather_body(const GatherArgs &a);
 template <int D, bool kStore>
 __global__ void __launch_bounds__(kGatherThreads)
     extend_gather_kernel(const GatherArgs a) {
-  // the chunk's K/V may come from the previous kernel (store_kv)
-  if (!a.defer_wait) grid_dependency_wait();
+  grid_dependency_wait();  // the chunk's K/V may come from the previous kernel (store_kv)
   grid_dependents_launch();
   gather_body<D, kStore>(a);
-  if (a.defer_wait) grid_dependency_wait();
 }
 
 template <int D, bool kStore>
@@ -439,7 +413,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       req = sorted[2 * rank];
       j0 = sorted[2 * rank + 1];
       c = a.qo_indptr[req + 1] - a.qo_indptr[req];
-      p = a.causal ? a.seq_lens[req] - c : a.seq_lens[req];
+      p = a.seq_lens[req] - c;
     }
     s_req = req;
     s_j0 = j0;
@@ -465,42 +439,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   // walks key tiles 0 .. n_X - 1 (n_1 = 0 when it holds no token).
   const int tok1 = max(0, min(tpt, tokens - tpt));
   const int tok0 = min(tpt, tokens);
-  // causal: p is the cached prefix, query tile X's last token sees
-  // p + j0 + X tpt + tok_X keys; otherwise every query sees the p keys, and
-  // this CTA takes key tiles tile0 .. tile0 + n - 1 of them (its key range).
-  int tile0 = 0, n_nc = 0;
-  if (!a.causal) {
-    const int nk = (p + kN - 1) / kN;
-    const int per = (nk + a.key_splits - 1) / a.key_splits;
-    tile0 = static_cast<int>(blockIdx.z) * per;
-    n_nc = max(0, min(nk, tile0 + per) - tile0);
-  }
-  const int n0 = a.causal ? (p + j0 + tok0 + kN - 1) / kN : n_nc;
-  const int n1 = tok1 == 0 ? 0 : a.causal ? (p + j0 + tpt + tok1 + kN - 1) / kN : n_nc;
-  const int n_tiles = max(n0, n1);
-  const int pslot = a.pslot + static_cast<int>(blockIdx.z);  // partial slot of this key range
-  if (n_tiles == 0) {
-    // No visible key (an empty shared prefix): o = 0, lse = -inf.
-    if (warp < kSoftmaxWarps) {
-      const int r = (warp & 3) * 32 + lane;
-      const int tok = (warp >> 2) * tpt + r / a.group;
-      const int qt = (r / a.group < tpt && tok < tokens) ? query_token(a, t_base, j0, tok) : -1;
-      if (qt >= 0) {
-        const int64_t bh = static_cast<int64_t>(qt) * a.hq + kvh * a.group + (r % a.group);
-        if (a.part_o) {
-          const int64_t prow = bh * a.pstride + pslot;
-          for (int d = 0; d < D; d += 4)
-            *reinterpret_cast<float4 *>(a.part_o + prow * D + d) = make_float4(0.f, 0.f, 0.f, 0.f);
-          a.part_lse[prow] = -INFINITY;
-        } else {
-          for (int d = 0; d < D; d += 8)
-            *reinterpret_cast<uint4 *>(a.o + bh * D + d) = make_uint4(0u, 0u, 0u, 0u);
-          if (a.lse) a.lse[bh] = -INFINITY;
-        }
-      }
-    }
-    return;
-  }
+  // p is the cached prefix: query tile X's last token sees p + j0 + X tpt +
+  // tok_X keys.
+  const int n0 = (p + j0 + tok0 + kN - 1) / kN;
+  const int n1 = tok1 == 0 ? 0 : (p + j0 + tpt + tok1 + kN - 1) / kN;
+  const int n_tiles = max(n0, n1);  // >= 1: a CTA holds at least one token
 
   if (tid == 0) {
     for (int i = 0; i < 2; ++i) {
@@ -539,7 +482,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int r = 4 * lane + e;
         const int tt = r / a.group;  // token within the query tile
         const int tok = x * tpt + tt;
-        const int qt = (tt < tpt && tok < tokens) ? query_token(a, t_base, j0, tok) : -1;
+        const int qt = (tt < tpt && tok < tokens) ? t_base + j0 + tok : -1;
         qr[e] = qt >= 0 ? qt * a.hq + kvh * a.group + (r % a.group) : -1;
       }
 #pragma unroll
@@ -560,10 +503,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive_expect_tx(bar(kBarFull + s), 2 * S::kTileBytes);
 #pragma unroll
         for (int h = 0; h < kHalves; ++h) {
-          tma_load_2d(dst + h * (kN * 128), &kv_map, h * 64, k_run + (tile0 + j) * kN,
-                      bar(kBarFull + s));
-          tma_load_2d(dst + S::kTileBytes + h * (kN * 128), &kv_map, h * 64,
-                      v_run + (tile0 + j) * kN,
+          tma_load_2d(dst + h * (kN * 128), &kv_map, h * 64, k_run + j * kN, bar(kBarFull + s));
+          tma_load_2d(dst + S::kTileBytes + h * (kN * 128), &kv_map, h * 64, v_run + j * kN,
                       bar(kBarFull + s));
         }
       }
@@ -655,12 +596,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = quarter * 32 + lane;  // query row == TMEM lane
     const int tt = r / a.group;         // token within the query tile
     const int tok = x * tpt + tt;       // token within the CTA
-    const int qtok = (tt < tpt && tok < tokens) ? query_token(a, t_base, j0, tok) : -1;
+    const int qtok = (tt < tpt && tok < tokens) ? t_base + j0 + tok : -1;
     const bool valid = qtok >= 0;
-    if (!valid && a.members && tt < tpt && tok < tokens) flag_error(a.err, kErrIndptr);
     // last key of the tile's first token, and the last key this row may see
-    const int min_limit = a.causal ? p + j0 + x * tpt : p - 1;
-    const int limit = a.causal ? min_limit + (valid ? tt : 0) : p - 1;
+    const int min_limit = p + j0 + x * tpt;
+    const int limit = min_limit + (valid ? tt : 0);
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t srow = tmem + lane_base + kTmemS + x * kN;
     const uint32_t orow_t = tmem + lane_base + kTmemO + x * D;
@@ -698,7 +638,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld32(srow + 64, *reinterpret_cast<float(*)[32]>(&v[64]));
       tmem_ld32(srow + 96, *reinterpret_cast<float(*)[32]>(&v[96]));
       tmem_ld_wait();
-      const int key0 = (tile0 + j) * kN;
+      const int key0 = j * kN;
       if (key0 + kN - 1 > min_limit) {  // tile crosses some row's last key (warp-uniform)
 #pragma unroll
         for (int cc = 0; cc < kN; ++cc) v[cc] = key0 + cc <= limit ? v[cc] : -INFINITY;
@@ -773,19 +713,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float inv = l > 0.f ? 1.f / l : 0.f;
       const int64_t orow =
           static_cast<int64_t>(valid ? qtok : 0) * a.hq + kvh * a.group + (r % a.group);
-      const int64_t prow = orow * a.pstride + pslot;  // cascade partial slot
 #pragma unroll 1
       for (int cb = 0; cb < D / 32; ++cb) {
         float o[32];
         tmem_ld32(orow_t + cb * 32, o);
         tmem_ld_wait();
-        if (valid && a.part_o) {
-          float4 *dst = reinterpret_cast<float4 *>(a.part_o + prow * D + cb * 32);
-#pragma unroll
-          for (int q4 = 0; q4 < 8; ++q4)
-            dst[q4] = make_float4(o[q4 * 4] * inv, o[q4 * 4 + 1] * inv, o[q4 * 4 + 2] * inv,
-                                  o[q4 * 4 + 3] * inv);
-        } else if (valid) {
+        if (valid) {
           uint4 *dst = reinterpret_cast<uint4 *>(a.o + orow * D + cb * 32);
 #pragma unroll
           for (int q4 = 0; q4 < 4; ++q4) {
@@ -798,11 +731,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      const float lse_nat = l > 0.f ? (m_used + __log2f(l)) * kLn2 : -INFINITY;
-      if (valid && a.part_o)
-        a.part_lse[prow] = lse_nat;
-      else if (valid && a.lse)
-        a.lse[orow] = lse_nat;
+      if (valid && a.lse) a.lse[orow] = l > 0.f ? (m_used + __log2f(l)) * kLn2 : -INFINITY;
     }
   }
 
@@ -868,21 +797,6 @@ size_t extend_workspace_bytes(int32_t batch, int32_t hkv, int32_t d, int32_t cap
   return kv + 4ull * static_cast<uint64_t>(plan_ints(batch, extend_s_pad(capacity)));
 }
 
-int32_t cascade_prefix_splits(int32_t batch, int32_t hq, int32_t hkv, int32_t num_groups,
-                              int32_t max_prefix, int32_t sm_count) {
-  // As many key ranges as keep the (block, kv head, key range) CTAs within
-  // one wave (one CTA per SM), each range at least four key tiles long.
-  const int64_t per = static_cast<int64_t>(kQTiles) * (kM / (hq / hkv));
-  int64_t blocks = (static_cast<int64_t>(batch) + per - 1) / per;
-  if (blocks < num_groups) blocks = num_groups;
-  const int64_t ctas = static_cast<int64_t>(hkv) * (blocks > 0 ? blocks : 1);
-  const int64_t want = static_cast<int64_t>(sm_count > 0 ? sm_count : 1) / ctas;
-  const int64_t nk = (static_cast<int64_t>(max_prefix > 0 ? max_prefix : 0) + kN - 1) / kN;
-  int64_t ks = want < nk / 4 ? want : nk / 4;
-  if (ks > 64) ks = 64;
-  return static_cast<int32_t>(ks < 1 ? 1 : ks);
-}
-
 cudaError_t launch_extend(const PoolGeom &g, int32_t layer, const void *q,
                           const int32_t *qo_indptr, void *o, float *lse,
                           const int32_t *page_table, int64_t table_stride,
@@ -915,11 +829,9 @@ cudaError_t launch_extend(const PoolGeom &g, int32_t layer, const void *q,
   ga.qo_indptr = qo_indptr;
   ga.total_q = total_q;
   ga.tokens_per_tile = kM / (hq / g.hkv);
-  ga.causal = mode.causal;
   ga.k_new = static_cast<const __nv_bfloat16 *>(mode.k_new);
   ga.v_new = static_cast<const __nv_bfloat16 *>(mode.v_new);
   ga.kv_row_stride = mode.kv_row_stride;
-  ga.defer_wait = mode.overlap_previous;
   ga.pool_w = static_cast<__nv_bfloat16 *>(const_cast<void *>(g.base));
   ga.plan = reinterpret_cast<int32_t *>(
       static_cast<uint8_t *>(workspace) +
@@ -942,13 +854,6 @@ cudaError_t launch_extend(const PoolGeom &g, int32_t layer, const void *q,
   a.scale_log2 = scale > 0.f ? scale * kLog2e : (scale < 0.f ? -scale * kLog2e : kLog2e);
   a.err = err;
   a.plan = ga.plan;
-  a.causal = mode.causal;
-  a.members = mode.members;
-  a.part_o = mode.part_o;
-  a.part_lse = mode.part_lse;
-  a.pstride = mode.pstride;
-  a.pslot = mode.pslot;
-  a.key_splits = mode.causal ? 1 : (mode.key_splits < 1 ? 1 : mode.key_splits);
   CUtensorMap kv_map, q_map;
   if (!bf16_map(&kv_map, workspace, ws_rows, static_cast<uint64_t>(g.d), kN) ||
       !bf16_map(&q_map, q, q_rows, static_cast<uint64_t>(g.d), 1))
@@ -959,8 +864,7 @@ cudaError_t launch_extend(const PoolGeom &g, int32_t layer, const void *q,
   // one row of gather CTAs per request, plus one row holding the planner
   const dim3 ggrid(static_cast<unsigned>((s_pad + kGatherKeys - 1) / kGatherKeys),
                    static_cast<unsigned>(batch + 1));
-  const dim3 grid(g.hkv, static_cast<unsigned>(tiles),
-                   static_cast<unsigned>(mode.causal ? 1 : mode.key_splits));
+  const dim3 grid(g.hkv, static_cast<unsigned>(tiles));
   cudaError_t e;
   if (g.d == 128) {
     e = ga.k_new ? launch_pdl(extend_gather_kernel<128, true>, ggrid, dim3(kGatherThreads), 0,

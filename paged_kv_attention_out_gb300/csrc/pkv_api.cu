@@ -263,12 +263,12 @@ size_t pkv_cascade_workspace_size(int32_t batch, int32_t num_q_heads, int32_t nu
     return 0;
   DevInfo *d = nullptr;
   if (device_info(&d) != PKV_OK) return 0;
-  const pkv::DecodePlan plan = pkv::plan_decode(batch, num_q_heads, num_kv_heads, head_dim,
-                                                effective_hint(max_suffix_len_hint), d->sm_count);
+  const pkv::DecodePlan plan = pkv::plan_cascade_suffix(
+      batch, num_q_heads, num_kv_heads, head_dim, effective_hint(max_suffix_len_hint), d->sm_count);
   const int32_t ks = pkv::cascade_prefix_splits(batch, num_q_heads, num_kv_heads, num_groups,
-                                                max_prefix_len_hint, d->sm_count);
-  return align256(pkv::cascade_partial_bytes(batch, num_q_heads, head_dim, plan.splits + ks)) +
-         pkv::extend_workspace_bytes(num_groups, num_kv_heads, head_dim, max_prefix_len_hint);
+                                                max_prefix_len_hint, max_suffix_len_hint,
+                                                d->sm_count);
+  return align256(pkv::cascade_partial_bytes(batch, num_q_heads, head_dim, plan.splits + ks));
 }
 
 pkv_status pkv_paged_cascade_decode_attn(
@@ -312,57 +312,46 @@ pkv_status pkv_paged_cascade_decode_attn(
   const int64_t prefix_row_capacity = prefix_table_stride * g.page_size;
   int64_t pcap = max_prefix_len_hint >= 1 ? max_prefix_len_hint : prefix_row_capacity;
   if (pcap > prefix_row_capacity) pcap = prefix_row_capacity;
-  if (pcap > (int64_t(1) << 30)) return fail(PKV_ERR_UNSUPPORTED, "prefix capacity too large");
-  if (2 * static_cast<int64_t>(num_groups) * g.hkv *
-          pkv::extend_s_pad(static_cast<int32_t>(pcap)) >= (int64_t(1) << 31))
-    return fail(PKV_ERR_UNSUPPORTED, "cascade: groups x kv heads x prefix capacity too large");
-  const int64_t tpc = 2 * (128 / group);  // members per prefix-attention CTA
-  if ((static_cast<int64_t>(batch) + tpc - 1) / tpc + num_groups > 65535)
+  if (pcap > (int64_t(1) << 30)) pcap = int64_t(1) << 30;
+  if (static_cast<int64_t>(pkv::cascade_prefix_blocks(batch, num_q_heads, g.hkv, num_groups)) >
+      65535)
     return fail(PKV_ERR_UNSUPPORTED, "cascade: too many member blocks in one call");
   DevInfo *d = nullptr;
   if ((s = device_info(&d)) != PKV_OK) return s;
-  const pkv::DecodePlan plan = pkv::plan_decode(batch, num_q_heads, g.hkv, g.d,
-                                                effective_hint(max_suffix_len_hint), d->sm_count);
+  const pkv::DecodePlan plan = pkv::plan_cascade_suffix(
+      batch, num_q_heads, g.hkv, g.d, effective_hint(max_suffix_len_hint), d->sm_count);
   const int32_t ks = pkv::cascade_prefix_splits(batch, num_q_heads, g.hkv, num_groups,
-                                                static_cast<int32_t>(pcap), d->sm_count);
-  const size_t part_bytes =
-      align256(pkv::cascade_partial_bytes(batch, num_q_heads, g.d, plan.splits + ks));
-  const size_t need = part_bytes + pkv::extend_workspace_bytes(num_groups, g.hkv, g.d,
-                                                               static_cast<int32_t>(pcap));
+                                                static_cast<int32_t>(pcap), max_suffix_len_hint,
+                                                d->sm_count);
+  const int32_t slots = plan.splits + ks;
+  const size_t need = align256(pkv::cascade_partial_bytes(batch, num_q_heads, g.d, slots));
   if (!workspace)
     return fail(PKV_ERR_WORKSPACE_TOO_SMALL, "workspace is NULL, %zu bytes needed", need);
   if (workspace_bytes < need)
     return fail(PKV_ERR_WORKSPACE_TOO_SMALL, "workspace %zu bytes, %zu needed", workspace_bytes,
                 need);
   if (!aligned(workspace, 256)) return fail(PKV_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
-  // All on `stream`: the suffix decode, then the shared-prefix gather (it
-  // reads nothing the suffix decode writes, so it runs beside the suffix's
-  // tail and only its exit waits for it), the prefix attention, the merge.
-  // 1. suffix partial states (slots 0 .. splits - 1)
   float *part_o = nullptr, *part_lse = nullptr;
-  cudaError_t e = pkv::launch_cascade_suffix(g, layer, q, o, lse, page_table, table_stride,
-                                             table_idx, seq_lens, batch, num_q_heads, scale, plan,
-                                             ks, workspace, d->err, stream, &part_o, &part_lse);
-  if (e != cudaSuccess) return cuda_fail(e, "cascade suffix launch");
-  // 2. shared-prefix states of every member (slots splits .. splits + ks - 1):
-  //    the extend kernels, non-causal, one block of queries per group's
-  //    members, ks key ranges
-  pkv::ExtendMode mode;
-  mode.causal = 0;
-  mode.members = members;
-  mode.part_o = part_o;
-  mode.part_lse = part_lse;
-  mode.pstride = plan.splits + ks;
-  mode.pslot = plan.splits;
-  mode.key_splits = ks;
-  mode.overlap_previous = 1;
-  e = pkv::launch_extend(g, layer, q, member_indptr, o, nullptr, prefix_page_table,
-                         prefix_table_stride, nullptr, prefix_lens, num_groups, batch,
-                         num_q_heads, scale, static_cast<int32_t>(pcap),
-                         static_cast<uint8_t *>(workspace) + part_bytes, d->sm_count, d->err,
-                         stream, mode);
+  pkv::cascade_partial_ptrs(workspace, batch, num_q_heads, g.d, slots, &part_o, &part_lse);
+  // All on `stream`, in this order:
+  // 1. the shared-prefix states of every member (slots splits .. splits +
+  //    ks - 1): each group's prefix once per kv head and key range, K/V read
+  //    from the pool by the tensor-core prefix kernel;
+  cudaError_t e = pkv::launch_cascade_prefix(
+      g, layer, q, prefix_page_table, prefix_table_stride, prefix_lens, member_indptr, members,
+      num_groups, batch, num_q_heads, scale, part_o, part_lse, slots, plan.splits, ks, d->err,
+      stream);
   if (e != cudaSuccess) return cuda_fail(e, "cascade prefix launch");
-  // 3. merge of every request's suffix splits and prefix states
+  // 2. the suffix partial states (slots 0 .. splits - 1): split-KV decode,
+  //    started as soon as every prefix CTA is running (it reads nothing the
+  //    prefix kernel writes; its last request's split-0 CTAs wait for that
+  //    kernel at their exit, so this grid completes after it);
+  float *po = nullptr, *pl = nullptr;
+  e = pkv::launch_cascade_suffix(g, layer, q, o, lse, page_table, table_stride, table_idx,
+                                 seq_lens, batch, num_q_heads, scale, plan, ks, workspace, d->err,
+                                 stream, &po, &pl);
+  if (e != cudaSuccess) return cuda_fail(e, "cascade suffix launch");
+  // 3. the merge of every request's suffix splits and prefix states.
   e = pkv::launch_cascade_merge(g, layer, q, o, lse, page_table, table_stride, table_idx,
                                 seq_lens, batch, num_q_heads, scale, plan, ks, part_o, part_lse,
                                 d->err, stream);

@@ -27,10 +27,14 @@ struct DecodePlan {
   int32_t chunk;           // keys per split (multiple of 16)
   int32_t splits;          // splits per request (grid.y)
   size_t workspace_bytes;  // 0 when splits == 1
+  int32_t sm_count;        // of the device the plan was made for
 };
 
 DecodePlan plan_decode(int32_t batch, int32_t hq, int32_t hkv, int32_t d, int32_t max_seq_len,
                        int32_t sm_count);
+// The split plan of a cascade's suffix decode (host scalars only).
+DecodePlan plan_cascade_suffix(int32_t batch, int32_t hq, int32_t hkv, int32_t d,
+                               int32_t max_seq_len, int32_t sm_count);
 
 cudaError_t launch_kv_store(const PoolGeom &g, int32_t layer, const void *k, const void *v,
                             int64_t row_stride, const int32_t *out_loc, int64_t n,
@@ -43,13 +47,26 @@ cudaError_t launch_decode(const PoolGeom &g, int32_t layer, const void *q, void 
                           unsigned *err, cudaStream_t stream, const void *k_new = nullptr,
                           const void *v_new = nullptr, int64_t kv_row_stride = 0);
 
-// Cascade decode: suffix partial states for split slots 0 .. splits - 1 of
-// [B, Hq, splits + 1] (decode_kernel, always partial), then the merge of those
-// with slot `splits`, the shared-prefix state written by the extend kernel.
+// Cascade decode: the shared-prefix states of every member (cascade.cu,
+// slots splits .. splits + key ranges - 1 of [B, Hq, slots]), the suffix
+// partial states in slots 0 .. splits - 1 (decode_kernel, always partial),
+// then the merge of all of them per (request, q head).
 size_t cascade_partial_bytes(int32_t batch, int32_t hq, int32_t d, int32_t slots);
+void cascade_partial_ptrs(void *partials, int32_t batch, int32_t hq, int32_t d, int32_t slots,
+                          float **part_o, float **part_lse);
 // Key ranges the shared prefix of a cascade is cut into, from host sizes only.
 int32_t cascade_prefix_splits(int32_t batch, int32_t hq, int32_t hkv, int32_t num_groups,
-                              int32_t max_prefix, int32_t sm_count);
+                              int32_t max_prefix, int32_t max_suffix, int32_t sm_count);
+// Upper bound on the shared-prefix CTAs per (kv head, key range): member
+// blocks of 128 / (Hq / Hkv) members, cut per group.
+int32_t cascade_prefix_blocks(int32_t batch, int32_t hq, int32_t hkv, int32_t num_groups);
+cudaError_t launch_cascade_prefix(const PoolGeom &g, int32_t layer, const void *q,
+                                  const int32_t *prefix_table, int64_t prefix_stride,
+                                  const int32_t *prefix_lens, const int32_t *member_indptr,
+                                  const int32_t *members, int32_t num_groups, int32_t batch,
+                                  int32_t hq, float scale, float *part_o, float *part_lse,
+                                  int32_t pstride, int32_t pslot, int32_t key_splits,
+                                  unsigned *err, cudaStream_t stream);
 cudaError_t launch_cascade_suffix(const PoolGeom &g, int32_t layer, const void *q, void *o,
                                   float *lse, const int32_t *page_table, int64_t table_stride,
                                   const int32_t *table_idx, const int32_t *seq_lens,
@@ -63,28 +80,13 @@ cudaError_t launch_cascade_merge(const PoolGeom &g, int32_t layer, const void *q
                                  int32_t prefix_slots, float *part_o, float *part_lse,
                                  unsigned *err, cudaStream_t stream);
 
-// Where the extend kernel's queries come from and where its results go. The
-// defaults are the extend call: chunk token t of request r is q row
-// qo_indptr[r] + t, causal, bf16 o and lse. The cascade's shared-prefix
-// attention sets members (token t of group r is request members[qo_indptr[r]
-// + t]), causal = 0 (every member sees all seq_lens[r] prefix keys) and
-// writes fp32 partial states into slot `pslot` of [B, Hq, pstride].
+// Options of the extend call: store_kv fused into the gather (the chunk's
+// rows of k_new / v_new, kv_row_stride elements apart, are written into the
+// pool at their slots and attended in the same call).
 struct ExtendMode {
-  int32_t causal = 1;
-  const int32_t *members = nullptr;
-  float *part_o = nullptr;
-  float *part_lse = nullptr;
-  int32_t pstride = 0;
-  int32_t pslot = 0;
-  int32_t key_splits = 1;  // non-causal: key ranges per block (slots pslot .. + key_splits - 1)
-  // causal only: store_kv fused into the gather (chunk rows of k_new / v_new,
-  // kv_row_stride elements apart, written into the pool at their slots)
   const void *k_new = nullptr;
   const void *v_new = nullptr;
   int64_t kv_row_stride = 0;
-  // the gather reads nothing the previous kernel on the stream writes: it
-  // may run beside that kernel (its dependency wait moves to its exit)
-  int32_t overlap_previous = 0;
 };
 
 // Gathered-K/V workspace of the extend call: [2][batch][hkv][s_pad][d] bf16,

@@ -221,7 +221,7 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
 // Waits until the phase of `bar` with the given parity has completed. Gives
 // up (returns false) after ~2 s or as soon as *abort becomes non-zero, so a
 // broken pipeline ends the kernel with an error flag instead of a hang.
-__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort) {
+static __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort) {
   uint64_t t0 = 0;
   for (uint32_t i = 0;; ++i) {
     uint32_t done;
@@ -313,6 +313,12 @@ __device__ __forceinline__ bool mbar_wait_fast(uint32_t bar, uint32_t parity, vo
 __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, volatile int *abort) {
   const bool ok = mbar_wait_fast(bar, parity, abort);
   return __all_sync(0xffffffffu, ok);
+}
+
+// Barrier among `count` threads (a multiple of 32) of the CTA on hardware
+// barrier `id` (1 .. 15; 0 is the one __syncthreads uses).
+__device__ __forceinline__ void named_barrier_sync(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
 // Softmax arithmetic of the tcgen05 attention kernels (one query row per
