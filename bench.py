@@ -243,11 +243,13 @@ class Workload:
         self.o = torch.empty_like(self.q)
         self.lse = torch.empty(self.q.shape[:2], dtype=torch.float32, device=dev)
         self.hint = case.max_seq_len
+        self.total_keys = int(case.seq_lens.sum())  # the scheduler knows it on the host
         self.ws = None
         if case.kind == "decode":
             n = pkv.pkv_decode_workspace_size(case.B, case.Hq, case.Hkv, case.D, self.hint)
         else:
-            n = pkv.pkv_extend_workspace_size(case.B, case.Hkv, case.D, self.hint)
+            n = pkv.pkv_extend_workspace_size(case.B, case.Hkv, case.D, self.hint,
+                                              self.total_keys)
         self.ws = torch.empty(max(n, 256), dtype=torch.uint8, device=dev)
         self.launches_per_step = None
 
@@ -264,7 +266,8 @@ class Workload:
         else:
             self.pkv.pkv_paged_extend_attn(self.pool, c.layer, self.q, t["qo_indptr"], self.o,
                                            self.lse, t["page_table"], t["seq_lens"], c.scale,
-                                           self.hint, self.ws, table_idx=t.get("table_idx"))
+                                           self.hint, self.ws, table_idx=t.get("table_idx"),
+                                           max_total_keys_hint=self.total_keys)
 
     def kernels_per_step(self) -> int:
         c = self.case
@@ -313,7 +316,8 @@ class FusedExtendWorkload(Workload):
         self.pkv.pkv_paged_extend_attn_store(self.pool, c.layer, self.q, self.k, self.v,
                                              t["qo_indptr"], self.o, self.lse, t["page_table"],
                                              t["seq_lens"], c.scale, self.hint, self.ws,
-                                             table_idx=t.get("table_idx"))
+                                             table_idx=t.get("table_idx"),
+                                             max_total_keys_hint=self.total_keys)
 
     def kernels_per_step(self) -> int:
         return 2  # gather (with the store), attention

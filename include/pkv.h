@@ -212,14 +212,20 @@ pkv_status pkv_paged_decode_attn_noalloc(const pkv_pool *pool, int32_t layer, co
 
 /*
  * Bytes of device workspace pkv_paged_extend_attn needs: the visible K and V
- * rows of every request, gathered once out of the paged pool into
- * contiguous per-(request, kv head) runs, [2][batch][Hkv][S][head_dim] bf16
- * with S = max_seq_len_hint rounded up to a multiple of 128. Depends only on
- * these host-side sizes. max_seq_len_hint < 1: no bound known, pass the row
- * capacity table_stride * page_size instead.
+ * rows of every request, gathered once out of the paged pool into one
+ * contiguous run per (request, kv head), each request's seq_len rounded up
+ * to 128 rows, the requests' runs back to back ([2][Hkv][C][head_dim] bf16,
+ * C = max_total_keys_hint rounded up to 128, plus 128 per request), then the
+ * attention's block schedule. So the size follows the keys present, not
+ * batch x the longest request. Depends only on these host-side sizes:
+ *   max_seq_len_hint     a bound on every seq_len (>= 1; it sets the
+ *                        schedule's cost buckets: scheduling only);
+ *   max_total_keys_hint  a bound on the sum of the call's seq_lens; < 1: no
+ *                        sum known, batch x max_seq_len_hint is used.
+ * Returns 0 for invalid sizes.
  */
 size_t pkv_extend_workspace_size(int32_t batch, int32_t num_kv_heads, int32_t head_dim,
-                                 int32_t max_seq_len_hint);
+                                 int32_t max_seq_len_hint, int64_t max_total_keys_hint);
 
 /*
  * Extend (chunked-prefill) attention ("Code Notes: mini-sglang", Scheduler
@@ -235,18 +241,24 @@ size_t pkv_extend_workspace_size(int32_t batch, int32_t num_kv_heads, int32_t he
  * [total_q, Hq] or NULL; qo_indptr: device int32 [batch + 1], qo_indptr[0]
  * = 0, non-decreasing, qo_indptr[batch] = total_q. Other tables as for
  * decode. max_seq_len_hint: a bound on every seq_len of the call (< 1: the
- * row capacity table_stride * page_size); a request above it is not
- * computed (its outputs are unspecified) and PKV_DEVERR_SEQ_LEN_RANGE is
- * flagged. workspace: device, 256-byte aligned, at least
- * pkv_extend_workspace_size(batch, Hkv, D, max_seq_len_hint) bytes (with the
- * same effective bound), contents irrelevant on entry.
+ * row capacity table_stride * page_size); it only sets how finely the
+ * attention's blocks are sorted by cost, and a longer request is still
+ * computed. max_total_keys_hint: a bound on the sum of the seq_lens (< 1:
+ * batch x max_seq_len_hint); a request whose rounded-up keys, counted in
+ * request order, would go past it is not computed (its outputs are
+ * unspecified) and PKV_DEVERR_SEQ_LEN_RANGE is flagged, as it is for a
+ * seq_len outside [0, table_stride * page_size]. workspace: device, 256-byte
+ * aligned, at least pkv_extend_workspace_size(batch, Hkv, D,
+ * max_seq_len_hint, max_total_keys_hint) bytes (with the same effective
+ * bounds), contents irrelevant on entry.
  */
 pkv_status pkv_paged_extend_attn(const pkv_pool *pool, int32_t layer, const void *q,
                                  const int32_t *qo_indptr, void *o, float *lse,
                                  const int32_t *page_table, int64_t table_stride,
                                  const int32_t *table_idx, const int32_t *seq_lens,
                                  int32_t batch, int32_t total_q, int32_t num_q_heads,
-                                 float scale, int32_t max_seq_len_hint, void *workspace,
+                                 float scale, int32_t max_seq_len_hint,
+                                 int64_t max_total_keys_hint, void *workspace,
                                  size_t workspace_bytes, cudaStream_t stream);
 
 /*
@@ -263,8 +275,8 @@ pkv_status pkv_paged_extend_attn(const pkv_pool *pool, int32_t layer, const void
  * pkv_paged_extend_attn, provided no other request's row of the call holds
  * those slots. A bad page id at a chunk position is flagged
  * (PKV_DEVERR_PAGE_RANGE) and that token is not stored; a request whose
- * qo_indptr pair is malformed (PKV_DEVERR_INDPTR) or whose seq_len is above
- * the hint (PKV_DEVERR_SEQ_LEN_RANGE) stores nothing.
+ * qo_indptr pair is malformed (PKV_DEVERR_INDPTR) or whose keys go past the
+ * bounds (PKV_DEVERR_SEQ_LEN_RANGE) stores nothing.
  */
 pkv_status pkv_paged_extend_attn_store(const pkv_pool *pool, int32_t layer, const void *q,
                                        const void *k_new, const void *v_new,
@@ -273,15 +285,15 @@ pkv_status pkv_paged_extend_attn_store(const pkv_pool *pool, int32_t layer, cons
                                        int64_t table_stride, const int32_t *table_idx,
                                        const int32_t *seq_lens, int32_t batch, int32_t total_q,
                                        int32_t num_q_heads, float scale,
-                                       int32_t max_seq_len_hint, void *workspace,
-                                       size_t workspace_bytes, cudaStream_t stream);
+                                       int32_t max_seq_len_hint, int64_t max_total_keys_hint,
+                                       void *workspace, size_t workspace_bytes,
+                                       cudaStream_t stream);
 
 /*
- * Bytes of device workspace pkv_paged_cascade_decode_attn needs: the split
- * partial states of the suffix decode plus one slot per (request, q head)
- * for the shared-prefix state, then the gathered prefix K/V of num_groups
- * groups with capacity max_prefix_len_hint (>= 1) and their block schedule.
- * Depends only on these host-side sizes (and the device's SM count).
+ * Bytes of device workspace pkv_paged_cascade_decode_attn needs: fp32 partial
+ * states per (request, q head), one per suffix split and one per key range
+ * the shared prefixes are cut into. Depends only on these host-side sizes
+ * (max_prefix_len_hint >= 1) and the device's SM count.
  */
 size_t pkv_cascade_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
                                   int32_t head_dim, int32_t num_groups,
@@ -300,22 +312,27 @@ size_t pkv_cascade_workspace_size(int32_t batch, int32_t num_q_heads, int32_t nu
  *   its own suffix: seq_lens[b] keys of row table_idx[b] (or b) of page_table,
  * i.e. o[b,h,:], lse[b,h] = attention of q[b,h,:] over those keys. The
  * prefix is attended once per group for all its members together (tensor
- * cores, one 128-row query tile per 128 / (Hq/Hkv) members and kv head), the
- * suffix per request (split-KV decode), and the two states are merged by
- * log-sum-exp. A group may have prefix_lens[k] = 0. Requires Hq/Hkv <= 8 and
+ * cores, one 128-row query tile per 128 / (Hq/Hkv) members and kv head, its
+ * K/V read from the pool once per kv head), the suffix per request
+ * (split-KV decode), and the states are merged by log-sum-exp. A group may have prefix_lens[k] = 0. Requires Hq/Hkv <= 8 and
  * Hkv in {1, 2} or a multiple of 4 (as decode). Tables and q/o/lse as for
  * decode; member_indptr: device int32 [num_groups + 1], member_indptr[0] = 0,
  * non-decreasing, member_indptr[num_groups] <= batch; members: device int32,
  * a permutation of 0 .. batch - 1 laid out by member_indptr (trusted: a
  * request in no group gets an unspecified result, one in two groups a racy
- * one). max_prefix_len_hint: a bound on every prefix_lens entry (< 1: the
- * row capacity prefix_table_stride * page_size); a group above it is not
- * computed and PKV_DEVERR_SEQ_LEN_RANGE is flagged. max_suffix_len_hint
+ * one; a member index outside the batch is skipped and flagged
+ * PKV_DEVERR_INDPTR). max_prefix_len_hint: a bound on every prefix_lens
+ * entry (< 1: the row capacity prefix_table_stride * page_size); with
+ * max_suffix_len_hint it sets how the prefix is cut into key ranges (host
+ * sizes only); a longer prefix is still computed. A prefix length outside
+ * [0, prefix_table_stride * page_size] is flagged (PKV_DEVERR_SEQ_LEN_RANGE)
+ * and its members get their suffix's attention alone. max_suffix_len_hint
  * sizes the suffix split plan as max_seq_len_hint does for decode. workspace:
  * device, 256-byte aligned, at least pkv_cascade_workspace_size(...) bytes
- * (with the same effective prefix bound). Every kernel runs on `stream`
- * (the shared-prefix gather is launched so that it can run beside the
- * suffix decode's last CTAs).
+ * (with the same effective prefix bound). Every kernel runs on `stream`:
+ * the shared-prefix kernel first, then the suffix decode, which starts as
+ * soon as every prefix CTA is running and fills the SMs those leave free,
+ * then the merge.
  */
 pkv_status pkv_paged_cascade_decode_attn(
     const pkv_pool *pool, int32_t layer, const void *q, void *o, float *lse,

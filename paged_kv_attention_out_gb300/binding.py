@@ -75,15 +75,15 @@ def load() -> ctypes.CDLL:
                                                 _p, _c_int32, _c_int32, ctypes.c_float,
                                                 _c_int32, _p]
     L.pkv_extend_workspace_size.restype = ctypes.c_size_t
-    L.pkv_extend_workspace_size.argtypes = [_c_int32] * 4
+    L.pkv_extend_workspace_size.argtypes = [_c_int32] * 4 + [_c_int64]
     L.pkv_paged_extend_attn.restype = ctypes.c_int
     L.pkv_paged_extend_attn.argtypes = [pool_p, _c_int32, _p, _p, _p, _p, _p, _c_int64, _p, _p,
                                         _c_int32, _c_int32, _c_int32, ctypes.c_float,
-                                        _c_int32, _p, ctypes.c_size_t, _p]
+                                        _c_int32, _c_int64, _p, ctypes.c_size_t, _p]
     L.pkv_paged_extend_attn_store.restype = ctypes.c_int
     L.pkv_paged_extend_attn_store.argtypes = [pool_p, _c_int32, _p, _p, _p, _c_int64, _p, _p, _p,
                                               _p, _c_int64, _p, _p, _c_int32, _c_int32,
-                                              _c_int32, ctypes.c_float, _c_int32, _p,
+                                              _c_int32, ctypes.c_float, _c_int32, _c_int64, _p,
                                               ctypes.c_size_t, _p]
     L.pkv_cascade_workspace_size.restype = ctypes.c_size_t
     L.pkv_cascade_workspace_size.argtypes = [_c_int32] * 7
@@ -259,16 +259,19 @@ def pkv_paged_decode_attn_noalloc(pool, layer: int, q, o, lse, page_table, seq_l
 
 
 def pkv_extend_workspace_size(batch: int, num_kv_heads: int, head_dim: int,
-                              max_seq_len_hint: int) -> int:
+                              max_seq_len_hint: int, max_total_keys_hint: int = 0) -> int:
+    """max_total_keys_hint: a bound on the sum of the call's seq_lens (0: none,
+    batch x max_seq_len_hint is used)."""
     return int(load().pkv_extend_workspace_size(batch, num_kv_heads, head_dim,
-                                                max_seq_len_hint))
+                                                max_seq_len_hint, int(max_total_keys_hint)))
 
 
 def pkv_paged_extend_attn(pool, layer: int, q, qo_indptr, o, lse, page_table, seq_lens,
                           scale: float, max_seq_len_hint: int, workspace, table_idx=None,
-                          stream=None) -> None:
+                          stream=None, max_total_keys_hint: int = 0) -> None:
     """Extend attention; q, o [T, Hq, D] bf16; qo_indptr [B+1]; lse [T, Hq] fp32 or None;
-    workspace: device tensor of at least pkv_extend_workspace_size(...) bytes."""
+    workspace: device tensor of at least pkv_extend_workspace_size(...) bytes for the same
+    hints."""
     ps = pool_struct(pool)
     _want(q, torch.bfloat16, "q", 3)
     _want(o, torch.bfloat16, "o", 3)
@@ -293,12 +296,14 @@ def pkv_paged_extend_attn(pool, layer: int, q, qo_indptr, o, lse, page_table, se
     _check(load().pkv_paged_extend_attn(
         ctypes.byref(ps), int(layer), _ptr(q), _ptr(qo_indptr), _ptr(o), _ptr(lse),
         _ptr(page_table), page_table.shape[1], _ptr(table_idx), _ptr(seq_lens), B, T, Hq,
-        float(scale), int(max_seq_len_hint), _ptr(workspace), ws_bytes, _stream(stream)))
+        float(scale), int(max_seq_len_hint), int(max_total_keys_hint), _ptr(workspace), ws_bytes,
+        _stream(stream)))
 
 
 def pkv_paged_extend_attn_store(pool, layer: int, q, k_new, v_new, qo_indptr, o, lse,
                                 page_table, seq_lens, scale: float, max_seq_len_hint: int,
-                                workspace, table_idx=None, stream=None) -> None:
+                                workspace, table_idx=None, stream=None,
+                                max_total_keys_hint: int = 0) -> None:
     """Extend step with store_kv fused: k_new, v_new [T, Hkv, D] bf16 (row t = query
     token t) go to the chunk's key positions of each row, then extend as
     pkv_paged_extend_attn."""
@@ -334,7 +339,7 @@ def pkv_paged_extend_attn_store(pool, layer: int, q, k_new, v_new, qo_indptr, o,
         ctypes.byref(ps), int(layer), _ptr(q), _ptr(k_new), _ptr(v_new), k_new.stride(0),
         _ptr(qo_indptr), _ptr(o), _ptr(lse), _ptr(page_table), page_table.shape[1],
         _ptr(table_idx), _ptr(seq_lens), B, T, Hq, float(scale), int(max_seq_len_hint),
-        _ptr(workspace), ws_bytes, _stream(stream)))
+        int(max_total_keys_hint), _ptr(workspace), ws_bytes, _stream(stream)))
 
 
 def pkv_cascade_workspace_size(batch: int, num_q_heads: int, num_kv_heads: int, head_dim: int,

@@ -9,8 +9,12 @@
 // Two kernels per call:
 //   extend_gather_kernel  copies each request's visible K and V rows, for
 //       every kv head, out of the paged pool into a contiguous run of the
-//       workspace ([2][batch][Hkv][S_pad][D], zero rows up to the next
-//       multiple of 128 keys), reading the pool once per call;
+//       workspace (zero rows up to the next multiple of 128 keys), reading
+//       the pool once per call. The runs of the requests lie back to back in
+//       request order, [2][Hkv][cap_rows][D], so the workspace is sized by the
+//       keys present (a host bound on their sum), not by batch x max length;
+//       one CTA row per 16 rows of that space, each finding its request by a
+//       prefix sum of the rounded lengths;
 //   extend_tc_kernel      the attention, which then reads every 128-key K or
 //       V tile with plain 2-D TMA boxes instead of row gathers.
 //
@@ -109,8 +113,10 @@ struct GatherArgs {
   const int32_t *table_idx;
   const int32_t *seq_lens;
   int32_t batch;
-  int32_t capacity;  // bound on every seq_len of the call
-  int32_t s_pad;     // capacity rounded up to 128: keys per workspace run
+  int64_t row_capacity;  // table_stride * page_size: a longer seq_len is invalid
+  int32_t cap_rows;      // rows of one (K or V, kv head) region of the workspace
+  int32_t nbuck;         // cost buckets of the block schedule
+  int32_t max_blocks;    // bound on the schedule's blocks
   __nv_bfloat16 *ws;
   unsigned *err;
   // block schedule (built by the planner CTA, read by the attention)
@@ -138,8 +144,9 @@ struct ExtendArgs {
   int32_t hq;
   int32_t group;
   int32_t tokens_per_tile;  // floor(128 / group) chunk tokens per query tile
-  int32_t capacity;
-  int32_t s_pad;
+  int32_t cap_rows;
+  int32_t nbuck;
+  int32_t max_blocks;
   float scale_log2;  // |scale| * log2(e) (log2(e) when scale is 0), always > 0
   // How the softmax scale's sign reaches the scores: the row max is taken
   // on raw scores, which needs scale_log2 > 0, so a negative scale negates
@@ -153,38 +160,72 @@ struct ExtendArgs {
 constexpr int kGatherKeys = 16;     // keys per gather CTA (two per warp)
 constexpr int kGatherThreads = 256;
 
-// Workspace run of request r, kv head h, K (c = 0) or V (c = 1): s_pad rows
-// of D elements starting at row ((c * batch + r) * hkv + h) * s_pad. Rows
-// seq_len .. (seq_len rounded up to 128) - 1 are written as zeros so a tile
-// never holds stale bits (a NaN there would survive P = 0 in P V).
+// Workspace run of request r, kv head h, K (c = 0) or V (c = 1): the
+// request's seq_len rounded up to 128 rows of D elements, starting at row
+// (c * Hkv + h) * cap_rows + off_r, where off_r is the sum of the rounded
+// lengths of requests 0 .. r - 1 (a seq_len outside [0, row capacity] has
+// none). A request whose run would end past cap_rows is not gathered or
+// attended (flagged). Rows seq_len .. (seq_len rounded up to 128) - 1 are
+// written as zeros so a tile never holds stale bits (a NaN there would
+// survive P = 0 in P V).
+__device__ __forceinline__ int64_t run_rows(const GatherArgs &a, int seq) {
+  return (seq >= 0 && seq <= a.row_capacity) ? ((static_cast<int64_t>(seq) + 127) & ~int64_t(127))
+                                             : 0;
+}
+
 // Longest-first block schedule. A "block" is one attention CTA's work: two
 // query tiles (2 * tokens_per_tile chunk tokens) of one request. Its cost is
 // the number of (query tile, key tile) pairs it computes plus two for its
 // prologue and epilogue; blocks are counting-sorted by cost, largest first,
 // so the longest CTAs start in the first wave and the tail is short. Layout
-// (int32): plan[0] = block count; the histogram at kPlanHist (plan_buckets
+// (int32): plan[0] = block count; the histogram at kPlanHist (nbuck
 // entries); then (request, first token, cost) per block in request order;
-// then the sorted (request, first token) pairs.
+// then the sorted (request, first token) pairs; then off_r per request.
 constexpr int kPlanHist = 16;
 
-__host__ __device__ inline int64_t plan_buckets(int64_t s_pad) { return 2 * (s_pad / 128) + 4; }
-__host__ __device__ inline int64_t plan_max_blocks(int64_t batch, int64_t s_pad) {
-  return batch * (s_pad / 16 + 1);  // a block holds >= 16 tokens (group <= 16)
+__host__ __device__ inline int64_t plan_ints(int64_t batch, int64_t nbuck, int64_t max_blocks) {
+  return kPlanHist + nbuck + 5 * max_blocks + batch;
 }
-__host__ __device__ inline int64_t plan_ints(int64_t batch, int64_t s_pad) {
-  return kPlanHist + plan_buckets(s_pad) + 5 * plan_max_blocks(batch, s_pad);
+__host__ __device__ inline int64_t plan_sorted(int64_t nbuck, int64_t max_blocks) {
+  return kPlanHist + nbuck + 3 * max_blocks;
+}
+__host__ __device__ inline int64_t plan_offsets(int64_t nbuck, int64_t max_blocks) {
+  return kPlanHist + nbuck + 5 * max_blocks;
+}
+
+// Block-wide inclusive scan of one int64 per thread (kGatherThreads threads);
+// returns the thread's inclusive sum and writes the round's total.
+__device__ __forceinline__ int64_t block_scan(int64_t v, int64_t *s_warp, int64_t *total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int64_t u = __shfl_up_sync(0xffffffffu, v, off);
+    if (lane >= off) v += u;
+  }
+  if (lane == 31) s_warp[warp] = v;
+  __syncthreads();
+  int64_t before = 0, all = 0;
+#pragma unroll
+  for (int w = 0; w < kGatherThreads / 32; ++w) {
+    before += w < warp ? s_warp[w] : 0;
+    all += s_warp[w];
+  }
+  __syncthreads();  // s_warp may be reused by the caller's next round
+  *total = all;
+  return v + before;
 }
 
 __device__ void plan_blocks(const GatherArgs &a) {
   __shared__ int s_first_bad;
   __shared__ int s_part[kGatherThreads];
+  __shared__ int64_t s_warp[kGatherThreads / 32];
   const int tid = threadIdx.x;
   const int per = 2 * a.tokens_per_tile;
-  const int nbuck = static_cast<int>(plan_buckets(a.s_pad));
-  const int64_t maxb = plan_max_blocks(a.batch, a.s_pad);
+  const int nbuck = a.nbuck;
   int *hist = a.plan + kPlanHist;
-  int *ent = hist + nbuck;       // 3 per block, request order
-  int *sorted = ent + 3 * maxb;  // 2 per block, by cost
+  int *ent = hist + nbuck;                // 3 per block, request order
+  int *sorted = ent + 3 * a.max_blocks;   // 2 per block, by cost
+  int *offsets = a.plan + plan_offsets(nbuck, a.max_blocks);
   if (tid == 0) s_first_bad = a.batch;
   for (int i = tid; i < nbuck; i += kGatherThreads) hist[i] = 0;
   __syncthreads();
@@ -196,21 +237,35 @@ __device__ void plan_blocks(const GatherArgs &a) {
   __syncthreads();
   if (tid == 0 && s_first_bad < a.batch) flag_error(a.err, kErrIndptr);
   const int nreq = s_first_bad;
-  // Block offsets: a running exclusive scan over requests, kGatherThreads at a time.
+  // Run offsets and block offsets: running scans over all requests,
+  // kGatherThreads at a time (the gather CTAs find their runs by the same
+  // run-offset scan).
   int base = 0;
-  for (int r0 = 0; r0 < nreq; r0 += kGatherThreads) {
+  int64_t run_base = 0;
+  for (int r0 = 0; r0 < a.batch; r0 += kGatherThreads) {
     const int r = r0 + tid;
     int nb = 0, c = 0, p = 0;
-    if (r < nreq) {
-      c = a.qo_indptr[r + 1] - a.qo_indptr[r];
+    int64_t rows = 0;
+    bool placed = false;
+    if (r < a.batch) {
       const int seq = a.seq_lens[r];
-      p = seq - c;  // the cached prefix
-      if (p < 0) {
-        flag_error(a.err, kErrIndptr);
-      } else if (seq <= a.capacity) {  // above capacity: flagged by the gather
-        nb = (c + per - 1) / per;
+      rows = run_rows(a, seq);
+      if (rows == 0 && seq != 0) flag_error(a.err, kErrSeqLen);  // outside [0, row capacity]
+      if (r < nreq) {
+        c = a.qo_indptr[r + 1] - a.qo_indptr[r];
+        p = seq - c;  // the cached prefix
+        if (p < 0) flag_error(a.err, kErrIndptr);
       }
     }
+    int64_t round_rows;
+    const int64_t run_end = run_base + block_scan(rows, s_warp, &round_rows);
+    if (r < a.batch) {
+      placed = run_end <= a.cap_rows;
+      if (rows > 0 && !placed) flag_error(a.err, kErrSeqLen);  // past the workspace's key bound
+      offsets[r] = placed ? static_cast<int>(run_end - rows) : 0;
+      if (r < nreq && p >= 0 && rows > 0 && placed) nb = (c + per - 1) / per;
+    }
+    run_base += round_rows;
     s_part[tid] = nb;
     __syncthreads();
     for (int off = 1; off < kGatherThreads; off <<= 1) {  // inclusive scan
@@ -287,19 +342,38 @@ __global__ void __launch_bounds__(kGatherThreads)
 
 template <int D, bool kStore>
 __device__ __forceinline__ void gather_body(const GatherArgs &a) {
-  if (static_cast<int>(blockIdx.y) == a.batch) {  // the extra row: one planner CTA
-    if (blockIdx.x == 0) plan_blocks(a);
+  if (blockIdx.x == gridDim.x - 1) {  // the last CTA: the planner
+    plan_blocks(a);
     return;
   }
-  const int r = blockIdx.y;
+  // The request whose run holds this CTA's 16 rows (runs are multiples of
+  // 128 rows, so they never straddle two requests): the same scan of the
+  // rounded lengths as the planner's, kGatherThreads requests per round.
+  __shared__ int64_t s_warp[kGatherThreads / 32];
+  __shared__ int s_r;
+  __shared__ int64_t s_off;
+  const int64_t pos = static_cast<int64_t>(blockIdx.x) * kGatherKeys;
+  if (threadIdx.x == 0) s_r = -1;
+  int64_t run_base = 0;
+  for (int r0 = 0; r0 < a.batch; r0 += kGatherThreads) {
+    const int rr = r0 + static_cast<int>(threadIdx.x);
+    const int64_t rows = rr < a.batch ? run_rows(a, a.seq_lens[rr]) : 0;
+    int64_t round_rows;
+    const int64_t run_end = run_base + block_scan(rows, s_warp, &round_rows);
+    if (rows > 0 && pos >= run_end - rows && pos < run_end) {
+      s_r = rr;
+      s_off = run_end - rows;
+    }
+    run_base += round_rows;
+    if (pos < run_base) break;  // uniform: found in this round (or in no run)
+  }
+  __syncthreads();
+  const int r = s_r;
+  if (r < 0) return;  // past the last run
+  const int64_t off = s_off;
   const int seq = a.seq_lens[r];
-  if (seq < 0 || seq > a.capacity) {
-    if (blockIdx.x == 0 && threadIdx.x == 0) flag_error(a.err, kErrSeqLen);
-    return;
-  }
-  const int key0 = static_cast<int>(blockIdx.x) * kGatherKeys;
-  const int n_pad = (seq + 127) & ~127;
-  if (key0 >= n_pad) return;
+  if (off + run_rows(a, seq) > a.cap_rows) return;  // past the key bound (flagged by the planner)
+  const int key0 = static_cast<int>(pos - off);
   const int row = a.table_idx ? a.table_idx[r] : r;
   if (row < 0) {
     if (blockIdx.x == 0 && threadIdx.x == 0) flag_error(a.err, kErrTableIdx);
@@ -325,7 +399,7 @@ __device__ __forceinline__ void gather_body(const GatherArgs &a) {
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int64_t row_elems = static_cast<int64_t>(a.hkv) * D;
-  const int64_t run_elems = static_cast<int64_t>(a.s_pad) * D;  // one kv head's run
+  const int64_t run_elems = static_cast<int64_t>(a.cap_rows) * D;  // one kv head's region
   const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
   constexpr int kUnroll = 4;  // chunks per lane per row in flight (x 2 rows)
   for (int kk = warp; kk < kGatherKeys; kk += kGatherThreads / 32) {
@@ -367,8 +441,8 @@ __device__ __forceinline__ void gather_body(const GatherArgs &a) {
         }
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
-        __nv_bfloat16 *dst = a.ws + (static_cast<int64_t>(c) * a.batch + r) * a.hkv * run_elems +
-                             static_cast<int64_t>(key) * D;
+        __nv_bfloat16 *dst = a.ws + static_cast<int64_t>(c) * a.hkv * run_elems +
+                             (off + key) * D;
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
           const int ch = ch0 + 32 * u;
@@ -383,7 +457,7 @@ __device__ __forceinline__ void gather_body(const GatherArgs &a) {
   }
 }
 
-// kv_map: the workspace as a 2-D bf16 tensor [2 * batch * Hkv * s_pad rows][D],
+// kv_map: the workspace as a 2-D bf16 tensor [2 * Hkv * cap_rows rows][D],
 // box {64, 128}; q_map: q as [total_q * Hq rows][D], box {64, 1}. Both with
 // 128-byte swizzle.
 template <int D>
@@ -392,7 +466,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                      const __grid_constant__ CUtensorMap q_map, const ExtendArgs a) {
   using S = Smem<D>;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ int s_req, s_j0, s_c, s_p;
+  __shared__ int s_req, s_j0, s_c, s_p, s_off;
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
   const int tid = threadIdx.x;
@@ -406,15 +480,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     // This CTA's (request, first token) from the longest-first schedule;
     // the schedule holds only well-formed requests.
     const int rank = blockIdx.y;
-    const int *sorted =
-        a.plan + kPlanHist + plan_buckets(a.s_pad) + 3 * plan_max_blocks(a.batch, a.s_pad);
-    int req = -1, j0 = 0, c = 0, p = 0;
+    const int *sorted = a.plan + plan_sorted(a.nbuck, a.max_blocks);
+    int req = -1, j0 = 0, c = 0, p = 0, off = 0;
     if (rank < a.plan[0]) {
       req = sorted[2 * rank];
       j0 = sorted[2 * rank + 1];
       c = a.qo_indptr[req + 1] - a.qo_indptr[req];
       p = a.seq_lens[req] - c;
+      off = a.plan[plan_offsets(a.nbuck, a.max_blocks) + req];
     }
+    s_off = off;
     s_req = req;
     s_j0 = j0;
     s_c = c;
@@ -492,8 +567,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     &q_map, h * 64, qr[0], qr[1], qr[2], qr[3], bar(kBarQFull));
     }
     // first workspace rows of this request's K and V runs for this kv head
-    const int k_run = (req * a.hkv + kvh) * a.s_pad;
-    const int v_run = ((a.batch + req) * a.hkv + kvh) * a.s_pad;
+    const int k_run = kvh * a.cap_rows + s_off;
+    const int v_run = (a.hkv + kvh) * a.cap_rows + s_off;
     int issued = 0;
     for (int j = 0; j < n_tiles; ++j) {
       const int s = j & 1;
@@ -784,31 +859,34 @@ bool bf16_map(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols, ui
 
 }  // namespace
 
-int64_t extend_s_pad(int32_t capacity) { return (static_cast<int64_t>(capacity) + 127) & ~int64_t(127); }
-
-// Gathered K/V, then (256-byte aligned) the block schedule.
-static uint64_t extend_kv_bytes(int32_t batch, int32_t hkv, int32_t d, int32_t capacity) {
-  return 2ull * static_cast<uint64_t>(batch) * static_cast<uint64_t>(hkv) *
-         static_cast<uint64_t>(extend_s_pad(capacity)) * static_cast<uint64_t>(d) * 2ull;
-}
-
-size_t extend_workspace_bytes(int32_t batch, int32_t hkv, int32_t d, int32_t capacity) {
-  const uint64_t kv = (extend_kv_bytes(batch, hkv, d, capacity) + 255) & ~uint64_t(255);
-  return kv + 4ull * static_cast<uint64_t>(plan_ints(batch, extend_s_pad(capacity)));
+ExtendLayout extend_layout(int32_t batch, int32_t hkv, int32_t d, int64_t max_seq,
+                           int64_t max_total_keys) {
+  ExtendLayout l{};
+  const int64_t seq_pad = ((max_seq > 0 ? max_seq : 1) + 127) & ~int64_t(127);
+  const int64_t total = max_total_keys >= 1 ? max_total_keys : static_cast<int64_t>(batch) * seq_pad;
+  // Every request's run is its seq_len rounded up to 128: at most 127 rows
+  // more per request than the keys present.
+  l.cap_rows = ((total + 127) & ~int64_t(127)) + 128 * static_cast<int64_t>(batch);
+  l.nbuck = 2 * (seq_pad / 128) + 4;
+  l.max_blocks = l.cap_rows / 16 + batch;  // a block holds >= 16 chunk tokens (group <= 16)
+  l.kv_bytes = 2ull * static_cast<uint64_t>(hkv) * static_cast<uint64_t>(l.cap_rows) *
+               static_cast<uint64_t>(d) * 2ull;
+  l.plan_offset = (l.kv_bytes + 255) & ~uint64_t(255);
+  l.total_bytes = l.plan_offset + 4ull * static_cast<uint64_t>(plan_ints(batch, l.nbuck, l.max_blocks));
+  return l;
 }
 
 cudaError_t launch_extend(const PoolGeom &g, int32_t layer, const void *q,
                           const int32_t *qo_indptr, void *o, float *lse,
                           const int32_t *page_table, int64_t table_stride,
                           const int32_t *table_idx, const int32_t *seq_lens, int32_t batch,
-                          int32_t total_q, int32_t hq, float scale, int32_t capacity,
-                          void *workspace, int32_t sm_count, unsigned *err, cudaStream_t stream,
+                          int32_t total_q, int32_t hq, float scale, const ExtendLayout &lay,
+                          void *workspace, unsigned *err, cudaStream_t stream,
                           const ExtendMode &mode) {
-  (void)sm_count;
-  const int64_t s_pad = extend_s_pad(capacity);
-  const uint64_t ws_rows = 2ull * static_cast<uint64_t>(batch) * g.hkv * s_pad;
+  const uint64_t ws_rows = 2ull * static_cast<uint64_t>(g.hkv) * static_cast<uint64_t>(lay.cap_rows);
   const uint64_t q_rows = static_cast<uint64_t>(total_q) * hq;
-  if (ws_rows >= (1ull << 31) || q_rows >= (1ull << 31)) return cudaErrorInvalidValue;
+  if (ws_rows >= (1ull << 31) || q_rows >= (1ull << 31) || lay.max_blocks >= (int64_t(1) << 28))
+    return cudaErrorInvalidValue;
 
   GatherArgs ga{};
   ga.pool = static_cast<const __nv_bfloat16 *>(g.base);
@@ -822,8 +900,10 @@ cudaError_t launch_extend(const PoolGeom &g, int32_t layer, const void *q,
   ga.table_idx = table_idx;
   ga.seq_lens = seq_lens;
   ga.batch = batch;
-  ga.capacity = capacity;
-  ga.s_pad = static_cast<int32_t>(s_pad);
+  ga.row_capacity = table_stride * g.page_size;
+  ga.cap_rows = static_cast<int32_t>(lay.cap_rows);
+  ga.nbuck = static_cast<int32_t>(lay.nbuck);
+  ga.max_blocks = static_cast<int32_t>(lay.max_blocks);
   ga.ws = static_cast<__nv_bfloat16 *>(workspace);
   ga.err = err;
   ga.qo_indptr = qo_indptr;
@@ -833,9 +913,7 @@ cudaError_t launch_extend(const PoolGeom &g, int32_t layer, const void *q,
   ga.v_new = static_cast<const __nv_bfloat16 *>(mode.v_new);
   ga.kv_row_stride = mode.kv_row_stride;
   ga.pool_w = static_cast<__nv_bfloat16 *>(const_cast<void *>(g.base));
-  ga.plan = reinterpret_cast<int32_t *>(
-      static_cast<uint8_t *>(workspace) +
-      ((extend_kv_bytes(batch, g.hkv, g.d, capacity) + 255) & ~uint64_t(255)));
+  ga.plan = reinterpret_cast<int32_t *>(static_cast<uint8_t *>(workspace) + lay.plan_offset);
 
   ExtendArgs a{};
   a.qo_indptr = qo_indptr;
@@ -848,8 +926,9 @@ cudaError_t launch_extend(const PoolGeom &g, int32_t layer, const void *q,
   a.hq = hq;
   a.group = hq / g.hkv;
   a.tokens_per_tile = kM / a.group;
-  a.capacity = capacity;
-  a.s_pad = static_cast<int32_t>(s_pad);
+  a.cap_rows = ga.cap_rows;
+  a.nbuck = ga.nbuck;
+  a.max_blocks = ga.max_blocks;
   a.q_mode = scale > 0.f ? 0 : (scale < 0.f ? 1 : 2);
   a.scale_log2 = scale > 0.f ? scale * kLog2e : (scale < 0.f ? -scale * kLog2e : kLog2e);
   a.err = err;
@@ -861,9 +940,8 @@ cudaError_t launch_extend(const PoolGeom &g, int32_t layer, const void *q,
   const int64_t per_cta = static_cast<int64_t>(kQTiles) * a.tokens_per_tile;
   const int64_t tiles = (static_cast<int64_t>(total_q) + per_cta - 1) / per_cta + batch;
   if (tiles > 65535 || batch >= 65535) return cudaErrorInvalidConfiguration;
-  // one row of gather CTAs per request, plus one row holding the planner
-  const dim3 ggrid(static_cast<unsigned>((s_pad + kGatherKeys - 1) / kGatherKeys),
-                   static_cast<unsigned>(batch + 1));
+  // one gather CTA per 16 rows of a region, plus the planner
+  const dim3 ggrid(static_cast<unsigned>(lay.cap_rows / kGatherKeys + 1));
   const dim3 grid(g.hkv, static_cast<unsigned>(tiles));
   cudaError_t e;
   if (g.d == 128) {

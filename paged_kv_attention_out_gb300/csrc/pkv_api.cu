@@ -359,9 +359,10 @@ pkv_status pkv_paged_cascade_decode_attn(
 }
 
 size_t pkv_extend_workspace_size(int32_t batch, int32_t num_kv_heads, int32_t head_dim,
-                                 int32_t max_seq_len_hint) {
+                                 int32_t max_seq_len_hint, int64_t max_total_keys_hint) {
   if (batch <= 0 || num_kv_heads <= 0 || head_dim <= 0 || max_seq_len_hint < 1) return 0;
-  return pkv::extend_workspace_bytes(batch, num_kv_heads, head_dim, max_seq_len_hint);
+  return pkv::extend_layout(batch, num_kv_heads, head_dim, max_seq_len_hint, max_total_keys_hint)
+      .total_bytes;
 }
 
 // Extend with (k_new != NULL) or without the fused store of the chunk's K/V.
@@ -371,8 +372,8 @@ static pkv_status extend_call(const pkv_pool *pool, int32_t layer, const void *q
                               const int32_t *page_table, int64_t table_stride,
                               const int32_t *table_idx, const int32_t *seq_lens, int32_t batch,
                               int32_t total_q, int32_t num_q_heads, float scale,
-                              int32_t max_seq_len_hint, void *workspace, size_t workspace_bytes,
-                              cudaStream_t stream) {
+                              int32_t max_seq_len_hint, int64_t max_total_keys_hint,
+                              void *workspace, size_t workspace_bytes, cudaStream_t stream) {
   pkv::PoolGeom g;
   pkv_status s = check_pool(pool, layer, &g);
   if (s != PKV_OK) return s;
@@ -398,16 +399,19 @@ static pkv_status extend_call(const pkv_pool *pool, int32_t layer, const void *q
   int64_t cap = max_seq_len_hint >= 1 ? max_seq_len_hint : row_capacity;
   if (cap > row_capacity) cap = row_capacity;
   if (cap > (int64_t(1) << 30)) return fail(PKV_ERR_UNSUPPORTED, "sequence capacity too large");
-  const size_t need = pkv::extend_workspace_bytes(batch, g.hkv, g.d, static_cast<int32_t>(cap));
+  if (max_total_keys_hint > (int64_t(1) << 40))
+    return fail(PKV_ERR_UNSUPPORTED, "max_total_keys_hint too large");
+  const pkv::ExtendLayout lay = pkv::extend_layout(batch, g.hkv, g.d, cap, max_total_keys_hint);
+  if (2 * g.hkv * lay.cap_rows >= (int64_t(1) << 31) || lay.max_blocks >= (int64_t(1) << 28))
+    return fail(PKV_ERR_UNSUPPORTED, "extend: kv heads x key bound too large (%lld rows)",
+                static_cast<long long>(2 * g.hkv * lay.cap_rows));
+  const size_t need = lay.total_bytes;
   if (!workspace)
     return fail(PKV_ERR_WORKSPACE_TOO_SMALL, "workspace is NULL, %zu bytes needed", need);
   if (workspace_bytes < need)
     return fail(PKV_ERR_WORKSPACE_TOO_SMALL, "workspace %zu bytes, %zu needed", workspace_bytes,
                 need);
   if (!aligned(workspace, 256)) return fail(PKV_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
-  if (2 * static_cast<int64_t>(batch) * g.hkv * pkv::extend_s_pad(static_cast<int32_t>(cap)) >=
-      (int64_t(1) << 31))
-    return fail(PKV_ERR_UNSUPPORTED, "extend: batch x kv heads x capacity too large");
   const int64_t tpc = 2 * (128 / group);  // chunk tokens per CTA (two 128-row query tiles)
   if ((static_cast<int64_t>(total_q) + tpc - 1) / tpc + batch > 65535)
     return fail(PKV_ERR_UNSUPPORTED, "extend: too many query tiles in one call");
@@ -418,9 +422,8 @@ static pkv_status extend_call(const pkv_pool *pool, int32_t layer, const void *q
   mode.v_new = v_new;
   mode.kv_row_stride = kv_row_stride;
   cudaError_t e = pkv::launch_extend(g, layer, q, qo_indptr, o, lse, page_table, table_stride,
-                                     table_idx, seq_lens, batch, total_q, num_q_heads, scale,
-                                     static_cast<int32_t>(cap), workspace, d->sm_count, d->err,
-                                     stream, mode);
+                                     table_idx, seq_lens, batch, total_q, num_q_heads, scale, lay,
+                                     workspace, d->err, stream, mode);
   return e == cudaSuccess ? PKV_OK : cuda_fail(e, "extend launch");
 }
 
@@ -429,11 +432,12 @@ pkv_status pkv_paged_extend_attn(const pkv_pool *pool, int32_t layer, const void
                                  const int32_t *page_table, int64_t table_stride,
                                  const int32_t *table_idx, const int32_t *seq_lens,
                                  int32_t batch, int32_t total_q, int32_t num_q_heads,
-                                 float scale, int32_t max_seq_len_hint, void *workspace,
+                                 float scale, int32_t max_seq_len_hint,
+                                 int64_t max_total_keys_hint, void *workspace,
                                  size_t workspace_bytes, cudaStream_t stream) {
   return extend_call(pool, layer, q, nullptr, nullptr, 0, qo_indptr, o, lse, page_table,
                      table_stride, table_idx, seq_lens, batch, total_q, num_q_heads, scale,
-                     max_seq_len_hint, workspace, workspace_bytes, stream);
+                     max_seq_len_hint, max_total_keys_hint, workspace, workspace_bytes, stream);
 }
 
 pkv_status pkv_paged_extend_attn_store(const pkv_pool *pool, int32_t layer, const void *q,
@@ -443,8 +447,9 @@ pkv_status pkv_paged_extend_attn_store(const pkv_pool *pool, int32_t layer, cons
                                        int64_t table_stride, const int32_t *table_idx,
                                        const int32_t *seq_lens, int32_t batch, int32_t total_q,
                                        int32_t num_q_heads, float scale,
-                                       int32_t max_seq_len_hint, void *workspace,
-                                       size_t workspace_bytes, cudaStream_t stream) {
+                                       int32_t max_seq_len_hint, int64_t max_total_keys_hint,
+                                       void *workspace, size_t workspace_bytes,
+                                       cudaStream_t stream) {
   if (batch > 0 && total_q > 0) {
     if (!k_new || !v_new) return fail(PKV_ERR_INVALID_ARG, "k_new and v_new must be non-NULL");
     if (!aligned(k_new, 16) || !aligned(v_new, 16))
@@ -456,8 +461,8 @@ pkv_status pkv_paged_extend_attn_store(const pkv_pool *pool, int32_t layer, cons
   }
   return extend_call(pool, layer, q, batch > 0 && total_q > 0 ? k_new : nullptr, v_new,
                      kv_row_stride, qo_indptr, o, lse, page_table, table_stride, table_idx,
-                     seq_lens, batch, total_q, num_q_heads, scale, max_seq_len_hint, workspace,
-                     workspace_bytes, stream);
+                     seq_lens, batch, total_q, num_q_heads, scale, max_seq_len_hint,
+                     max_total_keys_hint, workspace, workspace_bytes, stream);
 }
 
 pkv_status pkv_merge_lse(const float *o_a, const float *lse_a, const float *o_b,

@@ -89,17 +89,29 @@ struct ExtendMode {
   int64_t kv_row_stride = 0;
 };
 
-// Gathered-K/V workspace of the extend call: [2][batch][hkv][s_pad][d] bf16,
-// s_pad = capacity rounded up to 128.
-int64_t extend_s_pad(int32_t capacity);
-size_t extend_workspace_bytes(int32_t batch, int32_t hkv, int32_t d, int32_t capacity);
+// Workspace of the extend call, from host scalars only: the gathered K/V
+// runs ([2][Hkv][cap_rows][D] bf16, every request's keys rounded up to 128,
+// back to back in request order), then (256-byte aligned) the block schedule
+// and the run offsets.
+struct ExtendLayout {
+  int64_t cap_rows;     // rows of one (K or V, kv head) region
+  int64_t nbuck;        // cost buckets of the block schedule
+  int64_t max_blocks;   // bound on the schedule's blocks
+  uint64_t kv_bytes;
+  uint64_t plan_offset;
+  uint64_t total_bytes;
+};
+// max_seq: a bound on every seq_len (sets the schedule's cost buckets);
+// max_total_keys: a bound on their sum (< 1: batch x max_seq).
+ExtendLayout extend_layout(int32_t batch, int32_t hkv, int32_t d, int64_t max_seq,
+                           int64_t max_total_keys);
 
 cudaError_t launch_extend(const PoolGeom &g, int32_t layer, const void *q,
                           const int32_t *qo_indptr, void *o, float *lse,
                           const int32_t *page_table, int64_t table_stride,
                           const int32_t *table_idx, const int32_t *seq_lens, int32_t batch,
-                          int32_t total_q, int32_t hq, float scale, int32_t capacity,
-                          void *workspace, int32_t sm_count, unsigned *err, cudaStream_t stream,
+                          int32_t total_q, int32_t hq, float scale, const ExtendLayout &lay,
+                          void *workspace, unsigned *err, cudaStream_t stream,
                           const ExtendMode &mode = ExtendMode());
 
 cudaError_t launch_merge(const float *o_a, const float *lse_a, const float *o_b,

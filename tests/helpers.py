@@ -151,10 +151,12 @@ def gpu_attention(case: W.Case, pool, q, t, hint=None, with_lse=True, table_idx=
                                   case.scale, h, ws, table_idx=ti)
     else:
         h = case.max_seq_len if hint is None else hint
-        n = pkv.pkv_extend_workspace_size(case.B, case.Hkv, case.D, h)
+        total = int(case.seq_lens.sum())  # the workspace follows the keys present
+        n = pkv.pkv_extend_workspace_size(case.B, case.Hkv, case.D, h, total)
         ws = torch.empty(max(n, 1), dtype=torch.uint8, device=q.device)
         pkv.pkv_paged_extend_attn(pool, case.layer, q, t["qo_indptr"], o, lse, t["page_table"],
-                                  t["seq_lens"], case.scale, h, ws, table_idx=ti)
+                                  t["seq_lens"], case.scale, h, ws, table_idx=ti,
+                                  max_total_keys_hint=total)
     return o, lse
 
 

@@ -87,7 +87,7 @@ def test_bad_host_arguments_are_rejected_before_any_gpu_work(lib):
     # the workspace query refuses nonsense instead of guessing
     assert lib.pkv_decode_workspace_size(0, 32, 8, 128, 4096) == 0
     assert lib.pkv_decode_workspace_size(4, 30, 8, 128, 4096) == 0
-    assert lib.pkv_extend_workspace_size(0, 8, 128, 4096) == 0
+    assert lib.pkv_extend_workspace_size(0, 8, 128, 4096, 0) == 0
     assert lib.pkv_cascade_workspace_size(4, 32, 8, 128, 0, 2048, 512) == 0
     assert lib.pkv_cascade_workspace_size(4, 30, 8, 128, 2, 2048, 512) == 0
     # fused store + decode: NULL or misaligned new rows, row stride below Hkv * D
@@ -100,13 +100,13 @@ def test_bad_host_arguments_are_rejected_before_any_gpu_work(lib):
                                            16, 4, None, 16, 1, 4, f, 4, None, 0, None) == 1
     # fused store + extend: the same refusals
     assert lib.pkv_paged_extend_attn_store(ctypes.byref(pool), 0, 16, None, 16, 256, 16, 16,
-                                           None, 16, 4, None, 16, 1, 8, 4, f, 8, None, 0,
+                                           None, 16, 4, None, 16, 1, 8, 4, f, 8, 0, None, 0,
                                            None) == 1
     assert lib.pkv_paged_extend_attn_store(ctypes.byref(pool), 0, 16, 16, 34, 256, 16, 16,
-                                           None, 16, 4, None, 16, 1, 8, 4, f, 8, None, 0,
+                                           None, 16, 4, None, 16, 1, 8, 4, f, 8, 0, None, 0,
                                            None) == 1
     assert lib.pkv_paged_extend_attn_store(ctypes.byref(pool), 0, 16, 16, 16, 100, 16, 16,
-                                           None, 16, 4, None, 16, 1, 8, 4, f, 8, None, 0,
+                                           None, 16, 4, None, 16, 1, 8, 4, f, 8, 0, None, 0,
                                            None) == 1
     # cascade: group above 8; every request must be in a group; NULL member lists
     assert lib.pkv_paged_cascade_decode_attn(
@@ -118,6 +118,23 @@ def test_bad_host_arguments_are_rejected_before_any_gpu_work(lib):
     assert lib.pkv_paged_cascade_decode_attn(
         ctypes.byref(pool), 0, 16, 16, None, 16, 4, 16, None, None, 1, 16, 4, None, 16, 1, 4, f,
         64, 64, None, 0, None) == 1
+
+
+def test_extend_workspace_follows_the_keys_present():
+    """The extend workspace holds each request's keys rounded up to 128, back
+    to back, so it is sized by a bound on their sum: 64 requests, one of 128k
+    keys and 63 of at most 512, at 8 kv heads and head_dim 128, need under
+    1 GB (batch x the longest would be 34 GB)."""
+    from paged_kv_attention_out_gb300 import binding
+    lib = binding.load()
+    total = 131072 + 63 * 512
+    keyed = lib.pkv_extend_workspace_size(64, 8, 128, 131072, total)
+    longest = lib.pkv_extend_workspace_size(64, 8, 128, 131072, 0)
+    kv = 2 * 8 * 128 * 2  # K and V bytes of one key, all kv heads
+    assert total * kv <= keyed < (1 << 30)
+    assert longest >= 64 * 131072 * kv > 30 * (1 << 30)
+    # the bound covers the 127 rows of rounding per request
+    assert keyed >= (total + 64 * 127) * kv
 
 
 @pytest.mark.gpu

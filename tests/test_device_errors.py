@@ -71,24 +71,46 @@ def test_decode_seq_len_past_the_row_is_flagged():
     compare(o.float().cpu().double().numpy()[1:], want[1:])
 
 
-def test_extend_request_longer_than_the_hint_is_flagged_and_skipped():
+def test_extend_requests_past_the_key_bound_are_flagged_and_skipped():
+    """Runs are laid out in request order, each seq_len rounded up to 128; with
+    a bound of 300 keys the workspace holds 384 + 3 x 128 rows, so request 0
+    (128 rows) fits and requests 1 (768) and 2 (128, starting past the end)
+    do not: they are flagged and not computed, request 0 is."""
     import paged_kv_attention_out_gb300 as pkv
     case = W.random_case(33, kind="extend", seq_lens=[100, 700, 60], chunk_lens=[40, 100, 60],
                          Hq=8, Hkv=2, D=128, P=1)
     pool, k, v, q, t = gpu_inputs(case)
     pkv.pkv_kv_store(pool, case.layer, k, v, t["out_loc"])
-    hint = 200  # request 1 (700 keys) is beyond it
-    ws = torch.empty(pkv.pkv_extend_workspace_size(case.B, case.Hkv, case.D, hint),
+    hint, total = 700, 300
+    ws = torch.empty(pkv.pkv_extend_workspace_size(case.B, case.Hkv, case.D, hint, total),
+                     dtype=torch.uint8, device="cuda")
+    o = torch.full_like(q, float("nan"))
+    _errors()
+    pkv.pkv_paged_extend_attn(pool, case.layer, q, t["qo_indptr"], o, None, t["page_table"],
+                              t["seq_lens"], case.scale, hint, ws, max_total_keys_hint=total)
+    assert _errors() & SEQ
+    want, _, _ = oracle_run(case)
+    compare(o.float().cpu().double().numpy()[0:40], want[0:40])
+
+
+def test_extend_request_longer_than_the_length_hint_is_still_computed():
+    """max_seq_len_hint only sizes the schedule's cost buckets: a longer request
+    is computed (sorted as if it had the hint's length)."""
+    import paged_kv_attention_out_gb300 as pkv
+    case = W.random_case(36, kind="extend", seq_lens=[100, 700, 60], chunk_lens=[40, 100, 60],
+                         Hq=8, Hkv=2, D=128, P=1)
+    pool, k, v, q, t = gpu_inputs(case)
+    pkv.pkv_kv_store(pool, case.layer, k, v, t["out_loc"])
+    hint = 200  # request 1 has 700 keys; no sum given: 3 x 256 rows of keys
+    ws = torch.empty(pkv.pkv_extend_workspace_size(case.B, case.Hkv, case.D, hint, 0),
                      dtype=torch.uint8, device="cuda")
     o = torch.full_like(q, float("nan"))
     _errors()
     pkv.pkv_paged_extend_attn(pool, case.layer, q, t["qo_indptr"], o, None, t["page_table"],
                               t["seq_lens"], case.scale, hint, ws)
-    assert _errors() & SEQ
+    assert _errors() == 0
     want, _, _ = oracle_run(case)
-    got = o.float().cpu().double().numpy()
-    rows = np.r_[0:40, 140:200]  # requests 0 and 2
-    compare(got[rows], want[rows])
+    compare(o.float().cpu().double().numpy(), want)
 
 
 def test_extend_malformed_qo_indptr_is_flagged():

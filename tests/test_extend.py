@@ -74,6 +74,28 @@ def test_extend_any_finite_scale(scale, D):
     check_against_oracle(case)
 
 
+def test_workspace_sized_by_keys_present():
+    """64 requests, one with a 131,008-key cached prefix and a 64-token chunk,
+    63 with short prefixes and chunks: the workspace from the sum of the
+    seq_lens stays under 1 GB (batch x the longest would be 4.3 GB here) and
+    every query matches the oracle."""
+    import paged_kv_attention_out_gb300 as pkv
+    rng = np.random.default_rng(57)
+    chunks = [64] + rng.integers(1, 65, size=63).tolist()
+    seq = [131072] + (np.array(chunks[1:]) + rng.integers(0, 449, size=63)).tolist()
+    case = W.random_case(57, kind="extend", seq_lens=seq, chunk_lens=chunks, Hq=8, Hkv=2, D=128,
+                         P=16)
+    total = int(case.seq_lens.sum())
+    need = pkv.pkv_extend_workspace_size(case.B, case.Hkv, case.D, case.max_seq_len, total)
+    assert 0 < need < (1 << 30)
+    assert pkv.pkv_extend_workspace_size(case.B, case.Hkv, case.D, case.max_seq_len, 0) > 4 << 30
+    o, lse, _ = gpu_run(case)
+    assert_every_row_written(o, lse)
+    want_o, want_lse, _ = oracle_run(case)
+    compare(o, want_o)
+    lse_compare(lse, want_lse)
+
+
 def test_chunked_prefill_full_size():
     case = W.chunked_prefill_extend(0)
     o, lse, _ = gpu_run(case)

@@ -20,13 +20,13 @@ pytestmark = pytest.mark.gpu
 def fused_run(case, poison=True):
     import paged_kv_attention_out_gb300 as pkv
     pool, k, v, q, t = gpu_inputs(case, poison)
-    h = case.max_seq_len
-    ws = torch.empty(pkv.pkv_extend_workspace_size(case.B, case.Hkv, case.D, h),
+    h, total = case.max_seq_len, int(case.seq_lens.sum())
+    ws = torch.empty(pkv.pkv_extend_workspace_size(case.B, case.Hkv, case.D, h, total),
                      dtype=torch.uint8, device="cuda")
     o, lse = nan_outputs(q)
     pkv.pkv_paged_extend_attn_store(pool, case.layer, q, k, v, t["qo_indptr"], o, lse,
                                     t["page_table"], t["seq_lens"], case.scale, h, ws,
-                                    table_idx=t.get("table_idx"))
+                                    table_idx=t.get("table_idx"), max_total_keys_hint=total)
     torch.cuda.synchronize()
     return o, lse, pool
 
@@ -34,13 +34,14 @@ def fused_run(case, poison=True):
 def separate_run(case, poison=True):
     import paged_kv_attention_out_gb300 as pkv
     pool, k, v, q, t = gpu_inputs(case, poison)
-    h = case.max_seq_len
-    ws = torch.empty(pkv.pkv_extend_workspace_size(case.B, case.Hkv, case.D, h),
+    h, total = case.max_seq_len, int(case.seq_lens.sum())
+    ws = torch.empty(pkv.pkv_extend_workspace_size(case.B, case.Hkv, case.D, h, total),
                      dtype=torch.uint8, device="cuda")
     o, lse = nan_outputs(q)
     pkv.pkv_kv_store(pool, case.layer, k, v, t["out_loc"])
     pkv.pkv_paged_extend_attn(pool, case.layer, q, t["qo_indptr"], o, lse, t["page_table"],
-                              t["seq_lens"], case.scale, h, ws, table_idx=t.get("table_idx"))
+                              t["seq_lens"], case.scale, h, ws, table_idx=t.get("table_idx"),
+                              max_total_keys_hint=total)
     torch.cuda.synchronize()
     return o, lse, pool
 
@@ -112,13 +113,13 @@ def test_fused_bad_chunk_page_is_flagged_and_not_stored():
     before = pool.clone()
     pt = t["page_table"].clone()
     pt[0, 70] = -3  # chunk key 70 of request 0 (chunk keys 60 .. 99)
-    h = case.max_seq_len
-    ws = torch.empty(pkv.pkv_extend_workspace_size(case.B, case.Hkv, case.D, h),
+    h, total = case.max_seq_len, int(case.seq_lens.sum())
+    ws = torch.empty(pkv.pkv_extend_workspace_size(case.B, case.Hkv, case.D, h, total),
                      dtype=torch.uint8, device="cuda")
     o, _ = nan_outputs(q, with_lse=False)
     pkv.pkv_read_device_errors()
     pkv.pkv_paged_extend_attn_store(pool, case.layer, q, k, v, t["qo_indptr"], o, None, pt,
-                                    t["seq_lens"], case.scale, h, ws)
+                                    t["seq_lens"], case.scale, h, ws, max_total_keys_hint=total)
     assert pkv.pkv_read_device_errors() & 0x2
     want_o, _, want_pool = oracle_run(case)
     compare(o.float().cpu().double().numpy()[40:], want_o[40:])  # request 1 untouched

@@ -80,8 +80,8 @@ def test_extend_step_in_a_graph():
                          chunk_lens=[100, 77, 200, 9], Hq=8, Hkv=2, D=128, P=1)
     inputs = _setup(case)
     t = inputs[4]
-    h = case.max_seq_len
-    ws = torch.empty(pkv.pkv_extend_workspace_size(case.B, case.Hkv, case.D, h),
+    h, total = case.max_seq_len, int(case.seq_lens.sum())
+    ws = torch.empty(pkv.pkv_extend_workspace_size(case.B, case.Hkv, case.D, h, total),
                      dtype=torch.uint8, device="cuda")
 
     def call(pool, k, v, q):
@@ -89,7 +89,7 @@ def test_extend_step_in_a_graph():
         lse = torch.full(q.shape[:2], float("nan"), dtype=torch.float32, device="cuda")
         pkv.pkv_kv_store(pool, case.layer, k, v, t["out_loc"])
         pkv.pkv_paged_extend_attn(pool, case.layer, q, t["qo_indptr"], o, lse, t["page_table"],
-                                  t["seq_lens"], case.scale, h, ws)
+                                  t["seq_lens"], case.scale, h, ws, max_total_keys_hint=total)
         return o, lse
 
     _graph_vs_eager(case, call, inputs)
