@@ -69,7 +69,10 @@ def build(force: bool = False, verbose: bool = False, extra=()) -> str:
     with ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
     tmp = LIB + f".{tag}.tmp"
-    cmd = [cc, *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs]
+    # -z defs: a declared but undefined function fails the link here instead
+    # of failing to load (or to resolve) at run time
+    cmd = [cc, *ARCH, "-shared", "-cudart", "shared", "-Xlinker", "-z", "-Xlinker", "defs",
+           "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     for o in objs:
         os.remove(o)
