@@ -54,13 +54,18 @@ CSRC = os.path.join(ROOT, "paged_kv_attention_out_gb300", "csrc")
 # it only while those sources are unchanged (else null).
 MEASURED_TRAFFIC = {
     # decode_kernel + decode_merge_kernel, Llama-3-8B-shaped decode
-    "decode": {"sources": ["decode.cu", "pkv_common.cuh"],
-               "sha256": "26163185fe6caad9331194f293495c329b9ec4affdb61e921c9b561df33c954d",
-               "bytes": 628162048},
+    "decode": {"sources": ['decode.cu', 'decode_common.cuh', 'pkv_common.cuh'],
+               "sha256": "63ea7af931f567f52fc2a827f494cc6e6c07923390337cab9e2a22d6f5d6baed",
+               "bytes": 628328192},
     # extend_gather_kernel + extend_tc_kernel, chunked-prefill extend
-    "extend": {"sources": ["extend.cu", "tc_common.cuh", "pkv_common.cuh"],
-               "sha256": "1346caf7eceeadf58410b7173be9f334d568cfb8d81e05685d2ce96fd612239b",
-               "bytes": 523301120},
+    "extend": {"sources": ['extend.cu', 'tc_common.cuh', 'pkv_common.cuh'],
+               "sha256": "0dd933b26e3e9bbf48bfa0594d1070f61cb15f9db76c58090b1c7da77b118259",
+               "bytes": 534103552},
+    # cascade_prefix_kernel + decode_kernel (suffix) + decode_merge_narrow_kernel,
+    # radix-shared decode through cascade decode
+    "cascade": {"sources": ['cascade.cu', 'decode.cu', 'decode_common.cuh', 'tc_common.cuh', 'pkv_common.cuh'],
+                "sha256": "cafcddf18dc1c687095d7a568327c543b0ebcfc98dd48929624b90f405c9c627",
+                "bytes": 373767936},
 }
 
 
@@ -660,7 +665,8 @@ def _extend_workload(args, dev, peaks, peak_src, flush, steps, warm):
         "roofline": {**roofline("tensor", fl, at, peaks, peak_src),
                      "kernel": ("pkv_paged_extend_attn: extend_gather_kernel + extend_tc_kernel "
                                 "(both launches inside the timed duration)"),
-                     "traffic": measured_traffic("extend", args.extend_traffic)}}
+                     "traffic": measured_traffic("extend", args.extend_traffic),
+                     "algorithmic_bytes": extend_bytes(case)}}
     del wl
     torch.cuda.empty_cache()
     return out
@@ -707,9 +713,10 @@ def _radix_workload(args, dev, peaks, peak_src, flush, steps, warm):
         "ms_attention": round(at, 4), "ms_step_with_store": round(st, 4),
         "unique_bytes": uniq, "logical_bytes": logical,
         "roofline": {**roofline("hbm", uniq, at, peaks, peak_src),
-                     "kernel": ("pkv_paged_cascade_decode_attn: suffix decode_kernel + "
-                                "extend_gather_kernel + extend_tc_kernel (prefix) + "
-                                "decode_merge_kernel, all inside the timed duration")}}
+                     "kernel": ("pkv_paged_cascade_decode_attn: cascade_prefix_kernel + "
+                                "suffix decode_kernel + decode_merge_narrow_kernel, all inside "
+                                "the timed duration"),
+                     "traffic": measured_traffic("cascade")}}
     del wl
     torch.cuda.empty_cache()
     return out
