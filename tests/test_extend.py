@@ -77,8 +77,8 @@ def test_extend_any_finite_scale(scale, D):
 def test_workspace_sized_by_keys_present():
     """64 requests, one with a 131,008-key cached prefix and a 64-token chunk,
     63 with short prefixes and chunks: the workspace from the sum of the
-    seq_lens stays under 1 GB (batch x the longest would be 4.3 GB here) and
-    every query matches the oracle."""
+    seq_lens stays under 1 GB (159 MB; batch x the longest would be 8.6 GB
+    here) and every query matches the oracle."""
     import paged_kv_attention_out_gb300 as pkv
     rng = np.random.default_rng(57)
     chunks = [64] + rng.integers(1, 65, size=63).tolist()
