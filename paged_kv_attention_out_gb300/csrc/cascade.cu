@@ -28,9 +28,11 @@
 //   warps 5-8  producers: the members' Q rows once, then per key tile the K
 //              and V rows of the kv head, gathered through the prefix page
 //              table with 16-byte cp.async into 128-byte-swizzled shared
-//              memory (three stages). A stage is handed to the MMA once its
-//              copies have landed (cp.async.wait_group, proxy fence, arrive)
-//              and refilled once the MMAs reading it are done.
+//              memory (three stages, all in flight). Each producer thread's
+//              copies of a stage arrive on its barrier when they land
+//              (cp.async.mbarrier.arrive); the MMA thread fences the async
+//              proxy after its wait; a stage is refilled once the MMAs
+//              reading it are done.
 // Every hand-off is an mbarrier; every wait is bounded (tc_common.cuh).
 #include <math.h>
 
@@ -296,10 +298,36 @@ __global__ void __launch_bounds__(kThreads, 1) cascade_prefix_kernel(const Prefi
       cp_async_16(sbase + S::kQ + sw128_offset(kM, r, ch * 8),
                   qr >= 0 ? a.q + qr * D + ch * 8 : a.q, qr >= 0 ? 16 : 0);
     }
-    cp_async_commit();
+    if (a.q_mode != 0) {
+      // Fold the softmax scale's sign into Q once its rows have landed: the
+      // row max is taken on raw scores, which needs a positive scale (scale *
+      // q.k = |scale| * (-q).k exactly; scale 0 makes every score 0, as q = 0
+      // does). Each thread rewrites the chunks it copied.
+      cp_async_wait_all();
+      for (int c = pt; c < kM * kChunks; c += kProducerThreads) {
+        const int r = c / kChunks, cq = c % kChunks;
+        uint4 *p = reinterpret_cast<uint4 *>(smem + S::kQ + sw128_offset(kM, r, cq * 8));
+        uint4 w = *p;
+        if (a.q_mode == 1) {
+          w.x ^= 0x80008000u;
+          w.y ^= 0x80008000u;
+          w.z ^= 0x80008000u;
+          w.w ^= 0x80008000u;
+        } else {
+          w = make_uint4(0u, 0u, 0u, 0u);
+        }
+        *p = w;
+      }
+      fence_async_shared();
+      mbar_arrive(bar(kBarQFull));
+    } else {
+      cp_async_mbar_arrive(bar(kBarQFull));  // arrives once this thread's Q copies land
+    }
+    // K/V tiles: every stage in flight at once. A thread's arrive on a stage's
+    // barrier fires when all its copies so far have landed; the MMA thread
+    // makes them visible to the tensor core with a proxy fence after its wait.
     constexpr int kKeysPerInstr = 32 / kChunks;  // keys one warp instruction covers
     const int ch = lane % kChunks;
-    int issued = 0;
     for (int j = 0; j < n_tiles; ++j) {
       const int s = j % kStages;
       if (j >= kStages &&
@@ -317,41 +345,10 @@ __global__ void __launch_bounds__(kThreads, 1) cascade_prefix_kernel(const Prefi
         cp_async_16(dst, kv_ok ? kbase + off : a.pool, kv_ok ? 16 : 0);
         cp_async_16(dst + S::kTileBytes, kv_ok ? vbase + off : a.pool, kv_ok ? 16 : 0);
       }
-      cp_async_commit();
-      ++issued;
+      cp_async_mbar_arrive(bar(kBarFull + s));
       if (j + 1 < n_tiles) slot = key_slot_of(j + 1);  // next tile's page entry, off the copy path
-      // The previous group (Q, or tile j - 1) has landed: hand it over.
-      cp_async_wait<1>();
-      fence_async_shared();
-      if (j == 0) {
-        if (a.q_mode != 0) {
-          // Fold the softmax scale's sign into Q: the row max is taken on raw
-          // scores, which needs a positive scale (scale * q.k = |scale| *
-          // (-q).k exactly; scale 0 makes every score 0, as q = 0 does).
-          for (int c = pt; c < kM * kChunks; c += kProducerThreads) {
-            const int r = c / kChunks, cq = c % kChunks;
-            uint4 *p = reinterpret_cast<uint4 *>(smem + S::kQ + sw128_offset(kM, r, cq * 8));
-            uint4 w = *p;
-            if (a.q_mode == 1) {
-              w.x ^= 0x80008000u;
-              w.y ^= 0x80008000u;
-              w.z ^= 0x80008000u;
-              w.w ^= 0x80008000u;
-            } else {
-              w = make_uint4(0u, 0u, 0u, 0u);
-            }
-            *p = w;
-          }
-          fence_async_shared();
-        }
-        mbar_arrive(bar(kBarQFull));
-      } else {
-        mbar_arrive(bar(kBarFull + (j - 1) % kStages));
-      }
     }
-    cp_async_wait<0>();  // the last tile (and every copy, on the abort path)
-    fence_async_shared();
-    if (ok) mbar_arrive(bar(kBarFull + (issued - 1) % kStages));
+    cp_async_wait_all();  // every copy has landed before the CTA may exit
     if (!ok) *abort = 1;
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
@@ -387,6 +384,7 @@ __global__ void __launch_bounds__(kThreads, 1) cascade_prefix_kernel(const Prefi
       };
       bool ok = mbar_wait_fast(bar(kBarQFull), 0, abort) && mbar_wait_fast(bar(kBarFull), 0, abort);
       if (ok) {
+        fence_async_shared();  // Q and tile 0, written by cp.async, read by tcgen05.mma
         tc_fence_after_sync();
         qk(0);
       }
@@ -395,6 +393,7 @@ __global__ void __launch_bounds__(kThreads, 1) cascade_prefix_kernel(const Prefi
         tc_fence_after_sync();
         pv(j - 1);
         if (!(ok = mbar_wait_fast(bar(kBarFull + j % kStages), (j / kStages) & 1, abort))) break;
+        fence_async_shared();  // tile j, written by cp.async, read by tcgen05.mma
         tc_fence_after_sync();
         qk(j);
       }
