@@ -64,6 +64,9 @@ constexpr uint32_t kTmemCols = 256;  // S / P at columns 0 .. 127, O at 128 .. 1
 constexpr uint32_t kTmemS = 0;
 constexpr uint32_t kTmemO = 128;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
+#ifndef PKV_PREFIX_EVICT_FIRST
+#define PKV_PREFIX_EVICT_FIRST 1  // prefix K/V read with the L2 evict-first policy
+#endif
 #ifndef PKV_PREFIX_MAX_SPLITS
 #define PKV_PREFIX_MAX_SPLITS 64  // key ranges per group at most
 #endif
@@ -328,6 +331,8 @@ __global__ void __launch_bounds__(kThreads, 1) cascade_prefix_kernel(const Prefi
     // makes them visible to the tensor core with a proxy fence after its wait.
     constexpr int kKeysPerInstr = 32 / kChunks;  // keys one warp instruction covers
     const int ch = lane % kChunks;
+    // each prefix byte is read once per call: its L2 lines go first
+    const uint64_t kv_policy = PKV_PREFIX_EVICT_FIRST ? l2_evict_first_policy() : 0ull;
     for (int j = 0; j < n_tiles; ++j) {
       const int s = j % kStages;
       if (j >= kStages &&
@@ -342,8 +347,14 @@ __global__ void __launch_bounds__(kThreads, 1) cascade_prefix_kernel(const Prefi
         const bool kv_ok = sl >= 0;
         const int64_t off = kv_ok ? sl * row_elems + ch * 8 : 0;
         const uint32_t dst = kst + sw128_offset(kN, kk, ch * 8);
-        cp_async_16(dst, kv_ok ? kbase + off : a.pool, kv_ok ? 16 : 0);
-        cp_async_16(dst + S::kTileBytes, kv_ok ? vbase + off : a.pool, kv_ok ? 16 : 0);
+        if (PKV_PREFIX_EVICT_FIRST) {
+          cp_async_16_hint(dst, kv_ok ? kbase + off : a.pool, kv_ok ? 16 : 0, kv_policy);
+          cp_async_16_hint(dst + S::kTileBytes, kv_ok ? vbase + off : a.pool, kv_ok ? 16 : 0,
+                           kv_policy);
+        } else {
+          cp_async_16(dst, kv_ok ? kbase + off : a.pool, kv_ok ? 16 : 0);
+          cp_async_16(dst + S::kTileBytes, kv_ok ? vbase + off : a.pool, kv_ok ? 16 : 0);
+        }
       }
       cp_async_mbar_arrive(bar(kBarFull + s));
       if (j + 1 < n_tiles) slot = key_slot_of(j + 1);  // next tile's page entry, off the copy path

@@ -17,6 +17,9 @@ namespace pkv {
 #ifndef PKV_DECODE_STAGES
 #define PKV_DECODE_STAGES 2  // cp.async pipeline depth per warp
 #endif
+#ifndef PKV_KV_EVICT_FIRST
+#define PKV_KV_EVICT_FIRST 1  // K/V tiles read with the L2 evict-first policy
+#endif
 #ifndef PKV_DECODE_WARPS
 #define PKV_DECODE_WARPS 4  // warps per CTA (each on one kv head)
 #endif
@@ -193,6 +196,9 @@ __device__ __forceinline__ void decode_body(const DecodeArgs &a, int hg, int spl
       a.pool + (static_cast<int64_t>(a.num_layers) + a.layer) * a.plane +
       static_cast<int64_t>(kvh) * D;
   const int P = a.page_size;
+  // Each K/V byte is read once: its L2 lines go first (the partial states
+  // the merge reads back and the page-table rows stay).
+  const uint64_t kv_policy = PKV_KV_EVICT_FIRST ? l2_evict_first_policy() : 0ull;
 
   // Page-table entry of this lane's key of warp tile j (lanes 0..15), or -1
   // past the end. Loaded one tile before its copies are issued, so the index
@@ -229,8 +235,13 @@ __device__ __forceinline__ void decode_body(const DecodeArgs &a, int hg, int spl
       const bool ok = s >= 0;
       const int64_t off = ok ? s * slot_stride + chunk * 8 : 0;
       const uint32_t dk = st + swz<D>(r, chunk);
-      cp_async_16(dk, ok ? kbase + off : a.pool, ok ? 16 : 0);
-      cp_async_16(dk + S::kTileBytes, ok ? vbase + off : a.pool, ok ? 16 : 0);
+      if (PKV_KV_EVICT_FIRST) {
+        cp_async_16_hint(dk, ok ? kbase + off : a.pool, ok ? 16 : 0, kv_policy);
+        cp_async_16_hint(dk + S::kTileBytes, ok ? vbase + off : a.pool, ok ? 16 : 0, kv_policy);
+      } else {
+        cp_async_16(dk, ok ? kbase + off : a.pool, ok ? 16 : 0);
+        cp_async_16(dk + S::kTileBytes, ok ? vbase + off : a.pool, ok ? 16 : 0);
+      }
     }
   };
 

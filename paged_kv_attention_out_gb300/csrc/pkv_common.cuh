@@ -37,6 +37,23 @@ __device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src, int s
                : "memory");
 }
 
+// The same copy with an L2 cache policy (createpolicy) attached.
+__device__ __forceinline__ void cp_async_16_hint(uint32_t dst, const void *src, int src_bytes,
+                                                 uint64_t policy) {
+  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2, %3;\n" ::"r"(dst),
+               "l"(src), "r"(src_bytes), "l"(policy)
+               : "memory");
+}
+
+// L2 policy for bytes read once (the K/V stream of attention): their lines
+// go first, so that what is read again soon (partial states, page tables,
+// q) stays in L2 meanwhile.
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
 __device__ __forceinline__ void cp_async_commit() {
   asm volatile("cp.async.commit_group;\n" ::: "memory");
 }
