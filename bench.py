@@ -55,17 +55,17 @@ CSRC = os.path.join(ROOT, "paged_kv_attention_out_gb300", "csrc")
 MEASURED_TRAFFIC = {
     # decode_kernel + decode_merge_kernel, Llama-3-8B-shaped decode
     "decode": {"sources": ['decode.cu', 'decode_common.cuh', 'pkv_common.cuh'],
-               "sha256": "63ea7af931f567f52fc2a827f494cc6e6c07923390337cab9e2a22d6f5d6baed",
-               "bytes": 628328192},
+               "sha256": "1946f3ac4ab631093fbc25b82b65651fec5fd69a755e14f8055eb573eab8ac9f",
+               "bytes": 625499392},
     # extend_gather_kernel + extend_tc_kernel, chunked-prefill extend
     "extend": {"sources": ['extend.cu', 'tc_common.cuh', 'pkv_common.cuh'],
-               "sha256": "0dd933b26e3e9bbf48bfa0594d1070f61cb15f9db76c58090b1c7da77b118259",
-               "bytes": 534103552},
+               "sha256": "83c54f87e8cd8696c109037f258a1557ecc5ee18817d22544846d2d5d4e6f5b0",
+               "bytes": 520547104},
     # cascade_prefix_kernel + decode_kernel (suffix) + decode_merge_narrow_kernel,
     # radix-shared decode through cascade decode
     "cascade": {"sources": ['cascade.cu', 'decode.cu', 'decode_common.cuh', 'tc_common.cuh', 'pkv_common.cuh'],
-                "sha256": "cafcddf18dc1c687095d7a568327c543b0ebcfc98dd48929624b90f405c9c627",
-                "bytes": 373767936},
+                "sha256": "14f710b0ce874b9bdbde9fb98e7430214229063dd2ce089aac515266ad9b2ea2",
+                "bytes": 372247776},
 }
 
 
