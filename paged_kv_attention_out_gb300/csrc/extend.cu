@@ -46,6 +46,7 @@
 #include <cudaTypedefs.h>
 #include <math.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "pkv_common.cuh"
@@ -154,7 +155,7 @@ struct ExtendArgs {
   // scale zeroes it (every score 0, as for q = 0). 0: Q as given.
   int32_t q_mode;
   unsigned *err;
-  const int32_t *plan;
+  int32_t *plan;  // the persistent form takes its work items from plan[1]
 };
 
 constexpr int kGatherKeys = 16;     // keys per gather CTA (two per warp)
@@ -324,7 +325,10 @@ __device__ void plan_blocks(const GatherArgs &a) {
     sorted[2 * pos] = ent[3 * b];
     sorted[2 * pos + 1] = ent[3 * b + 1];
   }
-  if (tid == 0) a.plan[0] = nblk;
+  if (tid == 0) {
+    a.plan[0] = nblk;
+    a.plan[1] = 0;  // the persistent attention's work-item counter
+  }
 }
 
 // kStore: the fused store (a.k_new != nullptr), a separate instantiation so
@@ -827,6 +831,472 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// ------------------------------------------------------------ persistent form
+// One CTA per SM pulls work items, (kv head, block) pairs in longest-first
+// order, from a counter the planner zeroes (plan[1]); item i is block
+// i / Hkv of the schedule on kv head i % Hkv. The roles run the per-tile
+// pipeline above, continued across items: the producer publishes the next
+// item (a two-slot descriptor ring) and loads its Q tiles as soon as every
+// S MMA of the current item is done, and its K/V tiles through the same
+// two-stage ring; the MMA thread issues the next item's first S while the
+// softmax warps write the current item's output, and its first P V once
+// they have read O. So a CTA's prologue (barrier setup, TMEM allocation,
+// the Q and first K/V loads) is paid once per SM, not once per block.
+// Every barrier keeps one phase sequence across items: tile counters for
+// the K/V stages and S/P hand-offs, item counters for the rest, counted per
+// query tile where a tile may sit out an item (no tokens), so a waiter is
+// never two phases behind.
+#ifndef PKV_EXTEND_PERSISTENT
+#define PKV_EXTEND_PERSISTENT 1  // 0: one CTA per block (extend_tc_kernel)
+#endif
+
+enum : int {
+  kPBarFull = 0,        // [2] producer: K and V tiles of stage s landed (TMA bytes)
+  kPBarEmpty = 2,       // [2] MMA: every MMA reading stage s done
+  kPBarSFull = 4,       // [2] MMA: S_X ready
+  kPBarPFull = 6,       // [2] softmax X: P_X in TMEM (and O_X rescaled)
+  kPBarOFull = 8,       // [2] MMA: every MMA of the item on query tile X done
+  kPBarOEmpty = 10,     // [2] softmax X: O_X read out (the item's output written)
+  kPBarItemFull = 12,   // [2] producer: descriptor slot written
+  kPBarItemEmpty = 14,  // [2] MMA thread + one lane per softmax warp: slot read
+  kPBarQFull = 16,      // producer: the item's Q tiles landed (TMA bytes)
+  kPBarQReady = 17,     // softmax warps: Q negated / zeroed in place (q_mode != 0)
+  kPBarQEmpty = 18,     // MMA: every S = Q K^T of the item done (Q may be reloaded)
+  kPBarTeardown = 19,   // MMA: everything issued has finished (abort path)
+  kPBarCount = 20,
+};
+static_assert(kPBarCount <= 32, "barrier area of Smem");
+
+// One work item as the producer publishes it (req < 0: no more items).
+struct ItemDesc {
+  int req, kvh, j0, c, p, off, t_base;
+};
+
+// The item's split into query tiles and key tiles (as in extend_tc_kernel).
+struct ItemGeom {
+  int tokens, n0, n1, n_tiles;
+};
+
+__device__ __forceinline__ ItemGeom item_geom(const ItemDesc &d, int tpt) {
+  ItemGeom g;
+  g.tokens = min(kQTiles * tpt, d.c - d.j0);
+  const int tok1 = max(0, min(tpt, g.tokens - tpt));
+  const int tok0 = min(tpt, g.tokens);
+  g.n0 = (d.p + d.j0 + tok0 + kN - 1) / kN;
+  g.n1 = tok1 == 0 ? 0 : (d.p + d.j0 + tpt + tok1 + kN - 1) / kN;
+  g.n_tiles = max(g.n0, g.n1);
+  return g;
+}
+
+__device__ __forceinline__ ItemDesc shfl_desc(ItemDesc d) {
+  d.req = __shfl_sync(0xffffffffu, d.req, 0);
+  d.kvh = __shfl_sync(0xffffffffu, d.kvh, 0);
+  d.j0 = __shfl_sync(0xffffffffu, d.j0, 0);
+  d.c = __shfl_sync(0xffffffffu, d.c, 0);
+  d.p = __shfl_sync(0xffffffffu, d.p, 0);
+  d.off = __shfl_sync(0xffffffffu, d.off, 0);
+  d.t_base = __shfl_sync(0xffffffffu, d.t_base, 0);
+  return d;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    extend_tc_persistent_kernel(const __grid_constant__ CUtensorMap kv_map,
+                                const __grid_constant__ CUtensorMap q_map, const ExtendArgs a) {
+  using S = Smem<D>;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ ItemDesc s_item[2];
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_abort;
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const int tpt = a.tokens_per_tile;
+
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_addr(smem);
+  const uint32_t bars = sbase + S::kBars;
+  auto bar = [&](int i) { return bars + 8u * static_cast<uint32_t>(i); };
+  volatile int *abort = &s_abort;
+
+  // Set-up that needs nothing from the gather kernel runs before the wait.
+  if (tid == 0) {
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(kPBarFull + i), 1);  // the producer's expect_tx arrival
+      mbar_init(bar(kPBarEmpty + i), 1);
+      mbar_init(bar(kPBarSFull + i), 1);
+      mbar_init(bar(kPBarPFull + i), 128);  // the four warps of one query tile
+      mbar_init(bar(kPBarOFull + i), 1);
+      mbar_init(bar(kPBarOEmpty + i), 128);
+      mbar_init(bar(kPBarItemFull + i), 1);
+      mbar_init(bar(kPBarItemEmpty + i), 1 + kSoftmaxWarps);
+    }
+    mbar_init(bar(kPBarQFull), 1);
+    mbar_init(bar(kPBarQReady), kSoftmaxWarps * 32);
+    mbar_init(bar(kPBarQEmpty), 1);
+    mbar_init(bar(kPBarTeardown), 1);
+    s_abort = 0;
+    mbar_init_fence();
+  }
+  if (warp == kMmaWarp) tmem_alloc(smem_addr(&s_tmem), kTmemCols);
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = s_tmem;
+  grid_dependency_wait();  // the schedule and the K/V runs come from the gather kernel
+
+  if (warp >= kProducerWarp) {
+    // ------------------------------------------------------------ producer
+    // Per item: take the next item from the counter and publish it; once
+    // every S of the previous item is done, load the item's two Q tiles
+    // (lane l: rows 4 l .. 4 l + 3 of each, both 64-column halves; rows past
+    // the item's tokens read as zeros); then its K and V tiles, tile g of
+    // the CTA into stage g % 2 once every MMA reading that stage (tile
+    // g - 2) is done. Lane 0 issues the loads.
+    constexpr int kHalves = D / 64;
+    const int total_items = a.hkv * a.plan[0];
+    const int *sorted = a.plan + plan_sorted(a.nbuck, a.max_blocks);
+    const int *offs = a.plan + plan_offsets(a.nbuck, a.max_blocks);
+    unsigned *counter = reinterpret_cast<unsigned *>(a.plan + 1);
+    bool ok = true;
+    uint32_t g = 0;  // K/V tiles issued (all items)
+    int q_loads = 0;
+    for (int k = 0;; ++k) {
+      const int slot = k & 1;
+      if (k >= 2 &&
+          !(ok = mbar_wait_warp(bar(kPBarItemEmpty + slot), ((k >> 1) - 1) & 1, abort)))
+        break;
+      ItemDesc d{-1, 0, 0, 0, 0, 0, 0};
+      if (lane == 0) {
+        const int i = static_cast<int>(atomicAdd(counter, 1u));
+        if (i < total_items) {
+          const int rank = i / a.hkv;
+          d.kvh = i - rank * a.hkv;
+          d.req = sorted[2 * rank];
+          d.j0 = sorted[2 * rank + 1];
+          d.t_base = a.qo_indptr[d.req];
+          d.c = a.qo_indptr[d.req + 1] - d.t_base;
+          d.p = a.seq_lens[d.req] - d.c;
+          d.off = offs[d.req];
+        }
+        s_item[slot] = d;
+        mbar_arrive(bar(kPBarItemFull + slot));  // release: the slot's contents
+      }
+      d = shfl_desc(d);
+      if (d.req < 0) break;
+      const ItemGeom ig = item_geom(d, tpt);
+      if (k >= 1 && !(ok = mbar_wait_warp(bar(kPBarQEmpty), (k - 1) & 1, abort))) break;
+      if (lane == 0) mbar_arrive_expect_tx(bar(kPBarQFull), kQTiles * S::kQBytes);
+      __syncwarp();
+#pragma unroll
+      for (int x = 0; x < kQTiles; ++x) {
+        int qr[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int r = 4 * lane + e;
+          const int tt = r / a.group;  // token within the query tile
+          const int tok = x * tpt + tt;
+          const int qt = (tt < tpt && tok < ig.tokens) ? d.t_base + d.j0 + tok : -1;
+          qr[e] = qt >= 0 ? qt * a.hq + d.kvh * a.group + (r % a.group) : -1;
+        }
+#pragma unroll
+        for (int h = 0; h < kHalves; ++h)
+          tma_gather4(sbase + S::kQ + static_cast<uint32_t>(x * S::kQBytes + h * (kM * 128) +
+                                                           (lane >> 1) * 1024 + (lane & 1) * 512),
+                      &q_map, h * 64, qr[0], qr[1], qr[2], qr[3], bar(kPBarQFull));
+      }
+      ++q_loads;
+      // first workspace rows of this request's K and V runs for this kv head
+      const int k_run = d.kvh * a.cap_rows + d.off;
+      const int v_run = (a.hkv + d.kvh) * a.cap_rows + d.off;
+      for (int j = 0; j < ig.n_tiles; ++j, ++g) {
+        const int st = static_cast<int>(g & 1);
+        if (g >= 2 && !(ok = mbar_wait_warp(bar(kPBarEmpty + st), ((g >> 1) - 1) & 1, abort)))
+          break;
+        if (lane == 0) {
+          const uint32_t dst = sbase + S::kKV + st * 2 * S::kTileBytes;
+          mbar_arrive_expect_tx(bar(kPBarFull + st), 2 * S::kTileBytes);
+#pragma unroll
+          for (int h = 0; h < kHalves; ++h) {
+            tma_load_2d(dst + h * (kN * 128), &kv_map, h * 64, k_run + j * kN, bar(kPBarFull + st));
+            tma_load_2d(dst + S::kTileBytes + h * (kN * 128), &kv_map, h * 64, v_run + j * kN,
+                        bar(kPBarFull + st));
+          }
+        }
+        __syncwarp();
+      }
+      if (!ok) break;
+    }
+    if (!ok) *abort = 1;
+    if (*abort && lane == 0) {
+      // Let every issued copy land before the CTA can exit: TMA writes to
+      // this CTA's shared memory need no other input to finish.
+      int never = 0;
+      if (q_loads > 0) mbar_wait(bar(kPBarQFull), (q_loads - 1) & 1, &never);
+      for (uint32_t t = g > 2 ? g - 2 : 0; t < g; ++t)
+        mbar_wait(bar(kPBarFull + (t & 1)), (t >> 1) & 1, &never);
+    }
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------ MMA issuer
+    // Per item, as in extend_tc_kernel: S_0(0), S_1(0), then per key tile j
+    // PV_0(j), S_0(j+1), PV_1(j), S_1(j+1) (in-order execution keeps P_X(j)
+    // until PV_X(j) has read it). Across items: the next item's S_X(0) may
+    // run while softmax X writes the previous output (it only reads O_X);
+    // its first PV_X waits until that output has been read out of O_X.
+    if (lane == 0) {
+      constexpr uint32_t idesc_qk = umma_idesc_bf16(kM, kN, 0, 0);
+      constexpr uint32_t idesc_pv = umma_idesc_bf16(kM, D, 0, 1);
+      const uint64_t dq0 = umma_desc_sw128(sbase + S::kQ, 16, 1024);
+      const uint64_t dk0 = umma_desc_sw128(sbase + S::kKV, 16, 1024);
+      const uint64_t dv0 = umma_desc_sw128(sbase + S::kKV + S::kTileBytes, kN * 128, 1024);
+      constexpr uint64_t kStageStep = (2 * S::kTileBytes) >> 4;
+      auto kstep = [](int ks, int rows) -> uint64_t {
+        return static_cast<uint64_t>(((ks >> 2) * (rows * 128) + (ks & 3) * 32) >> 4);
+      };
+      auto qk = [&](int x, uint32_t gt) {  // S_x from CTA tile gt's K
+        const uint64_t dq = dq0 + static_cast<uint64_t>((x * S::kQBytes) >> 4);
+        const uint64_t dk = dk0 + (gt & 1) * kStageStep;
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks)
+          umma_bf16_ss(tmem + kTmemS + x * kN, dq + kstep(ks, kM), dk + kstep(ks, kN), idesc_qk,
+                       ks > 0 ? 1u : 0u);
+        umma_commit(bar(kPBarSFull + x));
+      };
+      int pv_count[2] = {0, 0};  // P V products issued per query tile (all items)
+      int uses[2] = {0, 0};      // items that used query tile x (its O_X written out)
+      // O_x += P_x V(tile gt), j = the item's key tile; the item's first
+      // product overwrites O_x once the previous item's output is read out.
+      auto pv = [&](int x, int j, uint32_t gt) -> bool {
+        if (j == 0 && uses[x] > 0 &&
+            !mbar_wait_fast(bar(kPBarOEmpty + x), (uses[x] - 1) & 1, abort))
+          return false;
+        if (!mbar_wait_fast(bar(kPBarPFull + x), pv_count[x] & 1, abort)) return false;
+        ++pv_count[x];
+        tc_fence_after_sync();
+        const uint64_t dv = dv0 + (gt & 1) * kStageStep;
+#pragma unroll
+        for (int ks = 0; ks < kN / 16; ++ks)
+          umma_bf16_ts(tmem + kTmemO + x * D, tmem + kTmemS + x * kN + ks * 8,
+                       dv + ks * (2048 >> 4), idesc_pv, (j > 0 || ks > 0) ? 1u : 0u);
+        return true;
+      };
+      uint32_t g = 0;  // K/V tiles consumed (all items)
+      bool ok = true;
+      for (int k = 0; ok; ++k) {
+        const int slot = k & 1;
+        if (!(ok = mbar_wait_fast(bar(kPBarItemFull + slot), (k >> 1) & 1, abort))) break;
+        const ItemDesc d = s_item[slot];
+        mbar_arrive(bar(kPBarItemEmpty + slot));
+        if (d.req < 0) break;
+        const ItemGeom ig = item_geom(d, tpt);
+        const int n0 = ig.n0, n1 = ig.n1, n_tiles = ig.n_tiles;
+        const uint32_t g0 = g;
+        ok = mbar_wait_fast(bar(a.q_mode ? kPBarQReady : kPBarQFull), k & 1, abort) &&
+             mbar_wait_fast(bar(kPBarFull + (g0 & 1)), (g0 >> 1) & 1, abort);
+        if (!ok) break;
+        tc_fence_after_sync();
+        qk(0, g0);
+        if (n1 > 0) qk(1, g0);
+        if (n_tiles == 1) umma_commit(bar(kPBarQEmpty));
+        for (int j = 0; j < n_tiles && ok; ++j) {
+          const uint32_t gj = g0 + static_cast<uint32_t>(j);
+          const bool next = j + 1 < n_tiles;
+          if (j < n0) ok = pv(0, j, gj);
+          if (ok && next) ok = mbar_wait_fast(bar(kPBarFull + ((gj + 1) & 1)), ((gj + 1) >> 1) & 1, abort);
+          if (!ok) break;
+          tc_fence_after_sync();
+          if (next && j + 1 < n0) qk(0, gj + 1);
+          if (j < n1 && !(ok = pv(1, j, gj))) break;
+          umma_commit(bar(kPBarEmpty + (gj & 1)));
+          if (next && j + 1 < n1) qk(1, gj + 1);
+          if (j + 2 == n_tiles) umma_commit(bar(kPBarQEmpty));  // every S of the item issued
+          if (j == n0 - 1) umma_commit(bar(kPBarOFull + 0));
+          if (j == n1 - 1) umma_commit(bar(kPBarOFull + 1));
+        }
+        g = g0 + static_cast<uint32_t>(n_tiles);
+        ++uses[0];
+        if (n1 > 0) ++uses[1];
+      }
+      if (!ok) {
+        *abort = 1;
+        flag_error(a.err, kErrTimeout);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ softmax
+    // Query tile x = warp / 4; warp w owns TMEM lanes 32 (w % 4) .. + 31,
+    // one query row per thread, whole rows of S; per item as in
+    // extend_tc_kernel, then the item's output, then O_x is handed back.
+    const int quarter = warp & 3;
+    const int x = warp >> 2;
+    const int r = quarter * 32 + lane;  // query row == TMEM lane
+    const int tt = r / a.group;         // token within the query tile
+    const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t srow = tmem + lane_base + kTmemS + x * kN;
+    const uint32_t orow_t = tmem + lane_base + kTmemO + x * D;
+    int s_count = 0;  // S tiles of query tile x taken (all items)
+    int uses = 0;     // items that used query tile x
+    bool ok = true;
+    for (int k = 0; ok; ++k) {
+      const int slot = k & 1;
+      if (!(ok = mbar_wait_warp(bar(kPBarItemFull + slot), (k >> 1) & 1, abort))) break;
+      const ItemDesc d = s_item[slot];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kPBarItemEmpty + slot));
+      if (d.req < 0) break;
+      const ItemGeom ig = item_geom(d, tpt);
+      const int n_x = x == 0 ? ig.n0 : ig.n1;
+      const int tok = x * tpt + tt;  // token within the item
+      const int qtok = (tt < tpt && tok < ig.tokens) ? d.t_base + d.j0 + tok : -1;
+      const bool valid = qtok >= 0;
+      // last key of the tile's first token, and the last key this row may see
+      const int min_limit = d.p + d.j0 + x * tpt;
+      const int limit = min_limit + (valid ? tt : 0);
+      float m_used = -INFINITY, l = 0.f;
+      if (a.q_mode != 0) {
+        // Fold the softmax scale's sign into the item's Q (both query tiles,
+        // all eight softmax warps), before its first S = Q K^T is issued.
+        if (!(ok = mbar_wait_warp(bar(kPBarQFull), k & 1, abort))) break;
+        uint4 *qs = reinterpret_cast<uint4 *>(smem + S::kQ);
+        const uint32_t flip = 0x80008000u;  // the sign bits of a bf16 pair
+        for (int i = tid; i < kQTiles * S::kQBytes / 16; i += kSoftmaxWarps * 32) {
+          uint4 w = qs[i];
+          if (a.q_mode == 1) {
+            w.x ^= flip;
+            w.y ^= flip;
+            w.z ^= flip;
+            w.w ^= flip;
+          } else {
+            w = make_uint4(0u, 0u, 0u, 0u);
+          }
+          qs[i] = w;
+        }
+        fence_async_shared();  // generic-proxy writes, read next by tcgen05.mma
+        mbar_arrive(bar(kPBarQReady));
+      }
+      for (int j = 0; ok && j < n_x; ++j, ++s_count) {
+        if (!(ok = mbar_wait_warp(bar(kPBarSFull + x), s_count & 1, abort))) break;
+        tc_fence_after_sync();
+        float v[kN];
+        tmem_ld32(srow + 0, *reinterpret_cast<float(*)[32]>(&v[0]));
+        tmem_ld32(srow + 32, *reinterpret_cast<float(*)[32]>(&v[32]));
+        tmem_ld32(srow + 64, *reinterpret_cast<float(*)[32]>(&v[64]));
+        tmem_ld32(srow + 96, *reinterpret_cast<float(*)[32]>(&v[96]));
+        tmem_ld_wait();
+        const int key0 = j * kN;
+        if (key0 + kN - 1 > min_limit) {  // tile crosses some row's last key (warp-uniform)
+#pragma unroll
+          for (int cc = 0; cc < kN; ++cc) v[cc] = key0 + cc <= limit ? v[cc] : -INFINITY;
+        }
+        // Row max of the raw scores; scale_log2 > 0 commutes with max.
+        float mx0 = fmaxf(v[0], v[1]), mx1 = fmaxf(v[2], v[3]);
+        float mx2 = fmaxf(v[4], v[5]), mx3 = fmaxf(v[6], v[7]);
+#pragma unroll
+        for (int cc = 8; cc < kN; cc += 8) {
+          mx0 = max3f(mx0, v[cc], v[cc + 1]);
+          mx1 = max3f(mx1, v[cc + 2], v[cc + 3]);
+          mx2 = max3f(mx2, v[cc + 4], v[cc + 5]);
+          mx3 = max3f(mx3, v[cc + 6], v[cc + 7]);
+        }
+        const float mt = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * a.scale_log2;
+        // Lazy rescale (warp-uniform), as in extend_tc_kernel.
+        const bool rescale = j > 0 && __any_sync(0xffffffffu, mt > m_used + kRescaleThreshold);
+        float f = 1.f;
+        if (j == 0) {
+          m_used = mt;  // may be -inf: a row with no visible key in this tile
+        } else if (rescale) {
+          const float m_new = fmaxf(m_used, mt);
+          f = m_used == -INFINITY ? 0.f : fast_exp2(m_used - m_new);
+          m_used = m_new;
+        }
+        const float nm = m_used == -INFINITY ? 0.f : -m_used;
+        float sa0 = 0.f, sa1 = 0.f, sb0 = 0.f, sb1 = 0.f;
+#pragma unroll
+        for (int cc = 0; cc < kN; cc += 32) {
+          uint32_t w[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            float y0, y1;
+            fma2(y0, y1, v[cc + 2 * e], v[cc + 2 * e + 1], a.scale_log2, nm);
+            y0 = fast_exp2(y0);
+            y1 = fast_exp2(y1);
+            if (e & 1)
+              add2(sb0, sb1, y0, y1);
+            else
+              add2(sa0, sa1, y0, y1);
+            w[e] = pack_bf16(y0, y1);
+          }
+          tmem_st16u(srow + cc / 2, w);  // P_x: keys cc .. cc + 31 -> columns cc/2 ..
+        }
+        l = l * f + ((sa0 + sa1) + (sb0 + sb1));
+        if (rescale) {
+          // O_x is stable: S_x(j) completed, so did PV_x(j - 1) before it.
+#pragma unroll 1
+          for (int cb = 0; cb < D / 32; ++cb) {
+            float o[32];
+            tmem_ld32(orow_t + cb * 32, o);
+            tmem_ld_wait();
+#pragma unroll
+            for (int q = 0; q < 32; ++q) o[q] *= f;
+            tmem_st32(orow_t + cb * 32, o);
+          }
+        }
+        tmem_st_wait();
+        tc_fence_before_sync();
+        mbar_arrive(bar(kPBarPFull + x));
+      }
+      if (!ok) break;
+      if (n_x == 0) continue;
+      if (!(ok = mbar_wait_warp(bar(kPBarOFull + x), uses & 1, abort))) break;
+      tc_fence_after_sync();
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const int64_t orow =
+          static_cast<int64_t>(valid ? qtok : 0) * a.hq + d.kvh * a.group + (r % a.group);
+#pragma unroll 1
+      for (int cb = 0; cb < D / 32; ++cb) {
+        float o[32];
+        tmem_ld32(orow_t + cb * 32, o);
+        tmem_ld_wait();
+        if (valid) {
+          uint4 *dst = reinterpret_cast<uint4 *>(a.o + orow * D + cb * 32);
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            uint4 u;
+            u.x = pack_bf16(o[q4 * 8 + 0] * inv, o[q4 * 8 + 1] * inv);
+            u.y = pack_bf16(o[q4 * 8 + 2] * inv, o[q4 * 8 + 3] * inv);
+            u.z = pack_bf16(o[q4 * 8 + 4] * inv, o[q4 * 8 + 5] * inv);
+            u.w = pack_bf16(o[q4 * 8 + 6] * inv, o[q4 * 8 + 7] * inv);
+            dst[q4] = u;
+          }
+        }
+      }
+      if (valid && a.lse) a.lse[orow] = l > 0.f ? (m_used + __log2f(l)) * kLn2 : -INFINITY;
+      tc_fence_before_sync();
+      mbar_arrive(bar(kPBarOEmpty + x));  // O_x read out: the next item may overwrite it
+      ++uses;
+    }
+    if (!ok) {
+      *abort = 1;
+      flag_error(a.err, kErrTimeout);
+    }
+  }
+
+  // Teardown: every role has left its item loop (normally or through the
+  // abort flag); free TMEM once no MMA is in flight.
+  if (warp == kMmaWarp && lane == 0 && *abort) {
+    umma_commit(bar(kPBarTeardown));  // tracks every MMA this thread issued
+    int never = 0;
+    mbar_wait(bar(kPBarTeardown), 0, &never);
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
 // cuTensorMapEncodeTiled from the driver, looked up once per process.
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -881,7 +1351,7 @@ cudaError_t launch_extend(const PoolGeom &g, int32_t layer, const void *q,
                           const int32_t *page_table, int64_t table_stride,
                           const int32_t *table_idx, const int32_t *seq_lens, int32_t batch,
                           int32_t total_q, int32_t hq, float scale, const ExtendLayout &lay,
-                          void *workspace, unsigned *err, cudaStream_t stream,
+                          void *workspace, int32_t sm_count, unsigned *err, cudaStream_t stream,
                           const ExtendMode &mode) {
   const uint64_t ws_rows = 2ull * static_cast<uint64_t>(g.hkv) * static_cast<uint64_t>(lay.cap_rows);
   const uint64_t q_rows = static_cast<uint64_t>(total_q) * hq;
@@ -943,6 +1413,9 @@ cudaError_t launch_extend(const PoolGeom &g, int32_t layer, const void *q,
   // one gather CTA per 16 rows of a region, plus the planner
   const dim3 ggrid(static_cast<unsigned>(lay.cap_rows / kGatherKeys + 1));
   const dim3 grid(g.hkv, static_cast<unsigned>(tiles));
+  // persistent form: one CTA per SM (whole-SM shared memory), at most one per work item
+  const int64_t items = static_cast<int64_t>(g.hkv) * tiles;
+  const dim3 pgrid(static_cast<unsigned>(std::min<int64_t>(sm_count > 0 ? sm_count : 1, items)));
   cudaError_t e;
   if (g.d == 128) {
     e = ga.k_new ? launch_pdl(extend_gather_kernel<128, true>, ggrid, dim3(kGatherThreads), 0,
@@ -950,22 +1423,38 @@ cudaError_t launch_extend(const PoolGeom &g, int32_t layer, const void *q,
                  : launch_pdl(extend_gather_kernel<128, false>, ggrid, dim3(kGatherThreads), 0,
                               stream, ga);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(extend_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Smem<128>::kTotal);
-    if (e != cudaSuccess) return e;
-    e = launch_pdl(extend_tc_kernel<128>, grid, dim3(kThreads), Smem<128>::kTotal, stream,
-                   kv_map, q_map, a);
+    if (PKV_EXTEND_PERSISTENT) {
+      e = cudaFuncSetAttribute(extend_tc_persistent_kernel<128>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, Smem<128>::kTotal);
+      if (e != cudaSuccess) return e;
+      e = launch_pdl(extend_tc_persistent_kernel<128>, pgrid, dim3(kThreads), Smem<128>::kTotal,
+                     stream, kv_map, q_map, a);
+    } else {
+      e = cudaFuncSetAttribute(extend_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               Smem<128>::kTotal);
+      if (e != cudaSuccess) return e;
+      e = launch_pdl(extend_tc_kernel<128>, grid, dim3(kThreads), Smem<128>::kTotal, stream,
+                     kv_map, q_map, a);
+    }
   } else {
     e = ga.k_new ? launch_pdl(extend_gather_kernel<64, true>, ggrid, dim3(kGatherThreads), 0,
                               stream, ga)
                  : launch_pdl(extend_gather_kernel<64, false>, ggrid, dim3(kGatherThreads), 0,
                               stream, ga);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(extend_tc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Smem<64>::kTotal);
-    if (e != cudaSuccess) return e;
-    e = launch_pdl(extend_tc_kernel<64>, grid, dim3(kThreads), Smem<64>::kTotal, stream,
-                   kv_map, q_map, a);
+    if (PKV_EXTEND_PERSISTENT) {
+      e = cudaFuncSetAttribute(extend_tc_persistent_kernel<64>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, Smem<64>::kTotal);
+      if (e != cudaSuccess) return e;
+      e = launch_pdl(extend_tc_persistent_kernel<64>, pgrid, dim3(kThreads), Smem<64>::kTotal,
+                     stream, kv_map, q_map, a);
+    } else {
+      e = cudaFuncSetAttribute(extend_tc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               Smem<64>::kTotal);
+      if (e != cudaSuccess) return e;
+      e = launch_pdl(extend_tc_kernel<64>, grid, dim3(kThreads), Smem<64>::kTotal, stream,
+                     kv_map, q_map, a);
+    }
   }
   return e;
 }

@@ -423,7 +423,7 @@ static pkv_status extend_call(const pkv_pool *pool, int32_t layer, const void *q
   mode.kv_row_stride = kv_row_stride;
   cudaError_t e = pkv::launch_extend(g, layer, q, qo_indptr, o, lse, page_table, table_stride,
                                      table_idx, seq_lens, batch, total_q, num_q_heads, scale, lay,
-                                     workspace, d->err, stream, mode);
+                                     workspace, d->sm_count, d->err, stream, mode);
   return e == cudaSuccess ? PKV_OK : cuda_fail(e, "extend launch");
 }
 

@@ -111,7 +111,7 @@ cudaError_t launch_extend(const PoolGeom &g, int32_t layer, const void *q,
                           const int32_t *page_table, int64_t table_stride,
                           const int32_t *table_idx, const int32_t *seq_lens, int32_t batch,
                           int32_t total_q, int32_t hq, float scale, const ExtendLayout &lay,
-                          void *workspace, unsigned *err, cudaStream_t stream,
+                          void *workspace, int32_t sm_count, unsigned *err, cudaStream_t stream,
                           const ExtendMode &mode = ExtendMode());
 
 cudaError_t launch_merge(const float *o_a, const float *lse_a, const float *o_b,
