@@ -57,10 +57,10 @@ MEASURED_TRAFFIC = {
     "decode": {"sources": ['decode.cu', 'decode_common.cuh', 'pkv_common.cuh'],
                "sha256": "1946f3ac4ab631093fbc25b82b65651fec5fd69a755e14f8055eb573eab8ac9f",
                "bytes": 625499392},
-    # extend_gather_kernel + extend_tc_kernel, chunked-prefill extend
+    # extend_gather_kernel + extend_tc_persistent_kernel, chunked-prefill extend
     "extend": {"sources": ['extend.cu', 'tc_common.cuh', 'pkv_common.cuh'],
-               "sha256": "83c54f87e8cd8696c109037f258a1557ecc5ee18817d22544846d2d5d4e6f5b0",
-               "bytes": 520547104},
+               "sha256": "9315e2509f10a1486774db1bd193fa8179cb8d6d987346e8bb87c6980e80f3de",
+               "bytes": 522519552},
     # cascade_prefix_kernel + decode_kernel (suffix) + decode_merge_narrow_kernel,
     # radix-shared decode through cascade decode
     "cascade": {"sources": ['cascade.cu', 'decode.cu', 'decode_common.cuh', 'tc_common.cuh', 'pkv_common.cuh'],
@@ -663,7 +663,7 @@ def _extend_workload(args, dev, peaks, peak_src, flush, steps, warm):
         "ms_step_fused_store": round(ft, 4),
         "flops": fl, "tokens_per_s": round(case.total_q / (min(st, ft) * 1e-3), 1),
         "roofline": {**roofline("tensor", fl, at, peaks, peak_src),
-                     "kernel": ("pkv_paged_extend_attn: extend_gather_kernel + extend_tc_kernel "
+                     "kernel": ("pkv_paged_extend_attn: extend_gather_kernel + extend_tc_persistent_kernel "
                                 "(both launches inside the timed duration)"),
                      "traffic": measured_traffic("extend", args.extend_traffic),
                      "algorithmic_bytes": extend_bytes(case)}}

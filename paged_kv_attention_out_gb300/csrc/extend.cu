@@ -15,8 +15,10 @@
 //       keys present (a host bound on their sum), not by batch x max length;
 //       one CTA row per 16 rows of that space, each finding its request by a
 //       prefix sum of the rounded lengths;
-//   extend_tc_kernel      the attention, which then reads every 128-key K or
-//       V tile with plain 2-D TMA boxes instead of row gathers.
+//   extend_tc_persistent_kernel (extend_tc_kernel with PKV_EXTEND_PERSISTENT
+//       0)  the attention, which then reads every 128-key K or V tile with
+//       plain 2-D TMA boxes instead of row gathers; one CTA per SM takes the
+//       blocks described below as work items (see "persistent form").
 //
 // Tiling. A CTA owns two 128-row query tiles X = 0, 1 of one kv head; a
 // tile holds 128 / g chunk tokens x the g q heads that read that kv head, so
@@ -48,6 +50,7 @@
 
 #include <algorithm>
 #include <mutex>
+#include <type_traits>
 
 #include "pkv_common.cuh"
 #include "pkv_internal.h"
@@ -867,6 +870,9 @@ enum : int {
 };
 static_assert(kPBarCount <= 32, "barrier area of Smem");
 
+constexpr std::integral_constant<int, 0> kTile0{};
+constexpr std::integral_constant<int, 1> kTile1{};
+
 // One work item as the producer publishes it (req < 0: no more items).
 struct ItemDesc {
   int req, kvh, j0, c, p, off, t_base;
@@ -1063,16 +1069,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                        ks > 0 ? 1u : 0u);
         umma_commit(bar(kPBarSFull + x));
       };
-      int pv_count[2] = {0, 0};  // P V products issued per query tile (all items)
-      int uses[2] = {0, 0};      // items that used query tile x (its O_X written out)
+      // Per query tile (scalars): P V products issued and items that used
+      // the tile, over all items.
+      int pv_count0 = 0, pv_count1 = 0, uses0 = 0, uses1 = 0;
       // O_x += P_x V(tile gt), j = the item's key tile; the item's first
       // product overwrites O_x once the previous item's output is read out.
-      auto pv = [&](int x, int j, uint32_t gt) -> bool {
-        if (j == 0 && uses[x] > 0 &&
-            !mbar_wait_fast(bar(kPBarOEmpty + x), (uses[x] - 1) & 1, abort))
+      auto pv = [&](auto xc, int j, uint32_t gt) -> bool {
+        constexpr int x = decltype(xc)::value;
+        int &pv_count = x == 0 ? pv_count0 : pv_count1;
+        const int uses = x == 0 ? uses0 : uses1;
+        if (j == 0 && uses > 0 && !mbar_wait_fast(bar(kPBarOEmpty + x), (uses - 1) & 1, abort))
           return false;
-        if (!mbar_wait_fast(bar(kPBarPFull + x), pv_count[x] & 1, abort)) return false;
-        ++pv_count[x];
+        if (!mbar_wait_fast(bar(kPBarPFull + x), pv_count & 1, abort)) return false;
+        ++pv_count;
         tc_fence_after_sync();
         const uint64_t dv = dv0 + (gt & 1) * kStageStep;
 #pragma unroll
@@ -1102,21 +1111,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; j < n_tiles && ok; ++j) {
           const uint32_t gj = g0 + static_cast<uint32_t>(j);
           const bool next = j + 1 < n_tiles;
-          if (j < n0) ok = pv(0, j, gj);
+          if (j < n0) ok = pv(kTile0, j, gj);
+          // O_0 is final once its last product is done (not held for tile 1's)
+          if (ok && j == n0 - 1) umma_commit(bar(kPBarOFull + 0));
           if (ok && next) ok = mbar_wait_fast(bar(kPBarFull + ((gj + 1) & 1)), ((gj + 1) >> 1) & 1, abort);
           if (!ok) break;
           tc_fence_after_sync();
           if (next && j + 1 < n0) qk(0, gj + 1);
-          if (j < n1 && !(ok = pv(1, j, gj))) break;
+          if (j < n1 && !(ok = pv(kTile1, j, gj))) break;
+          if (j == n1 - 1) umma_commit(bar(kPBarOFull + 1));
           umma_commit(bar(kPBarEmpty + (gj & 1)));
           if (next && j + 1 < n1) qk(1, gj + 1);
           if (j + 2 == n_tiles) umma_commit(bar(kPBarQEmpty));  // every S of the item issued
-          if (j == n0 - 1) umma_commit(bar(kPBarOFull + 0));
-          if (j == n1 - 1) umma_commit(bar(kPBarOFull + 1));
         }
         g = g0 + static_cast<uint32_t>(n_tiles);
-        ++uses[0];
-        if (n1 > 0) ++uses[1];
+        ++uses0;
+        if (n1 > 0) ++uses1;
       }
       if (!ok) {
         *abort = 1;
