@@ -905,10 +905,13 @@ __device__ __forceinline__ ItemDesc shfl_desc(ItemDesc d) {
   return d;
 }
 
+// q3_map: q as a 3-D bf16 tensor [total_q][Hq][D], box {64, g, 128 / g}
+// (one query tile's half: its tokens x the g q heads of one kv head, rows in
+// (token, head) order as the tile's rows), 128-byte swizzle.
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     extend_tc_persistent_kernel(const __grid_constant__ CUtensorMap kv_map,
-                                const __grid_constant__ CUtensorMap q_map, const ExtendArgs a) {
+                                const __grid_constant__ CUtensorMap q3_map, const ExtendArgs a) {
   using S = Smem<D>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ ItemDesc s_item[2];
@@ -944,6 +947,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(kPBarTeardown), 1);
     s_abort = 0;
     mbar_init_fence();
+  }
+  {
+    // Rows g * tpt .. 127 of a query tile (group not dividing 128) are
+    // never loaded: zero them once, so those rows' scores stay finite.
+    constexpr int kHalves = D / 64;
+    const int pad_rows = kM - a.group * tpt;
+    for (int i = tid; i < kQTiles * kHalves * pad_rows * 8; i += kThreads) {
+      const int chunk = i & 7, row = (i >> 3) % pad_rows, region = (i >> 3) / pad_rows;
+      *reinterpret_cast<uint4 *>(smem + S::kQ + region * (kM * 128) + (kM - pad_rows + row) * 128 +
+                                 chunk * 16) = make_uint4(0u, 0u, 0u, 0u);
+    }
+    fence_async_shared();  // generic-proxy writes, read by tcgen05.mma
   }
   if (warp == kMmaWarp) tmem_alloc(smem_addr(&s_tmem), kTmemCols);
   tc_fence_before_sync();
@@ -993,25 +1008,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (d.req < 0) break;
       const ItemGeom ig = item_geom(d, tpt);
       if (k >= 1 && !(ok = mbar_wait_warp(bar(kPBarQEmpty), (k - 1) & 1, abort))) break;
-      if (lane == 0) mbar_arrive_expect_tx(bar(kPBarQFull), kQTiles * S::kQBytes);
-      __syncwarp();
+      if (lane == 0) {
+        // Query tile x: tokens t_base + j0 + x tpt .. + tpt - 1, the g q heads
+        // of this kv head, as one 3-D box per 64-column half. Rows of tokens
+        // past the item (the next request's, or zeros past the last token)
+        // belong to no output row.
+        const uint32_t box_bytes = static_cast<uint32_t>(a.group * tpt) * 128u;
+        mbar_arrive_expect_tx(bar(kPBarQFull), kQTiles * kHalves * box_bytes);
 #pragma unroll
-      for (int x = 0; x < kQTiles; ++x) {
-        int qr[4];
+        for (int x = 0; x < kQTiles; ++x)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int r = 4 * lane + e;
-          const int tt = r / a.group;  // token within the query tile
-          const int tok = x * tpt + tt;
-          const int qt = (tt < tpt && tok < ig.tokens) ? d.t_base + d.j0 + tok : -1;
-          qr[e] = qt >= 0 ? qt * a.hq + d.kvh * a.group + (r % a.group) : -1;
-        }
-#pragma unroll
-        for (int h = 0; h < kHalves; ++h)
-          tma_gather4(sbase + S::kQ + static_cast<uint32_t>(x * S::kQBytes + h * (kM * 128) +
-                                                           (lane >> 1) * 1024 + (lane & 1) * 512),
-                      &q_map, h * 64, qr[0], qr[1], qr[2], qr[3], bar(kPBarQFull));
+          for (int h = 0; h < kHalves; ++h)
+            tma_load_3d(sbase + S::kQ + static_cast<uint32_t>(x * S::kQBytes + h * (kM * 128)),
+                        &q3_map, h * 64, d.kvh * a.group, d.t_base + d.j0 + x * tpt,
+                        bar(kPBarQFull));
       }
+      __syncwarp();
       ++q_loads;
       // first workspace rows of this request's K and V runs for this kv head
       const int k_run = d.kvh * a.cap_rows + d.off;
@@ -1325,6 +1337,21 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 // A 2-D bf16 tensor of `rows` rows of `cols` elements (row-major), read in
 // boxes of box_rows rows x 64 columns with 128-byte swizzle (box_rows = 1 for
 // tile::gather4); zeros outside.
+// q [total_q][Hq][D] bf16 as a 3-D tensor, box {64, g, tpt}, 128-byte
+// swizzle; zeros outside.
+bool q3_map_of(CUtensorMap *m, const void *q, uint64_t total_q, uint64_t hq, uint64_t d,
+               uint32_t g, uint32_t tpt) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {d, hq, total_q};
+  cuuint64_t strides[2] = {d * 2, hq * d * 2};
+  cuuint32_t box[3] = {64, g, tpt};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(q), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool bf16_map(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
   if (!enc) return false;
@@ -1415,7 +1442,11 @@ cudaError_t launch_extend(const PoolGeom &g, int32_t layer, const void *q,
   a.plan = ga.plan;
   CUtensorMap kv_map, q_map;
   if (!bf16_map(&kv_map, workspace, ws_rows, static_cast<uint64_t>(g.d), kN) ||
-      !bf16_map(&q_map, q, q_rows, static_cast<uint64_t>(g.d), 1))
+      !(PKV_EXTEND_PERSISTENT
+            ? q3_map_of(&q_map, q, static_cast<uint64_t>(total_q), static_cast<uint64_t>(hq),
+                        static_cast<uint64_t>(g.d), static_cast<uint32_t>(a.group),
+                        static_cast<uint32_t>(a.tokens_per_tile))
+            : bf16_map(&q_map, q, q_rows, static_cast<uint64_t>(g.d), 1)))
     return cudaErrorInvalidValue;
   const int64_t per_cta = static_cast<int64_t>(kQTiles) * a.tokens_per_tile;
   const int64_t tiles = (static_cast<int64_t>(total_q) + per_cta - 1) / per_cta + batch;

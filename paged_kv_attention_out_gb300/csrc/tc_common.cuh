@@ -276,6 +276,19 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, int 
       : "memory");
 }
 
+// TMA tile load of a 3-D box (coordinates x innermost, then y, z) into
+// shared memory at dst, laid out as the box's rows of 128 bytes in (z, y)
+// order with the map's swizzle. Completion counts the box's bytes down on
+// `bar`.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *tmap, int x, int y, int z,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z), "r"(bar)
+      : "memory");
+}
+
 // One test of the phase (may suspend the thread briefly in hardware, waking
 // when the phase completes).
 __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {

@@ -22,6 +22,21 @@ def test_extend_600_requests():
     check_against_oracle(case)
 
 
+@pytest.mark.parametrize("scale", [-0.125, 0.0, 0.125])
+def test_extend_many_items_per_sm_any_scale(scale):
+    """About seven (kv head, block) work items per SM for the persistent
+    attention kernel, with chunk lengths spanning one and two query tiles
+    (items whose second query tile is empty, and items whose second tile sees
+    one key tile more), under a negative, zero and positive scale (the sign
+    folded into each item's Q)."""
+    rng = np.random.default_rng(74)
+    chunks = rng.integers(1, 121, size=420)
+    prefix = rng.integers(0, 300, size=420)
+    case = W.random_case(74, kind="extend", seq_lens=(prefix + chunks).tolist(),
+                         chunk_lens=chunks.tolist(), Hq=8, Hkv=2, D=64, P=16, scale=scale)
+    check_against_oracle(case)
+
+
 def test_decode_3000_requests():
     rng = np.random.default_rng(72)
     case = W.random_case(72, seq_lens=rng.integers(1, 90, size=3000).tolist(), Hq=8, Hkv=2,
