@@ -917,6 +917,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ ItemDesc s_item[2];
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
+  // Per softmax warp: items taken, S tiles taken, items that used its query
+  // tile (kept here, not in registers, across the warp's key-tile loop).
+  __shared__ int s_sm_state[kSoftmaxWarps][3];
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
@@ -1157,10 +1160,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t srow = tmem + lane_base + kTmemS + x * kN;
     const uint32_t orow_t = tmem + lane_base + kTmemO + x * D;
-    int s_count = 0;  // S tiles of query tile x taken (all items)
-    int uses = 0;     // items that used query tile x
+    int *state = s_sm_state[warp];  // [0] items, [1] S tiles, [2] items that used tile x
+    if (lane == 0) state[0] = state[1] = state[2] = 0;
+    __syncwarp();
     bool ok = true;
-    for (int k = 0; ok; ++k) {
+    for (;;) {
+      const int k = state[0];
       const int slot = k & 1;
       if (!(ok = mbar_wait_warp(bar(kPBarItemFull + slot), (k >> 1) & 1, abort))) break;
       const ItemDesc d = s_item[slot];
@@ -1197,8 +1202,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_async_shared();  // generic-proxy writes, read next by tcgen05.mma
         mbar_arrive(bar(kPBarQReady));
       }
-      for (int j = 0; ok && j < n_x; ++j, ++s_count) {
-        if (!(ok = mbar_wait_warp(bar(kPBarSFull + x), s_count & 1, abort))) break;
+      const int s_par = state[1] & 1;  // parity of this item's first S tile
+      for (int j = 0; ok && j < n_x; ++j) {
+        if (!(ok = mbar_wait_warp(bar(kPBarSFull + x), (s_par ^ j) & 1, abort))) break;
         tc_fence_after_sync();
         float v[kN];
         tmem_ld32(srow + 0, *reinterpret_cast<float(*)[32]>(&v[0]));
@@ -1269,8 +1275,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(bar(kPBarPFull + x));
       }
       if (!ok) break;
+      __syncwarp();
+      if (lane == 0) {
+        state[0] = k + 1;
+        state[1] += n_x;
+      }
+      __syncwarp();
       if (n_x == 0) continue;
-      if (!(ok = mbar_wait_warp(bar(kPBarOFull + x), uses & 1, abort))) break;
+      if (!(ok = mbar_wait_warp(bar(kPBarOFull + x), state[2] & 1, abort))) break;
       tc_fence_after_sync();
       const float inv = l > 0.f ? 1.f / l : 0.f;
       const int64_t orow =
@@ -1296,7 +1308,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (valid && a.lse) a.lse[orow] = l > 0.f ? (m_used + __log2f(l)) * kLn2 : -INFINITY;
       tc_fence_before_sync();
       mbar_arrive(bar(kPBarOEmpty + x));  // O_x read out: the next item may overwrite it
-      ++uses;
+      __syncwarp();
+      if (lane == 0) ++state[2];
+      __syncwarp();
     }
     if (!ok) {
       *abort = 1;
