@@ -1287,21 +1287,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float inv = l > 0.f ? 1.f / l : 0.f;
       const int64_t orow =
           static_cast<int64_t>(valid ? qtok : 0) * a.hq + d.kvh * a.group + (r % a.group);
-#pragma unroll 1
-      for (int cb = 0; cb < D / 32; ++cb) {
-        float o[32];
-        tmem_ld32(orow_t + cb * 32, o);
+      {
+        // The whole row of O at once (the score registers are free here):
+        // one TMEM round trip instead of one per 32 columns.
+        float o[D];
+#pragma unroll
+        for (int cb = 0; cb < D / 32; ++cb)
+          tmem_ld32(orow_t + cb * 32, *reinterpret_cast<float(*)[32]>(&o[cb * 32]));
         tmem_ld_wait();
         if (valid) {
-          uint4 *dst = reinterpret_cast<uint4 *>(a.o + orow * D + cb * 32);
+          uint4 *dst = reinterpret_cast<uint4 *>(a.o + orow * D);
 #pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
+          for (int q8 = 0; q8 < D / 8; ++q8) {
             uint4 u;
-            u.x = pack_bf16(o[q4 * 8 + 0] * inv, o[q4 * 8 + 1] * inv);
-            u.y = pack_bf16(o[q4 * 8 + 2] * inv, o[q4 * 8 + 3] * inv);
-            u.z = pack_bf16(o[q4 * 8 + 4] * inv, o[q4 * 8 + 5] * inv);
-            u.w = pack_bf16(o[q4 * 8 + 6] * inv, o[q4 * 8 + 7] * inv);
-            dst[q4] = u;
+            u.x = pack_bf16(o[q8 * 8 + 0] * inv, o[q8 * 8 + 1] * inv);
+            u.y = pack_bf16(o[q8 * 8 + 2] * inv, o[q8 * 8 + 3] * inv);
+            u.z = pack_bf16(o[q8 * 8 + 4] * inv, o[q8 * 8 + 5] * inv);
+            u.w = pack_bf16(o[q8 * 8 + 6] * inv, o[q8 * 8 + 7] * inv);
+            dst[q8] = u;
           }
         }
       }
