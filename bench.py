@@ -59,13 +59,13 @@ MEASURED_TRAFFIC = {
                "bytes": 625499392},
     # extend_gather_kernel + extend_tc_persistent_kernel, chunked-prefill extend
     "extend": {"sources": ['extend.cu', 'tc_common.cuh', 'pkv_common.cuh'],
-               "sha256": "9315e2509f10a1486774db1bd193fa8179cb8d6d987346e8bb87c6980e80f3de",
-               "bytes": 522519552},
+               "sha256": "50dcb48e70dfd0686d70537f8678bbe99f6fc0c3a5517244ecd49be58ae7eb7f",
+               "bytes": 518785792},
     # cascade_prefix_kernel + decode_kernel (suffix) + decode_merge_narrow_kernel,
     # radix-shared decode through cascade decode
     "cascade": {"sources": ['cascade.cu', 'decode.cu', 'decode_common.cuh', 'tc_common.cuh', 'pkv_common.cuh'],
-                "sha256": "14f710b0ce874b9bdbde9fb98e7430214229063dd2ce089aac515266ad9b2ea2",
-                "bytes": 372247776},
+                "sha256": "7e12b981d9f98340b348997b9fb639f09932307628285b59d7298fa2e42cbb2a",
+                "bytes": 372238272},
 }
 
 
