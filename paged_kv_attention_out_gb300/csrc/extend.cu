@@ -970,7 +970,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = s_tmem;
   grid_dependency_wait();  // the schedule and the K/V runs come from the gather kernel
 
-  if (warp >= kProducerWarp) {
+  if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
     // Per item: take the next item from the counter and publish it; once
     // every S of the previous item is done, load the item's two Q tiles
