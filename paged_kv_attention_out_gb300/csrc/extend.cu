@@ -13,17 +13,17 @@
 //       the pool once per call. The runs of the requests lie back to back in
 //       request order, [2][Hkv][cap_rows][D], so the workspace is sized by the
 //       keys present (a host bound on their sum), not by batch x max length;
-//       one CTA row per 16 rows of that space, each finding its request by a
-//       prefix sum of the rounded lengths;
-//   extend_tc_persistent_kernel (extend_tc_kernel with PKV_EXTEND_PERSISTENT
-//       0)  the attention, which then reads every 128-key K or V tile with
-//       plain 2-D TMA boxes instead of row gathers; one CTA per SM takes the
-//       blocks described below as work items (see "persistent form").
+//       one CTA per 16 rows of that space, each finding its request by a
+//       prefix sum of the rounded lengths; the last CTA builds the block
+//       schedule;
+//   extend_tc_persistent_kernel  the attention, which then reads every
+//       128-key K or V tile with plain 2-D TMA boxes instead of row gathers;
+//       one CTA per SM takes blocks of the schedule as work items.
 //
-// Tiling. A CTA owns two 128-row query tiles X = 0, 1 of one kv head; a
-// tile holds 128 / g chunk tokens x the g q heads that read that kv head, so
-// every K/V tile loaded feeds 2 x 128 query rows. It walks the visible keys
-// in tiles of 128; per key tile j and query tile X:
+// Tiling. A block (work item) is two 128-row query tiles X = 0, 1 of one kv
+// head; a tile holds 128 / g chunk tokens x the g q heads that read that kv
+// head, so every K/V tile loaded feeds 2 x 128 query rows. It walks the
+// visible keys in tiles of 128; per key tile j and query tile X:
 //   S_X  = Q_X K_j^T           tcgen05.mma, M=128 N=128 K=D, fp32 in TMEM
 //   P_X  = exp2(scale*S_X - m) softmax warps of tile X, bf16 back into TMEM
 //                              over the first half of S_X
@@ -39,8 +39,8 @@
 //              only on tiles that cross some row's last key; then O / l ->
 //              bf16 and lse.
 //   warp 8     TMEM allocation and the single MMA-issuing thread.
-//   warp 9     producer: the Q rows (TMA tile::gather4, 4 rows per
-//              instruction), then the K and V tiles (2-D TMA boxes of 128
+//   warp 9     producer: takes the work items, then per item the Q tiles
+//              (3-D TMA boxes) and the K and V tiles (2-D TMA boxes of 128
 //              keys x 64 columns, 128-byte swizzle) into two stages; a stage
 //              is refilled once every MMA that reads it is done.
 // Every hand-off is an mbarrier; every wait is bounded (tc_common.cuh).
@@ -89,21 +89,6 @@ struct Smem {
 // takes it from there as its A operand.
 constexpr uint32_t kTmemS = 0;
 constexpr uint32_t kTmemO = 256;
-
-// Barrier indices. Every barrier that is waited on with a parity completes
-// at most once between two waits of the same waiter (so a waiter is never
-// two phases behind): per-buffer barriers for everything double-buffered.
-enum : int {
-  kBarFull = 0,       // [2] producer: K and V tiles of stage s landed (TMA bytes)
-  kBarEmpty = 2,      // [2] MMA: every MMA reading stage s done
-  kBarSFull = 4,      // [2] MMA: S_X ready (and every earlier MMA done)
-  kBarPFull = 6,      // [2] softmax X: P_X written to TMEM (and O_X rescaled)
-  kBarOFull = 8,      // MMA: every MMA done, O final
-  kBarTeardown = 9,   // MMA: everything issued has finished (abort path)
-  kBarQFull = 10,     // producer: both Q tiles landed (TMA bytes)
-  kBarQReady = 11,    // softmax warps: Q negated / zeroed in place (q_mode != 0)
-  kBarCount = 12,
-};
 
 struct GatherArgs {
   const __nv_bfloat16 *pool;  // plane (c, layer) starts at ((c * L + layer) * slots) rows
@@ -464,381 +449,11 @@ __device__ __forceinline__ void gather_body(const GatherArgs &a) {
   }
 }
 
-// kv_map: the workspace as a 2-D bf16 tensor [2 * Hkv * cap_rows rows][D],
-// box {64, 128}; q_map: q as [total_q * Hq rows][D], box {64, 1}. Both with
-// 128-byte swizzle.
-template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
-    extend_tc_kernel(const __grid_constant__ CUtensorMap kv_map,
-                     const __grid_constant__ CUtensorMap q_map, const ExtendArgs a) {
-  using S = Smem<D>;
-  extern __shared__ uint8_t smem_raw[];
-  __shared__ int s_req, s_j0, s_c, s_p, s_off;
-  __shared__ uint32_t s_tmem;
-  __shared__ int s_abort;
-  const int tid = threadIdx.x;
-  const int warp = tid >> 5;
-  const int lane = tid & 31;
-  const int kvh = blockIdx.x;
-  const int tpt = a.tokens_per_tile;
-
-  grid_dependency_wait();  // K/V come from the gather kernel
-  if (tid == 0) {
-    // This CTA's (request, first token) from the longest-first schedule;
-    // the schedule holds only well-formed requests.
-    const int rank = blockIdx.y;
-    const int *sorted = a.plan + plan_sorted(a.nbuck, a.max_blocks);
-    int req = -1, j0 = 0, c = 0, p = 0, off = 0;
-    if (rank < a.plan[0]) {
-      req = sorted[2 * rank];
-      j0 = sorted[2 * rank + 1];
-      c = a.qo_indptr[req + 1] - a.qo_indptr[req];
-      p = a.seq_lens[req] - c;
-      off = a.plan[plan_offsets(a.nbuck, a.max_blocks) + req];
-    }
-    s_off = off;
-    s_req = req;
-    s_j0 = j0;
-    s_c = c;
-    s_p = p;
-    s_abort = 0;
-  }
-  __syncthreads();
-  const int req = s_req;
-  if (req < 0) return;
-
-  uint8_t *smem = reinterpret_cast<uint8_t *>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  const uint32_t sbase = smem_addr(smem);
-  const uint32_t bars = sbase + S::kBars;
-  auto bar = [&](int i) { return bars + 8u * static_cast<uint32_t>(i); };
-  volatile int *abort = &s_abort;
-
-  const int j0 = s_j0, c = s_c, p = s_p;
-  const int t_base = a.qo_indptr[req];
-  const int tokens = min(kQTiles * tpt, c - j0);  // chunk tokens of this CTA
-  // Query tile X holds tokens X*tpt .. X*tpt + tok_X - 1 of the CTA and
-  // walks key tiles 0 .. n_X - 1 (n_1 = 0 when it holds no token).
-  const int tok1 = max(0, min(tpt, tokens - tpt));
-  const int tok0 = min(tpt, tokens);
-  // p is the cached prefix: query tile X's last token sees p + j0 + X tpt +
-  // tok_X keys.
-  const int n0 = (p + j0 + tok0 + kN - 1) / kN;
-  const int n1 = tok1 == 0 ? 0 : (p + j0 + tpt + tok1 + kN - 1) / kN;
-  const int n_tiles = max(n0, n1);  // >= 1: a CTA holds at least one token
-
-  if (tid == 0) {
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(bar(kBarFull + i), 1);  // the producer's expect_tx arrival
-      mbar_init(bar(kBarEmpty + i), 1);
-      mbar_init(bar(kBarSFull + i), 1);
-      mbar_init(bar(kBarPFull + i), 128);  // the four warps of one query tile
-    }
-    mbar_init(bar(kBarOFull), 1);
-    mbar_init(bar(kBarTeardown), 1);
-    mbar_init(bar(kBarQFull), 1);
-    mbar_init(bar(kBarQReady), kSoftmaxWarps * 32);
-    mbar_init_fence();
-  }
-  if (warp == kMmaWarp) tmem_alloc(smem_addr(&s_tmem), kTmemCols);
-  tc_fence_before_sync();
-  __syncthreads();
-  tc_fence_after_sync();
-  const uint32_t tmem = s_tmem;
-
-  if (warp >= kProducerWarp) {
-    // ------------------------------------------------------------ producer
-    // Loads both Q tiles (lane l: rows 4 l .. 4 l + 3 of each, all 64-column
-    // halves; rows past the CTA's tokens read as zeros), then per key tile
-    // the K and V boxes into stage j % 2 once every MMA reading that stage
-    // (tile j - 2) is done. Lane 0 issues the tile loads.
-    constexpr int kHalves = D / 64;
-    bool ok = true;
-    if (lane == 0) mbar_arrive_expect_tx(bar(kBarQFull), kQTiles * S::kQBytes);
-    __syncwarp();
-#pragma unroll
-    for (int x = 0; x < kQTiles; ++x) {
-      int qr[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int r = 4 * lane + e;
-        const int tt = r / a.group;  // token within the query tile
-        const int tok = x * tpt + tt;
-        const int qt = (tt < tpt && tok < tokens) ? t_base + j0 + tok : -1;
-        qr[e] = qt >= 0 ? qt * a.hq + kvh * a.group + (r % a.group) : -1;
-      }
-#pragma unroll
-      for (int h = 0; h < kHalves; ++h)
-        tma_gather4(sbase + S::kQ + static_cast<uint32_t>(x * S::kQBytes + h * (kM * 128) +
-                                                         (lane >> 1) * 1024 + (lane & 1) * 512),
-                    &q_map, h * 64, qr[0], qr[1], qr[2], qr[3], bar(kBarQFull));
-    }
-    // first workspace rows of this request's K and V runs for this kv head
-    const int k_run = kvh * a.cap_rows + s_off;
-    const int v_run = (a.hkv + kvh) * a.cap_rows + s_off;
-    int issued = 0;
-    for (int j = 0; j < n_tiles; ++j) {
-      const int s = j & 1;
-      if (j >= 2 && !(ok = mbar_wait_warp(bar(kBarEmpty + s), ((j >> 1) - 1) & 1, abort))) break;
-      if (lane == 0) {
-        const uint32_t dst = sbase + S::kKV + s * 2 * S::kTileBytes;
-        mbar_arrive_expect_tx(bar(kBarFull + s), 2 * S::kTileBytes);
-#pragma unroll
-        for (int h = 0; h < kHalves; ++h) {
-          tma_load_2d(dst + h * (kN * 128), &kv_map, h * 64, k_run + j * kN, bar(kBarFull + s));
-          tma_load_2d(dst + S::kTileBytes + h * (kN * 128), &kv_map, h * 64, v_run + j * kN,
-                      bar(kBarFull + s));
-        }
-      }
-      __syncwarp();
-      ++issued;
-    }
-    if (!ok) *abort = 1;
-    if (*abort && lane == 0) {
-      // Let every issued copy land before the CTA can exit: TMA writes to
-      // this CTA's shared memory need no other input to finish.
-      int never = 0;
-      mbar_wait(bar(kBarQFull), 0, &never);
-      for (int t = issued > 2 ? issued - 2 : 0; t < issued; ++t)
-        mbar_wait(bar(kBarFull + (t & 1)), (t >> 1) & 1, &never);
-    }
-  } else if (warp == kMmaWarp) {
-    // ------------------------------------------------------------ MMA issuer
-    // Order: S_0(0), S_1(0), then per key tile j: PV_0(j), S_0(j+1),
-    // PV_1(j), S_1(j+1). tcgen05.mma ops of one thread run in issue order,
-    // so S_X(j+1) overwrites P_X(j) only after PV_X(j) has read it, and a
-    // completed S_X(j+1) implies a completed PV_X(j) (O_X is then stable).
-    // An MMA issue returns about when the tensor core takes it, so the work
-    // between issues is kept small: inline barrier tests, three commits per
-    // key tile.
-    if (lane == 0) {
-      constexpr uint32_t idesc_qk = umma_idesc_bf16(kM, kN, 0, 0);
-      constexpr uint32_t idesc_pv = umma_idesc_bf16(kM, D, 0, 1);
-      // Descriptors are built once; a k-step adds its byte offset / 16 to the
-      // start-address field (addresses stay below 256 KB, so no carry).
-      const uint64_t dq0 = umma_desc_sw128(sbase + S::kQ, 16, 1024);
-      const uint64_t dk0 = umma_desc_sw128(sbase + S::kKV, 16, 1024);
-      const uint64_t dv0 = umma_desc_sw128(sbase + S::kKV + S::kTileBytes, kN * 128, 1024);
-      constexpr uint64_t kStageStep = (2 * S::kTileBytes) >> 4;
-      auto kstep = [](int ks, int rows) -> uint64_t {
-        return static_cast<uint64_t>(((ks >> 2) * (rows * 128) + (ks & 3) * 32) >> 4);
-      };
-      auto qk = [&](int x, int j) {
-        const uint64_t dq = dq0 + static_cast<uint64_t>((x * S::kQBytes) >> 4);
-        const uint64_t dk = dk0 + (j & 1) * kStageStep;
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks)
-          umma_bf16_ss(tmem + kTmemS + x * kN, dq + kstep(ks, kM), dk + kstep(ks, kN), idesc_qk,
-                       ks > 0 ? 1u : 0u);
-        umma_commit(bar(kBarSFull + x));
-      };
-      auto pv = [&](int x, int j) -> bool {
-        if (!mbar_wait_fast(bar(kBarPFull + x), j & 1, abort)) return false;
-        tc_fence_after_sync();
-        const uint64_t dv = dv0 + (j & 1) * kStageStep;
-#pragma unroll
-        for (int ks = 0; ks < kN / 16; ++ks)
-          umma_bf16_ts(tmem + kTmemO + x * D, tmem + kTmemS + x * kN + ks * 8,
-                       dv + ks * (2048 >> 4), idesc_pv, (j > 0 || ks > 0) ? 1u : 0u);
-        return true;
-      };
-      bool ok = mbar_wait_fast(bar(a.q_mode ? kBarQReady : kBarQFull), 0, abort) &&
-                mbar_wait_fast(bar(kBarFull), 0, abort);
-      if (ok) {
-        tc_fence_after_sync();
-        qk(0, 0);
-        if (n1 > 0) qk(1, 0);
-      }
-      for (int j = 0; j < n_tiles && ok; ++j) {
-        const int s = j & 1;
-        const bool next = j + 1 < n_tiles;
-        if (j < n0) ok = pv(0, j);
-        if (ok && next) ok = mbar_wait_fast(bar(kBarFull + (s ^ 1)), ((j + 1) >> 1) & 1, abort);
-        if (!ok) break;
-        tc_fence_after_sync();
-        if (next && j + 1 < n0) qk(0, j + 1);
-        if (j < n1 && !(ok = pv(1, j))) break;
-        umma_commit(bar(kBarEmpty + s));
-        if (next && j + 1 < n1) qk(1, j + 1);
-      }
-      if (ok) {
-        umma_commit(bar(kBarOFull));
-      } else {
-        *abort = 1;
-        flag_error(a.err, kErrTimeout);
-      }
-    }
-  } else {
-    // ------------------------------------------------------------ softmax
-    // Query tile x = warp / 4; warp w owns TMEM lanes 32 (w % 4) .. + 31,
-    // one query row per thread, whole rows of S.
-    const int quarter = warp & 3;
-    const int x = warp >> 2;
-    const int n_x = x == 0 ? n0 : n1;
-    const int r = quarter * 32 + lane;  // query row == TMEM lane
-    const int tt = r / a.group;         // token within the query tile
-    const int tok = x * tpt + tt;       // token within the CTA
-    const int qtok = (tt < tpt && tok < tokens) ? t_base + j0 + tok : -1;
-    const bool valid = qtok >= 0;
-    // last key of the tile's first token, and the last key this row may see
-    const int min_limit = p + j0 + x * tpt;
-    const int limit = min_limit + (valid ? tt : 0);
-    const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-    const uint32_t srow = tmem + lane_base + kTmemS + x * kN;
-    const uint32_t orow_t = tmem + lane_base + kTmemO + x * D;
-    float m_used = -INFINITY, l = 0.f;
-    bool ok = true;
-    if (a.q_mode != 0) {
-      // Fold the softmax scale's sign into Q once (both query tiles, all
-      // eight softmax warps), before the first S = Q K^T is issued.
-      ok = mbar_wait_warp(bar(kBarQFull), 0, abort);
-      if (ok) {
-        uint4 *qs = reinterpret_cast<uint4 *>(smem + S::kQ);
-        const uint32_t flip = 0x80008000u;  // the sign bits of a bf16 pair
-        for (int i = tid; i < kQTiles * S::kQBytes / 16; i += kSoftmaxWarps * 32) {
-          uint4 w = qs[i];
-          if (a.q_mode == 1) {
-            w.x ^= flip;
-            w.y ^= flip;
-            w.z ^= flip;
-            w.w ^= flip;
-          } else {
-            w = make_uint4(0u, 0u, 0u, 0u);
-          }
-          qs[i] = w;
-        }
-        fence_async_shared();  // generic-proxy writes, read next by tcgen05.mma
-      }
-      mbar_arrive(bar(kBarQReady));
-    }
-    for (int j = 0; ok && j < n_x; ++j) {
-      if (!(ok = mbar_wait_warp(bar(kBarSFull + x), j & 1, abort))) break;
-      tc_fence_after_sync();
-      float v[kN];
-      tmem_ld32(srow + 0, *reinterpret_cast<float(*)[32]>(&v[0]));
-      tmem_ld32(srow + 32, *reinterpret_cast<float(*)[32]>(&v[32]));
-      tmem_ld32(srow + 64, *reinterpret_cast<float(*)[32]>(&v[64]));
-      tmem_ld32(srow + 96, *reinterpret_cast<float(*)[32]>(&v[96]));
-      tmem_ld_wait();
-      const int key0 = j * kN;
-      if (key0 + kN - 1 > min_limit) {  // tile crosses some row's last key (warp-uniform)
-#pragma unroll
-        for (int cc = 0; cc < kN; ++cc) v[cc] = key0 + cc <= limit ? v[cc] : -INFINITY;
-      }
-      // Row max of the raw scores; scale_log2 > 0 commutes with max (a
-      // negative or zero softmax scale was folded into Q, see QMode).
-      float mx0 = fmaxf(v[0], v[1]), mx1 = fmaxf(v[2], v[3]);
-      float mx2 = fmaxf(v[4], v[5]), mx3 = fmaxf(v[6], v[7]);
-#pragma unroll
-      for (int cc = 8; cc < kN; cc += 8) {
-        mx0 = max3f(mx0, v[cc], v[cc + 1]);
-        mx1 = max3f(mx1, v[cc + 2], v[cc + 3]);
-        mx2 = max3f(mx2, v[cc + 4], v[cc + 5]);
-        mx3 = max3f(mx3, v[cc + 6], v[cc + 7]);
-      }
-      const float mt = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * a.scale_log2;
-      // Lazy rescale: move the reference max only when a row's max grew by
-      // more than 2^kRescaleThreshold (warp-uniform: tcgen05.ld/st are
-      // .sync.aligned, so every lane takes part, with factor 1 where its
-      // row did not move).
-      const bool rescale = j > 0 && __any_sync(0xffffffffu, mt > m_used + kRescaleThreshold);
-      float f = 1.f;
-      if (j == 0) {
-        m_used = mt;  // may be -inf: a row with no visible key in this tile
-      } else if (rescale) {
-        const float m_new = fmaxf(m_used, mt);
-        f = m_used == -INFINITY ? 0.f : fast_exp2(m_used - m_new);
-        m_used = m_new;
-      }
-      const float nm = m_used == -INFINITY ? 0.f : -m_used;
-      float sa0 = 0.f, sa1 = 0.f, sb0 = 0.f, sb1 = 0.f;
-#pragma unroll
-      for (int cc = 0; cc < kN; cc += 32) {
-        uint32_t w[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          float y0, y1;
-          fma2(y0, y1, v[cc + 2 * e], v[cc + 2 * e + 1], a.scale_log2, nm);
-          y0 = fast_exp2(y0);
-          y1 = fast_exp2(y1);
-          if (e & 1)
-            add2(sb0, sb1, y0, y1);
-          else
-            add2(sa0, sa1, y0, y1);
-          w[e] = pack_bf16(y0, y1);
-        }
-        tmem_st16u(srow + cc / 2, w);  // P_x: keys cc .. cc + 31 -> columns cc/2 ..
-      }
-      l = l * f + ((sa0 + sa1) + (sb0 + sb1));
-      if (rescale) {
-        // O_x is stable: S_x(j) completed, so did PV_x(j - 1) before it.
-#pragma unroll 1
-        for (int cb = 0; cb < D / 32; ++cb) {
-          float o[32];
-          tmem_ld32(orow_t + cb * 32, o);
-          tmem_ld_wait();
-#pragma unroll
-          for (int q = 0; q < 32; ++q) o[q] *= f;
-          tmem_st32(orow_t + cb * 32, o);
-        }
-      }
-      tmem_st_wait();
-      tc_fence_before_sync();
-      mbar_arrive(bar(kBarPFull + x));
-    }
-    if (ok && n_x > 0) ok = mbar_wait_warp(bar(kBarOFull), 0, abort);
-    if (!ok) {
-      *abort = 1;
-      flag_error(a.err, kErrTimeout);
-    } else if (n_x > 0) {
-      tc_fence_after_sync();
-      const float inv = l > 0.f ? 1.f / l : 0.f;
-      const int64_t orow =
-          static_cast<int64_t>(valid ? qtok : 0) * a.hq + kvh * a.group + (r % a.group);
-#pragma unroll 1
-      for (int cb = 0; cb < D / 32; ++cb) {
-        float o[32];
-        tmem_ld32(orow_t + cb * 32, o);
-        tmem_ld_wait();
-        if (valid) {
-          uint4 *dst = reinterpret_cast<uint4 *>(a.o + orow * D + cb * 32);
-#pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            uint4 u;
-            u.x = pack_bf16(o[q4 * 8 + 0] * inv, o[q4 * 8 + 1] * inv);
-            u.y = pack_bf16(o[q4 * 8 + 2] * inv, o[q4 * 8 + 3] * inv);
-            u.z = pack_bf16(o[q4 * 8 + 4] * inv, o[q4 * 8 + 5] * inv);
-            u.w = pack_bf16(o[q4 * 8 + 6] * inv, o[q4 * 8 + 7] * inv);
-            dst[q4] = u;
-          }
-        }
-      }
-      if (valid && a.lse) a.lse[orow] = l > 0.f ? (m_used + __log2f(l)) * kLn2 : -INFINITY;
-    }
-  }
-
-  // Teardown: every role has left its loop (normally or through the abort
-  // flag); free TMEM once no MMA is in flight (the softmax waited for the
-  // final commit, or the abort path below waits for it).
-  if (warp == kMmaWarp && lane == 0 && *abort) {
-    // Tracks every MMA this thread issued; they need no other input to finish.
-    umma_commit(bar(kBarTeardown));
-    int never = 0;
-    mbar_wait(bar(kBarTeardown), 0, &never);
-  }
-  tc_fence_before_sync();
-  __syncthreads();
-  if (warp == kMmaWarp) {
-    tc_fence_after_sync();
-    tmem_dealloc(tmem, kTmemCols);
-  }
-}
-
-// ------------------------------------------------------------ persistent form
+// ------------------------------------------------------------ attention
 // One CTA per SM pulls work items, (kv head, block) pairs in longest-first
 // order, from a counter the planner zeroes (plan[1]); item i is block
 // i / Hkv of the schedule on kv head i % Hkv. The roles run the per-tile
-// pipeline above, continued across items: the producer publishes the next
+// pipeline described at the top, continued across items: the producer publishes the next
 // item (a two-slot descriptor ring) and loads its Q tiles as soon as every
 // S MMA of the current item is done, and its K/V tiles through the same
 // two-stage ring; the MMA thread issues the next item's first S while the
@@ -848,10 +463,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 // Every barrier keeps one phase sequence across items: tile counters for
 // the K/V stages and S/P hand-offs, item counters for the rest, counted per
 // query tile where a tile may sit out an item (no tokens), so a waiter is
-// never two phases behind.
-#ifndef PKV_EXTEND_PERSISTENT
-#define PKV_EXTEND_PERSISTENT 1  // 0: one CTA per block (extend_tc_kernel)
-#endif
+// never two phases behind (a barrier waited on with a parity completes at
+// most once between two waits of the same waiter).
 
 enum : int {
   kPBarFull = 0,        // [2] producer: K and V tiles of stage s landed (TMA bytes)
@@ -878,7 +491,9 @@ struct ItemDesc {
   int req, kvh, j0, c, p, off, t_base;
 };
 
-// The item's split into query tiles and key tiles (as in extend_tc_kernel).
+// The item's split into query tiles and key tiles: query tile X holds
+// tokens X tpt .. X tpt + tok_X - 1 of the item and walks key tiles
+// 0 .. n_X - 1 (n_1 = 0 when it holds no token).
 struct ItemGeom {
   int tokens, n0, n1, n_tiles;
 };
@@ -1060,9 +675,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
-    // Per item, as in extend_tc_kernel: S_0(0), S_1(0), then per key tile j
-    // PV_0(j), S_0(j+1), PV_1(j), S_1(j+1) (in-order execution keeps P_X(j)
-    // until PV_X(j) has read it). Across items: the next item's S_X(0) may
+    // Per item: S_0(0), S_1(0), then per key tile j PV_0(j), S_0(j+1),
+    // PV_1(j), S_1(j+1). tcgen05.mma ops of one thread run in issue order, so
+    // S_X(j+1) overwrites P_X(j) only after PV_X(j) has read it, and a
+    // completed S_X(j+1) implies a completed PV_X(j) (O_X is then stable). Across items: the next item's S_X(0) may
     // run while softmax X writes the previous output (it only reads O_X);
     // its first PV_X waits until that output has been read out of O_X.
     if (lane == 0) {
@@ -1151,8 +767,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ------------------------------------------------------------ softmax
     // Query tile x = warp / 4; warp w owns TMEM lanes 32 (w % 4) .. + 31,
-    // one query row per thread, whole rows of S; per item as in
-    // extend_tc_kernel, then the item's output, then O_x is handed back.
+    // one query row per thread, whole rows of S; per item the key-tile loop,
+    // then the item's output, then O_x is handed back.
     const int quarter = warp & 3;
     const int x = warp >> 2;
     const int r = quarter * 32 + lane;  // query row == TMEM lane
@@ -1217,7 +833,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int cc = 0; cc < kN; ++cc) v[cc] = key0 + cc <= limit ? v[cc] : -INFINITY;
         }
-        // Row max of the raw scores; scale_log2 > 0 commutes with max.
+        // Row max of the raw scores; scale_log2 > 0 commutes with max (a
+        // negative or zero softmax scale was folded into Q, see q_mode).
         float mx0 = fmaxf(v[0], v[1]), mx1 = fmaxf(v[2], v[3]);
         float mx2 = fmaxf(v[4], v[5]), mx3 = fmaxf(v[6], v[7]);
 #pragma unroll
@@ -1228,7 +845,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           mx3 = max3f(mx3, v[cc + 6], v[cc + 7]);
         }
         const float mt = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * a.scale_log2;
-        // Lazy rescale (warp-uniform), as in extend_tc_kernel.
+        // Lazy rescale: move the reference max only when a row's max grew by
+        // more than 2^kRescaleThreshold (warp-uniform: tcgen05.ld/st are
+        // .sync.aligned, so every lane takes part, with factor 1 where its
+        // row did not move).
         const bool rescale = j > 0 && __any_sync(0xffffffffu, mt > m_used + kRescaleThreshold);
         float f = 1.f;
         if (j == 0) {
@@ -1351,9 +971,6 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-// A 2-D bf16 tensor of `rows` rows of `cols` elements (row-major), read in
-// boxes of box_rows rows x 64 columns with 128-byte swizzle (box_rows = 1 for
-// tile::gather4); zeros outside.
 // q [total_q][Hq][D] bf16 as a 3-D tensor, box {64, g, tpt}, 128-byte
 // swizzle; zeros outside.
 bool q3_map_of(CUtensorMap *m, const void *q, uint64_t total_q, uint64_t hq, uint64_t d,
@@ -1369,6 +986,8 @@ bool q3_map_of(CUtensorMap *m, const void *q, uint64_t total_q, uint64_t hq, uin
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// A 2-D bf16 tensor of `rows` rows of `cols` elements (row-major), read in
+// boxes of box_rows rows x 64 columns with 128-byte swizzle; zeros outside.
 bool bf16_map(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
   if (!enc) return false;
@@ -1459,19 +1078,16 @@ cudaError_t launch_extend(const PoolGeom &g, int32_t layer, const void *q,
   a.plan = ga.plan;
   CUtensorMap kv_map, q_map;
   if (!bf16_map(&kv_map, workspace, ws_rows, static_cast<uint64_t>(g.d), kN) ||
-      !(PKV_EXTEND_PERSISTENT
-            ? q3_map_of(&q_map, q, static_cast<uint64_t>(total_q), static_cast<uint64_t>(hq),
-                        static_cast<uint64_t>(g.d), static_cast<uint32_t>(a.group),
-                        static_cast<uint32_t>(a.tokens_per_tile))
-            : bf16_map(&q_map, q, q_rows, static_cast<uint64_t>(g.d), 1)))
+      !q3_map_of(&q_map, q, static_cast<uint64_t>(total_q), static_cast<uint64_t>(hq),
+                 static_cast<uint64_t>(g.d), static_cast<uint32_t>(a.group),
+                 static_cast<uint32_t>(a.tokens_per_tile)))
     return cudaErrorInvalidValue;
   const int64_t per_cta = static_cast<int64_t>(kQTiles) * a.tokens_per_tile;
   const int64_t tiles = (static_cast<int64_t>(total_q) + per_cta - 1) / per_cta + batch;
   if (tiles > 65535 || batch >= 65535) return cudaErrorInvalidConfiguration;
   // one gather CTA per 16 rows of a region, plus the planner
   const dim3 ggrid(static_cast<unsigned>(lay.cap_rows / kGatherKeys + 1));
-  const dim3 grid(g.hkv, static_cast<unsigned>(tiles));
-  // persistent form: one CTA per SM (whole-SM shared memory), at most one per work item
+  // attention: one CTA per SM (whole-SM shared memory), at most one per work item
   const int64_t items = static_cast<int64_t>(g.hkv) * tiles;
   const dim3 pgrid(static_cast<unsigned>(std::min<int64_t>(sm_count > 0 ? sm_count : 1, items)));
   cudaError_t e;
@@ -1481,38 +1097,22 @@ cudaError_t launch_extend(const PoolGeom &g, int32_t layer, const void *q,
                  : launch_pdl(extend_gather_kernel<128, false>, ggrid, dim3(kGatherThreads), 0,
                               stream, ga);
     if (e != cudaSuccess) return e;
-    if (PKV_EXTEND_PERSISTENT) {
-      e = cudaFuncSetAttribute(extend_tc_persistent_kernel<128>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, Smem<128>::kTotal);
-      if (e != cudaSuccess) return e;
-      e = launch_pdl(extend_tc_persistent_kernel<128>, pgrid, dim3(kThreads), Smem<128>::kTotal,
-                     stream, kv_map, q_map, a);
-    } else {
-      e = cudaFuncSetAttribute(extend_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               Smem<128>::kTotal);
-      if (e != cudaSuccess) return e;
-      e = launch_pdl(extend_tc_kernel<128>, grid, dim3(kThreads), Smem<128>::kTotal, stream,
-                     kv_map, q_map, a);
-    }
+    e = cudaFuncSetAttribute(extend_tc_persistent_kernel<128>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, Smem<128>::kTotal);
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(extend_tc_persistent_kernel<128>, pgrid, dim3(kThreads), Smem<128>::kTotal,
+                   stream, kv_map, q_map, a);
   } else {
     e = ga.k_new ? launch_pdl(extend_gather_kernel<64, true>, ggrid, dim3(kGatherThreads), 0,
                               stream, ga)
                  : launch_pdl(extend_gather_kernel<64, false>, ggrid, dim3(kGatherThreads), 0,
                               stream, ga);
     if (e != cudaSuccess) return e;
-    if (PKV_EXTEND_PERSISTENT) {
-      e = cudaFuncSetAttribute(extend_tc_persistent_kernel<64>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, Smem<64>::kTotal);
-      if (e != cudaSuccess) return e;
-      e = launch_pdl(extend_tc_persistent_kernel<64>, pgrid, dim3(kThreads), Smem<64>::kTotal,
-                     stream, kv_map, q_map, a);
-    } else {
-      e = cudaFuncSetAttribute(extend_tc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               Smem<64>::kTotal);
-      if (e != cudaSuccess) return e;
-      e = launch_pdl(extend_tc_kernel<64>, grid, dim3(kThreads), Smem<64>::kTotal, stream,
-                     kv_map, q_map, a);
-    }
+    e = cudaFuncSetAttribute(extend_tc_persistent_kernel<64>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, Smem<64>::kTotal);
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(extend_tc_persistent_kernel<64>, pgrid, dim3(kThreads), Smem<64>::kTotal,
+                   stream, kv_map, q_map, a);
   }
   return e;
 }

@@ -251,19 +251,6 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                : "memory");
 }
 
-// TMA gather: rows y0..y3 of a 2-D tensor (box {width, 1}), columns x ..
-// x + width - 1, into shared memory at dst (4 consecutive 128-byte rows with
-// the map's swizzle); out-of-range rows (e.g. -1) read zeros. Completion
-// counts 4 * width * 2 bytes down on `bar`.
-__device__ __forceinline__ void tma_gather4(uint32_t dst, const void *tmap, int x, int y0, int y1,
-                                            int y2, int y3, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(bar)
-      : "memory");
-}
-
 // TMA tile load: the box at column x, row y of a 2-D tensor into shared
 // memory at dst (box rows of 128 bytes with the map's swizzle). Completion
 // counts the box's bytes down on `bar`.
