@@ -59,13 +59,13 @@ MEASURED_TRAFFIC = {
                "bytes": 625499392},
     # extend_gather_kernel + extend_tc_persistent_kernel, chunked-prefill extend
     "extend": {"sources": ['extend.cu', 'tc_common.cuh', 'pkv_common.cuh'],
-               "sha256": "50dcb48e70dfd0686d70537f8678bbe99f6fc0c3a5517244ecd49be58ae7eb7f",
-               "bytes": 518785792},
+               "sha256": "b1a3c110649ba479087f66519171d1c044555dd64fe1984fad7b85664fdda528",
+               "bytes": 517911744},
     # cascade_prefix_kernel + decode_kernel (suffix) + decode_merge_narrow_kernel,
     # radix-shared decode through cascade decode
     "cascade": {"sources": ['cascade.cu', 'decode.cu', 'decode_common.cuh', 'tc_common.cuh', 'pkv_common.cuh'],
-                "sha256": "7e12b981d9f98340b348997b9fb639f09932307628285b59d7298fa2e42cbb2a",
-                "bytes": 372238272},
+                "sha256": "95269f4003f1cf0b7468f12db3d333a8acedc0066950197a33cf5c40428bfdcc",
+                "bytes": 372222432},
 }
 
 
