@@ -430,26 +430,30 @@ __global__ void __launch_bounds__(kThreads, 1) cascade_prefix_kernel(const Prefi
     for (int j = 0; j < n_tiles; ++j) {
       if (!(ok = mbar_wait_warp(bar(kBarSFull), j & 1, abort))) break;
       tc_fence_after_sync();
-      float v[kN];
-      tmem_ld32(srow + 0, *reinterpret_cast<float(*)[32]>(&v[0]));
-      tmem_ld32(srow + 32, *reinterpret_cast<float(*)[32]>(&v[32]));
-      tmem_ld32(srow + 64, *reinterpret_cast<float(*)[32]>(&v[64]));
-      tmem_ld32(srow + 96, *reinterpret_cast<float(*)[32]>(&v[96]));
+      // Row max of the raw scores; scale_log2 > 0 commutes with max. The
+      // loads return the max of the columns they read; the tile holding the
+      // prefix's last key (CTA-uniform) takes the max after the mask.
+      float v[kN], mx0, mx1, mx2, mx3;
+      tmem_ld32_max(srow + 0, *reinterpret_cast<float(*)[32]>(&v[0]), mx0);
+      tmem_ld32_max(srow + 32, *reinterpret_cast<float(*)[32]>(&v[32]), mx1);
+      tmem_ld32_max(srow + 64, *reinterpret_cast<float(*)[32]>(&v[64]), mx2);
+      tmem_ld32_max(srow + 96, *reinterpret_cast<float(*)[32]>(&v[96]), mx3);
       tmem_ld_wait();
       const int key0 = (tile0 + j) * kN;
-      if (key0 + kN > plen) {  // the tile holding the prefix's last key (CTA-uniform)
+      if (key0 + kN > plen) {
 #pragma unroll
         for (int cc = 0; cc < kN; ++cc) v[cc] = key0 + cc < plen ? v[cc] : -INFINITY;
-      }
-      // Row max of the raw scores; scale_log2 > 0 commutes with max.
-      float mx0 = fmaxf(v[0], v[1]), mx1 = fmaxf(v[2], v[3]);
-      float mx2 = fmaxf(v[4], v[5]), mx3 = fmaxf(v[6], v[7]);
+        mx0 = fmaxf(v[0], v[1]);
+        mx1 = fmaxf(v[2], v[3]);
+        mx2 = fmaxf(v[4], v[5]);
+        mx3 = fmaxf(v[6], v[7]);
 #pragma unroll
-      for (int cc = 8; cc < kN; cc += 8) {
-        mx0 = max3f(mx0, v[cc], v[cc + 1]);
-        mx1 = max3f(mx1, v[cc + 2], v[cc + 3]);
-        mx2 = max3f(mx2, v[cc + 4], v[cc + 5]);
-        mx3 = max3f(mx3, v[cc + 6], v[cc + 7]);
+        for (int cc = 8; cc < kN; cc += 8) {
+          mx0 = max3f(mx0, v[cc], v[cc + 1]);
+          mx1 = max3f(mx1, v[cc + 2], v[cc + 3]);
+          mx2 = max3f(mx2, v[cc + 4], v[cc + 5]);
+          mx3 = max3f(mx3, v[cc + 6], v[cc + 7]);
+        }
       }
       const float mt = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * a.scale_log2;
       // Lazy rescale: move the reference max only when some row's max grew

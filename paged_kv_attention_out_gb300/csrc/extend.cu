@@ -14,8 +14,10 @@
 //       request order, [2][Hkv][cap_rows][D], so the workspace is sized by the
 //       keys present (a host bound on their sum), not by batch x max length;
 //       one CTA per 16 rows of that space, each finding its request by a
-//       prefix sum of the rounded lengths; the last CTA builds the block
-//       schedule;
+//       prefix sum of the rounded lengths; the first CTA builds the block
+//       schedule meanwhile; pool rows are read with an L2 evict-first
+//       policy and the workspace rows written with evict-last, since the
+//       attention reads them right after;
 //   extend_tc_persistent_kernel  the attention, which then reads every
 //       128-key K or V tile with plain 2-D TMA boxes instead of row gathers;
 //       one CTA per SM takes blocks of the schedule as work items.
@@ -332,19 +334,41 @@ __global__ void __launch_bounds__(kGatherThreads)
   gather_body<D, kStore>(a);
 }
 
+// Read-only 16-byte load / 16-byte store with an L2 eviction-priority
+// policy (createpolicy): the pool rows are read once per call (evict first),
+// the workspace rows are read again by the attention right after (evict last).
+__device__ __forceinline__ uint4 ldg_nc_hint(const uint4 *p, uint64_t policy) {
+  uint4 v;
+  asm volatile("ld.global.nc.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p), "l"(policy));
+  return v;
+}
+__device__ __forceinline__ void st_hint(uint4 *p, uint4 v, uint64_t policy) {
+  asm volatile("st.global.L2::cache_hint.v4.u32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p), "r"(v.x),
+               "r"(v.y), "r"(v.z), "r"(v.w), "l"(policy)
+               : "memory");
+}
+__device__ __forceinline__ uint64_t l2_evict_last_policy() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
 template <int D, bool kStore>
 __device__ __forceinline__ void gather_body(const GatherArgs &a) {
-  if (blockIdx.x == gridDim.x - 1) {  // the last CTA: the planner
+  if (blockIdx.x == 0) {  // the first CTA: the planner, dispatched before the gather CTAs
     plan_blocks(a);
     return;
   }
+  const int gblock = static_cast<int>(blockIdx.x) - 1;
   // The request whose run holds this CTA's 16 rows (runs are multiples of
   // 128 rows, so they never straddle two requests): the same scan of the
   // rounded lengths as the planner's, kGatherThreads requests per round.
   __shared__ int64_t s_warp[kGatherThreads / 32];
   __shared__ int s_r;
   __shared__ int64_t s_off;
-  const int64_t pos = static_cast<int64_t>(blockIdx.x) * kGatherKeys;
+  const int64_t pos = static_cast<int64_t>(gblock) * kGatherKeys;
   if (threadIdx.x == 0) s_r = -1;
   int64_t run_base = 0;
   for (int r0 = 0; r0 < a.batch; r0 += kGatherThreads) {
@@ -368,7 +392,7 @@ __device__ __forceinline__ void gather_body(const GatherArgs &a) {
   const int key0 = static_cast<int>(pos - off);
   const int row = a.table_idx ? a.table_idx[r] : r;
   if (row < 0) {
-    if (blockIdx.x == 0 && threadIdx.x == 0) flag_error(a.err, kErrTableIdx);
+    if (key0 == 0 && threadIdx.x == 0) flag_error(a.err, kErrTableIdx);  // once per request
     return;
   }
   const int32_t *row_pages = a.page_table + static_cast<int64_t>(row) * a.table_stride;
@@ -394,6 +418,8 @@ __device__ __forceinline__ void gather_body(const GatherArgs &a) {
   const int64_t run_elems = static_cast<int64_t>(a.cap_rows) * D;  // one kv head's region
   const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
   constexpr int kUnroll = 4;  // chunks per lane per row in flight (x 2 rows)
+  const uint64_t pol_read = l2_evict_first_policy();
+  const uint64_t pol_write = l2_evict_last_policy();
   for (int kk = warp; kk < kGatherKeys; kk += kGatherThreads / 32) {
     const int key = key0 + kk;
     // the key's K row (c = 0) and V row (c = 1) are copied together
@@ -429,7 +455,7 @@ __device__ __forceinline__ void gather_body(const GatherArgs &a) {
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
           const int ch = ch0 + 32 * u;
-          v[c][u] = (src[c] != nullptr && ch < nch) ? __ldg(src[c] + ch) : zero;
+          v[c][u] = (src[c] != nullptr && ch < nch) ? ldg_nc_hint(src[c] + ch, pol_read) : zero;
         }
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
@@ -439,8 +465,8 @@ __device__ __forceinline__ void gather_body(const GatherArgs &a) {
         for (int u = 0; u < kUnroll; ++u) {
           const int ch = ch0 + 32 * u;
           if (ch < nch) {
-            *reinterpret_cast<uint4 *>(dst + (ch / kChunks) * run_elems + (ch % kChunks) * 8) =
-                v[c][u];
+            st_hint(reinterpret_cast<uint4 *>(dst + (ch / kChunks) * run_elems + (ch % kChunks) * 8),
+                    v[c][u], pol_write);
             if (kStore && store[c] != nullptr) store[c][ch] = v[c][u];
           }
         }
