@@ -350,20 +350,19 @@ __device__ __forceinline__ float max3f(float x, float y, float z) {
   return r;
 }
 
-// (y0, y1) = (x0, x1) * s + c, one packed fp32 instruction.
+// (y0, y1) = (x0, x1) * s + c, one packed fp32 instruction (the compiler's
+// own float2 builtin, so it pairs the registers and hoists the broadcasts).
 __device__ __forceinline__ void fma2(float &y0, float &y1, float x0, float x1, float s, float c) {
-  asm("{\n .reg .b64 x, m, a, y;\n mov.b64 x, {%2, %3};\n mov.b64 m, {%4, %4};\n"
-      " mov.b64 a, {%5, %5};\n fma.rn.f32x2 y, x, m, a;\n mov.b64 {%0, %1}, y;\n}"
-      : "=f"(y0), "=f"(y1)
-      : "f"(x0), "f"(x1), "f"(s), "f"(c));
+  const float2 r = __ffma2_rn(make_float2(x0, x1), make_float2(s, s), make_float2(c, c));
+  y0 = r.x;
+  y1 = r.y;
 }
 
 // (s0, s1) += (x0, x1), one packed fp32 instruction.
 __device__ __forceinline__ void add2(float &s0, float &s1, float x0, float x1) {
-  asm("{\n .reg .b64 s, x;\n mov.b64 s, {%0, %1};\n mov.b64 x, {%2, %3};\n"
-      " add.rn.f32x2 s, s, x;\n mov.b64 {%0, %1}, s;\n}"
-      : "+f"(s0), "+f"(s1)
-      : "f"(x0), "f"(x1));
+  const float2 r = __fadd2_rn(make_float2(s0, s1), make_float2(x0, x1));
+  s0 = r.x;
+  s1 = r.y;
 }
 
 }  // namespace pkv
