@@ -59,13 +59,13 @@ MEASURED_TRAFFIC = {
                "bytes": 625499392},
     # extend_gather_kernel + extend_tc_persistent_kernel, chunked-prefill extend
     "extend": {"sources": ['extend.cu', 'tc_common.cuh', 'pkv_common.cuh'],
-               "sha256": "b1a3c110649ba479087f66519171d1c044555dd64fe1984fad7b85664fdda528",
-               "bytes": 517911744},
+               "sha256": "1eb5c6aba3397722b47b05ccd3b89545eb05eee3ed26aa57c8e37cdef8804cde",
+               "bytes": 488397696},
     # cascade_prefix_kernel + decode_kernel (suffix) + decode_merge_narrow_kernel,
     # radix-shared decode through cascade decode
     "cascade": {"sources": ['cascade.cu', 'decode.cu', 'decode_common.cuh', 'tc_common.cuh', 'pkv_common.cuh'],
-                "sha256": "95269f4003f1cf0b7468f12db3d333a8acedc0066950197a33cf5c40428bfdcc",
-                "bytes": 372222432},
+                "sha256": "3e5d0f458ab7b66880974acc5521cb2eb68108f6736d1a82d0963b3ff761b592",
+                "bytes": 372296352},
 }
 
 

@@ -13,7 +13,7 @@ from paged_kv_attention_out_gb300 import workloads as W
 
 pytestmark = pytest.mark.gpu
 
-PAGE, SEQ, INDPTR = 0x2, 0x4, 0x8
+PAGE, SEQ, INDPTR, TABLE_IDX = 0x2, 0x4, 0x8, 0x10
 
 
 def _errors():
@@ -111,6 +111,33 @@ def test_extend_request_longer_than_the_length_hint_is_still_computed():
     assert _errors() == 0
     want, _, _ = oracle_run(case)
     compare(o.float().cpu().double().numpy(), want)
+
+
+def test_extend_negative_table_idx_is_flagged():
+    """A negative table_idx entry of a request other than the first (whose
+    keys start in a later gather CTA) is reported; the other requests are
+    computed as usual."""
+    import paged_kv_attention_out_gb300 as pkv
+    case = W.random_case(37, kind="extend", seq_lens=[100, 300, 200, 50],
+                         chunk_lens=[30, 64, 40, 50], Hq=8, Hkv=2, D=128, P=16,
+                         use_table_idx=True)
+    pool, k, v, q, t = gpu_inputs(case)
+    pkv.pkv_kv_store(pool, case.layer, k, v, t["out_loc"])
+    ti = t["table_idx"].clone()
+    ti[2] = -3
+    h = case.max_seq_len
+    ws = torch.empty(pkv.pkv_extend_workspace_size(case.B, case.Hkv, case.D, h),
+                     dtype=torch.uint8, device="cuda")
+    o = torch.full_like(q, float("nan"))
+    _errors()
+    pkv.pkv_paged_extend_attn(pool, case.layer, q, t["qo_indptr"], o, None, t["page_table"],
+                              t["seq_lens"], case.scale, h, ws, table_idx=ti)
+    assert _errors() & TABLE_IDX
+    want, _, _ = oracle_run(case)
+    got = o.float().cpu().double().numpy()
+    qo = case.qo_indptr
+    ok = np.r_[qo[0]:qo[2], qo[3]:qo[4]]  # requests 0, 1 and 3
+    compare(got[ok], want[ok])
 
 
 def test_extend_malformed_qo_indptr_is_flagged():
