@@ -148,7 +148,8 @@ struct ExtendArgs {
   int32_t *plan;  // the persistent form takes its work items from plan[1]
 };
 
-constexpr int kGatherKeys = 16;     // keys per gather CTA (two per warp)
+constexpr int kGatherKeys = 16;     // keys per chunk of a gather CTA (two per warp)
+constexpr int kGatherWaves = 2;     // copying CTAs: this many waves of resident CTAs
 constexpr int kGatherThreads = 256;
 
 // Workspace run of request r, kv head h, K (c = 0) or V (c = 1): the
@@ -325,6 +326,8 @@ __device__ void plan_blocks(const GatherArgs &a) {
 // the plain gather keeps its lean inner loop.
 template <int D, bool kStore>
 __device__ __forceinline__ void gather_body(const GatherArgs &a);
+template <int D, bool kStore>
+__device__ __forceinline__ bool gather_rows(const GatherArgs &a, int64_t pos);
 
 template <int D, bool kStore>
 __global__ void __launch_bounds__(kGatherThreads)
@@ -355,20 +358,31 @@ __device__ __forceinline__ uint64_t l2_evict_last_policy() {
   return p;
 }
 
+// The first CTA builds the schedule (dispatched before the copying CTAs);
+// the others copy 16-row chunks of the key space, chunk c by CTA 1 + c mod
+// (grid - 1), so a grid of whole waves finishes together.
 template <int D, bool kStore>
 __device__ __forceinline__ void gather_body(const GatherArgs &a) {
-  if (blockIdx.x == 0) {  // the first CTA: the planner, dispatched before the gather CTAs
+  if (blockIdx.x == 0) {
     plan_blocks(a);
     return;
   }
-  const int gblock = static_cast<int>(blockIdx.x) - 1;
-  // The request whose run holds this CTA's 16 rows (runs are multiples of
-  // 128 rows, so they never straddle two requests): the same scan of the
+  const int64_t chunks = a.cap_rows / kGatherKeys;
+  for (int64_t c = blockIdx.x - 1; c < chunks; c += gridDim.x - 1)
+    if (!gather_rows<D, kStore>(a, c * kGatherKeys)) break;
+}
+
+// Copies rows pos .. pos + 15 of the key space. Returns false once pos lies
+// past every run (so does every later chunk).
+template <int D, bool kStore>
+__device__ __forceinline__ bool gather_rows(const GatherArgs &a, int64_t pos) {
+  // The request whose run holds these 16 rows (runs are multiples of 128
+  // rows, so they never straddle two requests): the same scan of the
   // rounded lengths as the planner's, kGatherThreads requests per round.
   __shared__ int64_t s_warp[kGatherThreads / 32];
   __shared__ int s_r;
   __shared__ int64_t s_off;
-  const int64_t pos = static_cast<int64_t>(gblock) * kGatherKeys;
+  __syncthreads();  // the previous chunk's s_r / s_off are read
   if (threadIdx.x == 0) s_r = -1;
   int64_t run_base = 0;
   for (int r0 = 0; r0 < a.batch; r0 += kGatherThreads) {
@@ -385,15 +399,15 @@ __device__ __forceinline__ void gather_body(const GatherArgs &a) {
   }
   __syncthreads();
   const int r = s_r;
-  if (r < 0) return;  // past the last run
+  if (r < 0) return false;  // past the last run
   const int64_t off = s_off;
   const int seq = a.seq_lens[r];
-  if (off + run_rows(a, seq) > a.cap_rows) return;  // past the key bound (flagged by the planner)
+  if (off + run_rows(a, seq) > a.cap_rows) return false;  // past the key bound (flagged by the planner)
   const int key0 = static_cast<int>(pos - off);
   const int row = a.table_idx ? a.table_idx[r] : r;
   if (row < 0) {
     if (key0 == 0 && threadIdx.x == 0) flag_error(a.err, kErrTableIdx);  // once per request
-    return;
+    return true;
   }
   const int32_t *row_pages = a.page_table + static_cast<int64_t>(row) * a.table_stride;
   // Fused store: keys from new_key0 on are the chunk's, key k is row
@@ -473,6 +487,20 @@ __device__ __forceinline__ void gather_body(const GatherArgs &a) {
       }
     }
   }
+  return true;
+}
+
+// TMA tile load (as tma_load_2d) with an L2 eviction-priority policy
+// (createpolicy): the K/V workspace tiles are read again by every block of
+// their request, so they are kept (evict last) ahead of Q and O, which are
+// touched once.
+__device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const void *tmap, int x, int y,
+                                                 uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(bar), "l"(policy)
+      : "memory");
 }
 
 // ------------------------------------------------------------ attention
@@ -620,6 +648,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // the CTA into stage g % 2 once every MMA reading that stage (tile
     // g - 2) is done. Lane 0 issues the loads.
     constexpr int kHalves = D / 64;
+    const uint64_t kv_policy = l2_evict_last_policy();
     const int total_items = a.hkv * a.plan[0];
     const int *sorted = a.plan + plan_sorted(a.nbuck, a.max_blocks);
     const int *offs = a.plan + plan_offsets(a.nbuck, a.max_blocks);
@@ -681,9 +710,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive_expect_tx(bar(kPBarFull + st), 2 * S::kTileBytes);
 #pragma unroll
           for (int h = 0; h < kHalves; ++h) {
-            tma_load_2d(dst + h * (kN * 128), &kv_map, h * 64, k_run + j * kN, bar(kPBarFull + st));
-            tma_load_2d(dst + S::kTileBytes + h * (kN * 128), &kv_map, h * 64, v_run + j * kN,
-                        bar(kPBarFull + st));
+            tma_load_2d_hint(dst + h * (kN * 128), &kv_map, h * 64, k_run + j * kN,
+                             bar(kPBarFull + st), kv_policy);
+            tma_load_2d_hint(dst + S::kTileBytes + h * (kN * 128), &kv_map, h * 64,
+                             v_run + j * kN, bar(kPBarFull + st), kv_policy);
           }
         }
         __syncwarp();
@@ -987,6 +1017,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// Copying CTAs of one gather variant resident on an SM at once (looked up
+// once per variant).
+template <int D, bool kStore>
+int gather_ctas_per_sm() {
+  static const int n = [] {
+    int b = 0;
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, extend_gather_kernel<D, kStore>,
+                                                         kGatherThreads, 0) == cudaSuccess &&
+                   b > 0
+               ? b
+               : 1;
+  }();
+  return n;
+}
+
 // cuTensorMapEncodeTiled from the driver, looked up once per process.
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -1116,8 +1161,14 @@ cudaError_t launch_extend(const PoolGeom &g, int32_t layer, const void *q,
   const int64_t per_cta = static_cast<int64_t>(kQTiles) * a.tokens_per_tile;
   const int64_t tiles = (static_cast<int64_t>(total_q) + per_cta - 1) / per_cta + batch;
   if (tiles > 65535 || batch >= 65535) return cudaErrorInvalidConfiguration;
-  // one gather CTA per 16 rows of a region, plus the planner
-  const dim3 ggrid(static_cast<unsigned>(lay.cap_rows / kGatherKeys + 1));
+  // the planner, then two waves of copying CTAs (twice as many as are
+  // resident at once) looping over the 16-row chunks
+  const int64_t chunks = lay.cap_rows / kGatherKeys;
+  const int per_sm = g.d == 128 ? (ga.k_new ? gather_ctas_per_sm<128, true>() : gather_ctas_per_sm<128, false>())
+                                : (ga.k_new ? gather_ctas_per_sm<64, true>() : gather_ctas_per_sm<64, false>());
+  const int64_t copiers = std::min<int64_t>(
+      chunks, static_cast<int64_t>(sm_count > 0 ? sm_count : 1) * per_sm * kGatherWaves);
+  const dim3 ggrid(static_cast<unsigned>(1 + copiers));
   // attention: one CTA per SM (whole-SM shared memory), at most one per work item
   const int64_t items = static_cast<int64_t>(g.hkv) * tiles;
   const dim3 pgrid(static_cast<unsigned>(std::min<int64_t>(sm_count > 0 ? sm_count : 1, items)));
