@@ -59,8 +59,8 @@ MEASURED_TRAFFIC = {
                "bytes": 625499392},
     # extend_gather_kernel + extend_tc_persistent_kernel, chunked-prefill extend
     "extend": {"sources": ['extend.cu', 'tc_common.cuh', 'pkv_common.cuh'],
-               "sha256": "1eb5c6aba3397722b47b05ccd3b89545eb05eee3ed26aa57c8e37cdef8804cde",
-               "bytes": 488397696},
+               "sha256": "7ca968108dc2e5ad8b56438e2a787c67b914a5ea0617d6de8b334e8ff416a222",
+               "bytes": 492203584},
     # cascade_prefix_kernel + decode_kernel (suffix) + decode_merge_narrow_kernel,
     # radix-shared decode through cascade decode
     "cascade": {"sources": ['cascade.cu', 'decode.cu', 'decode_common.cuh', 'tc_common.cuh', 'pkv_common.cuh'],
