@@ -13,11 +13,11 @@
 //       the pool once per call. The runs of the requests lie back to back in
 //       request order, [2][Hkv][cap_rows][D], so the workspace is sized by the
 //       keys present (a host bound on their sum), not by batch x max length;
-//       one CTA per 16 rows of that space, each finding its request by a
-//       prefix sum of the rounded lengths; the first CTA builds the block
-//       schedule meanwhile; pool rows are read with an L2 evict-first
-//       policy and the workspace rows written with evict-last, since the
-//       attention reads them right after;
+//       two waves of resident CTAs loop over 16-row chunks of that space,
+//       finding each chunk's request by a prefix sum of the rounded lengths;
+//       the first CTA builds the block schedule meanwhile; pool rows are
+//       read with an L2 evict-first policy and the workspace rows written
+//       with evict-last, since the attention reads them right after;
 //   extend_tc_persistent_kernel  the attention, which then reads every
 //       128-key K or V tile with plain 2-D TMA boxes instead of row gathers;
 //       one CTA per SM takes blocks of the schedule as work items.
