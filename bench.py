@@ -59,8 +59,8 @@ MEASURED_TRAFFIC = {
                "bytes": 625499392},
     # extend_gather_kernel + extend_tc_persistent_kernel, chunked-prefill extend
     "extend": {"sources": ['extend.cu', 'tc_common.cuh', 'pkv_common.cuh'],
-               "sha256": "7ca968108dc2e5ad8b56438e2a787c67b914a5ea0617d6de8b334e8ff416a222",
-               "bytes": 492203584},
+               "sha256": "603ff433c0bcf92b10475c79a715087cc51e548d1834ee93f00ce253edbfd45c",
+               "bytes": 489539904},
     # cascade_prefix_kernel + decode_kernel (suffix) + decode_merge_narrow_kernel,
     # radix-shared decode through cascade decode
     "cascade": {"sources": ['cascade.cu', 'decode.cu', 'decode_common.cuh', 'tc_common.cuh', 'pkv_common.cuh'],
